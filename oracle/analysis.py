@@ -1,0 +1,121 @@
+"""Closed forms for the SANTA / S2ANTA estimators (float64, numpy).
+
+TEST INFRASTRUCTURE ONLY.  These formulas come from "Stochastic Sparse
+Attention for Memory-Bound Inference":
+
+* mean of every variant is the exact attention output mu = sum_n p_n V_n
+  (App. A, Prop. A.2 and A.4);
+* i.i.d. covariance trace tr(Sigma)/S with
+  tr(Sigma) = sum_n p_n |V_n|^2 - |mu|^2 (App. A.2, Prop. A.3; App. M);
+* independent stratified variance trace (1/S^2) sum_m tr(Sigma_m), Sigma_m
+  the value covariance of the within-stratum distribution (App. A.5,
+  Thm. A.6; App. M);
+* systematic variance by replicates (App. M) -- no closed form exists;
+* vector Bernstein tail for i.i.d. SANTA (App. B, Thm. B.1).
+
+Strata follow Sec. 2.1: I_m = [m/S, (m+1)/S), with the inverse CDF of App. A.4.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+
+def cdf(p: np.ndarray) -> np.ndarray:
+    return np.cumsum(np.asarray(p, dtype=np.float64))
+
+
+def exact_mean(p: np.ndarray, V: np.ndarray) -> np.ndarray:
+    return np.asarray(p, np.float64) @ np.asarray(V, np.float64)
+
+
+def iid_variance_trace(p: np.ndarray, V: np.ndarray, S: int) -> float:
+    V = np.asarray(V, np.float64)
+    mu = exact_mean(p, V)
+    tr = float(np.dot(p, np.einsum("nd,nd->n", V, V)) - mu @ mu)
+    return tr / S
+
+
+def iid_coordinate_variance(p: np.ndarray, V: np.ndarray, S: int) -> np.ndarray:
+    """Diagonal of Sigma / S (per output coordinate)."""
+    V = np.asarray(V, np.float64)
+    mu = exact_mean(p, V)
+    return (np.asarray(p) @ (V * V) - mu * mu) / S
+
+
+def stratum_weights(p: np.ndarray, S: int) -> np.ndarray:
+    """w[m, n] = S * |I_m intersect [F(n-1), F(n))| : the distribution of
+    F^-1(T) for T uniform on stratum I_m (rows sum to 1)."""
+    F = cdf(p)
+    Fl = np.concatenate([[0.0], F[:-1]])
+    m = np.arange(S, dtype=np.float64)
+    lo = np.maximum(Fl[None, :], (m / S)[:, None])
+    hi = np.minimum(F[None, :], ((m + 1) / S)[:, None])
+    return S * np.clip(hi - lo, 0.0, None)
+
+
+def stratified_mean(p: np.ndarray, V: np.ndarray, S: int) -> np.ndarray:
+    w = stratum_weights(p, S)
+    return (w @ np.asarray(V, np.float64)).sum(axis=0) / S
+
+
+def stratified_variance_trace(p: np.ndarray, V: np.ndarray, S: int) -> float:
+    V = np.asarray(V, np.float64)
+    w = stratum_weights(p, S)
+    mu_m = w @ V                                   # [S, d]
+    second = w @ np.einsum("nd,nd->n", V, V)       # [S]
+    tr_m = second - np.einsum("md,md->m", mu_m, mu_m)
+    return float(tr_m.sum()) / (S * S)
+
+
+def stratified_coordinate_variance(p: np.ndarray, V: np.ndarray, S: int) -> np.ndarray:
+    V = np.asarray(V, np.float64)
+    w = stratum_weights(p, S)
+    mu_m = w @ V
+    var_m = w @ (V * V) - mu_m * mu_m
+    return var_m.sum(axis=0) / (S * S)
+
+
+def systematic_breakpoints(p: np.ndarray, S: int) -> np.ndarray:
+    """Offsets u in [0,1) at which some systematic threshold (j+u)/S crosses a
+    CDF edge F(n): u = S F(n) - j.  Between consecutive breakpoints the
+    systematic sample is constant."""
+    F = cdf(p)
+    u = (S * F)[:, None] - np.arange(S)[None, :]
+    u = u[(u > 0.0) & (u < 1.0)]
+    return np.unique(np.concatenate([[0.0, 1.0], u]))
+
+
+def expectation_over_offset(estimator, breakpoints: np.ndarray) -> np.ndarray:
+    """Exact integral over u in [0,1) of a piecewise-constant estimator(u):
+    sum over the pieces of (length * value at the midpoint)."""
+    total = None
+    for a, b in zip(breakpoints[:-1], breakpoints[1:]):
+        if b <= a:
+            continue
+        val = np.asarray(estimator(0.5 * (a + b)), np.float64) * (b - a)
+        total = val if total is None else total + val
+    return total
+
+
+def replicate_variance_trace(estimates: np.ndarray) -> float:
+    """App. M replicate estimator: (1/(R-1)) sum_r |est_r - mean|^2."""
+    E = np.asarray(estimates, np.float64)
+    R = E.shape[0]
+    c = E - E.mean(axis=0, keepdims=True)
+    return float(np.einsum("rd,rd->", c, c)) / (R - 1)
+
+
+def bernstein_radius(v: float, vmax: float, S: int, delta: float) -> float:
+    """App. B: with probability >= 1 - delta the i.i.d. error norm is below
+    sqrt(2 v log(2/delta) / S) + 2 vmax log(2/delta) / (3 S)."""
+    L = math.log(2.0 / delta)
+    return math.sqrt(2.0 * v * L / S) + 2.0 * vmax * L / (3.0 * S)
+
+
+def systematic_count_bounds(p: np.ndarray, S: int):
+    """Each key's systematic count lies in {floor(S p_n), ceil(S p_n)}
+    (lattice points of spacing 1/S in an interval of length p_n)."""
+    Sp = S * np.asarray(p, np.float64)
+    return np.floor(Sp), np.ceil(Sp)

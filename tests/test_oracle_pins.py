@@ -1,0 +1,374 @@
+"""Pins for the CPU oracle: each check ties it to something other than itself.
+
+Sources ("Stochastic Sparse Attention for Memory-Bound Inference"):
+worked example Sec. 1 Eq. (2)-(3); SDPA Sec. 2 Eq. (1); estimators Eq. (4)
+and Sec. 2.1; inverse CDF App. A.4; unbiasedness Prop. A.2 / A.4; variance
+Prop. A.3, Thm. A.6, App. M; Bernstein tail App. B Thm. B.1.  The Philox
+stream is pinned against PyTorch's header-only engine (an independent
+implementation of Salmon et al., SC'11).
+"""
+import ctypes
+import json
+import os
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import analysis
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def make_problem(oracle, q, K, V, scale=0.0, dtype="fp32"):
+    """Single-sequence fp32 problem from float arrays: q [H,d], K/V [nk,Hkv,d]."""
+    q = np.asarray(q, np.float32)
+    K = np.asarray(K, np.float32)
+    V = np.asarray(V, np.float32)
+    if q.ndim == 2:
+        q = q[None]
+    offs = np.array([0, K.shape[0]], np.int64)
+    return oracle.Problem(q, K, V, offs, dtype, K.shape[1], scale)
+
+
+def problem_from_probs(oracle, p, V):
+    """nk keys whose softmax is (numerically) p: q = e0, K_n = log(p_n) e0, scale 1."""
+    p = np.asarray(p, np.float64)
+    V = np.asarray(V, np.float32)
+    nk, d = V.shape
+    q = np.zeros((1, max(d, 1)), np.float32)
+    q[0, 0] = 1.0
+    K = np.zeros((nk, 1, d), np.float32)
+    K[:, 0, 0] = np.log(p).astype(np.float32)
+    return make_problem(oracle, q, K, V[:, None, :], scale=1.0)
+
+
+def random_problem(oracle, rng, nk, d, H=1, Hkv=1, spread=2.0):
+    q = rng.standard_normal((H, d)).astype(np.float32) * np.float32(spread)
+    K = rng.standard_normal((nk, Hkv, d)).astype(np.float32)
+    V = rng.standard_normal((nk, Hkv, d)).astype(np.float32)
+    return make_problem(oracle, q, K, V)
+
+
+def values_of(P, b, h):
+    """V rows of head (b, h) as float64 [nk, d] (storage is fp32 here)."""
+    B, H, Hkv, d = P.shape
+    kvh = h // (H // Hkv)
+    off = P.kv_offsets
+    return synth.storage_to_f64(P.V[off[b]:off[b + 1], kvh], P.dtype)
+
+
+@pytest.fixture(scope="module")
+def torch_philox(tmp_path_factory):
+    inc = os.path.join(os.path.dirname(torch.__file__), "include")
+    out = tmp_path_factory.mktemp("philox") / "libtorch_philox.so"
+    subprocess.run(["g++", "-std=c++17", "-O1", "-shared", "-fPIC", "-I", inc,
+                    os.path.join(HERE, "philox_torch_shim.cpp"), "-o", str(out)], check=True)
+    lib = ctypes.CDLL(str(out))
+    lib.torch_philox_block.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
+                                       ctypes.c_void_p]
+
+    def block(seed, subsequence, offset):
+        w = np.zeros(4, np.uint32)
+        lib.torch_philox_block(seed, subsequence, offset, w.ctypes.data_as(ctypes.c_void_p))
+        return w
+    return block
+
+
+# ---------------------------------------------------------------------------
+# Philox stream and uniform map
+# ---------------------------------------------------------------------------
+
+def test_philox_words_match_torch_engine(oracle_lib, torch_philox):
+    """counter (i, h, b, step), key (seed_lo, seed_hi) == torch engine with
+    subsequence = step<<32 | b and offset = h<<32 | i."""
+    rng = np.random.default_rng(1)
+    cases = [(0, 0, 0, 0, 0), (0xFFFFFFFFFFFFFFFF, 7, 31, 5, 3), (123456789, 63, 27, 1 << 20, 1023)]
+    for _ in range(200):
+        cases.append((int(rng.integers(0, 2**63)), int(rng.integers(0, 64)), int(rng.integers(0, 64)),
+                      int(rng.integers(0, 2**32)), int(rng.integers(0, 4096))))
+    for seed, b, h, step, i in cases:
+        ours = oracle_lib.philox4x32_10([i, h, b, step], [seed & 0xFFFFFFFF, seed >> 32])
+        ref = torch_philox(seed, (step << 32) | b, (h << 32) | i)
+        np.testing.assert_array_equal(ours, ref)
+
+
+def test_uniform_map_and_threshold_layout(oracle_lib, torch_philox):
+    seed, b, h, step, S = 99, 3, 5, 7, 37
+    words = np.concatenate([torch_philox(seed, (step << 32) | b, (h << 32) | i) for i in range((S + 3) // 4)])
+    u_ref = (words >> 8).astype(np.float64) / 2.0**24
+    u = np.array([oracle_lib.uniform(seed, b, h, step, r) for r in range(S)])
+    np.testing.assert_array_equal(u, u_ref[:S])
+    assert u.min() >= 0.0 and u.max() <= 1.0 - 2.0**-24
+    # Sec. 2.1 threshold rules on that stream
+    np.testing.assert_array_equal(oracle_lib.thresholds("systematic", S, seed, b, h, step),
+                                  (np.arange(S) + u_ref[0]) / S)
+    np.testing.assert_array_equal(oracle_lib.thresholds("stratified", S, seed, b, h, step),
+                                  (np.arange(S) + u_ref[:S]) / S)
+    np.testing.assert_array_equal(oracle_lib.thresholds("iid", S, seed, b, h, step), np.sort(u_ref[:S]))
+
+
+# ---------------------------------------------------------------------------
+# worked example and the score / softmax stage
+# ---------------------------------------------------------------------------
+
+def test_worked_example_nk3(oracle_lib):
+    g = json.load(open(os.path.join(HERE, "golden", "worked_example_nk3.json")))
+    V = np.array(g["V"], np.float64)
+    P = problem_from_probs(oracle_lib, g["p"], V)
+    est, J, delta = oracle_lib.sample_head(P, 0, 0, np.array(g["thresholds"]))
+    assert list(J + 1) == g["sampled_keys_one_based"]
+    counts = np.bincount(J, minlength=g["nk"])
+    assert {str(k + 1): int(c) for k, c in enumerate(counts)} == g["counts_one_based"]
+    np.testing.assert_allclose(est, (V[0] + V[0] + V[2]) / 3.0, rtol=1e-15, atol=1e-15)
+    assert delta.min() > 0.05
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
+def test_dense_matches_torch_sdpa(oracle_lib, dtype):
+    """Dense oracle == torch scaled_dot_product_attention in float64 (Eq. 1)."""
+    wl = synth.Workload("t", 2, 8, 2, 64, 300, dtype, 8, "systematic")
+    inp = synth.generate(wl, 3)
+    P = oracle_lib.Problem.from_inputs(inp)
+    out = oracle_lib.dense(P)
+    q = torch.from_numpy(synth.storage_to_f64(inp.q, dtype))
+    K = torch.from_numpy(synth.storage_to_f64(inp.K, dtype))
+    V = torch.from_numpy(synth.storage_to_f64(inp.V, dtype))
+    G = wl.group
+    for b in range(wl.batch):
+        sl = slice(int(inp.kv_offsets[b]), int(inp.kv_offsets[b + 1]))
+        for h in range(wl.n_q_heads):
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                q[b, h][None, None, None], K[sl, h // G][None, None], V[sl, h // G][None, None])
+            np.testing.assert_allclose(out[b, h], ref.reshape(-1).numpy(), rtol=1e-12, atol=1e-13)
+            s, p = oracle_lib.scores(P, b, h)
+            ref_p = torch.softmax(q[b, h] @ K[sl, h // G].T / np.sqrt(wl.head_dim), dim=0).numpy()
+            np.testing.assert_allclose(p, ref_p, rtol=1e-12, atol=1e-300)
+
+
+def test_tile_stats_match_logsumexp(oracle_lib):
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(5)
+    P = random_problem(oracle_lib, rng, 1000, 32, H=2, Hkv=1)
+    for h in range(2):
+        s, _ = oracle_lib.scores(P, 0, h)
+        m, l = oracle_lib.tile_stats(P, 0, h, 96)
+        assert m.shape[0] == 11
+        for t in range(11):
+            seg = s[96 * t: 96 * (t + 1)]
+            assert m[t] == seg.max()
+            np.testing.assert_allclose(m[t] + np.log(l[t]), logsumexp(seg), rtol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# inverse CDF convention and special cases
+# ---------------------------------------------------------------------------
+
+def test_inverse_cdf_left_closed_boundary(oracle_lib):
+    """App. A.4: J = j with F(j-1) <= t < F(j).  With K = 0 and nk = 4 the CDF
+    is exactly (0.25, 0.5, 0.75, 1); a threshold on an edge picks the next key."""
+    V = np.arange(12, dtype=np.float32).reshape(4, 1, 3)
+    P = make_problem(oracle_lib, np.ones((1, 3)), np.zeros((4, 1, 3)), V)
+    _, J, delta = oracle_lib.sample_head(P, 0, 0, np.array([0.0, 0.25, 0.5, 0.75, 0.2499999, 0.9999]))
+    assert list(J) == [0, 1, 2, 3, 0, 3]
+    assert delta[0] == 0.0 and delta[1] == 0.0
+
+
+def test_all_rows_equal_gives_that_row(oracle_lib):
+    rng = np.random.default_rng(2)
+    row = rng.standard_normal(16).astype(np.float32)
+    V = np.tile(row, (50, 1, 1))
+    P = make_problem(oracle_lib, rng.standard_normal((1, 16)), rng.standard_normal((50, 1, 16)), V)
+    for variant in ("iid", "stratified", "systematic"):
+        est, _, _ = oracle_lib.decode(P, variant, 7, seed=11)
+        np.testing.assert_array_equal(est[0, 0], row.astype(np.float64))
+
+
+@pytest.mark.parametrize("variant", ["stratified", "systematic"])
+def test_uniform_attention_with_S_equal_nk_visits_every_key_once(oracle_lib, variant):
+    rng = np.random.default_rng(3)
+    nk, d = 64, 8
+    V = rng.standard_normal((nk, 1, d)).astype(np.float32)
+    P = make_problem(oracle_lib, rng.standard_normal((1, d)), np.zeros((nk, 1, d)), V)
+    for seed in range(5):
+        est, J, _ = oracle_lib.decode(P, variant, nk, seed=seed)
+        assert list(J[0, 0]) == list(range(nk))
+        np.testing.assert_allclose(est[0, 0], V[:, 0].astype(np.float64).mean(axis=0), rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(est[0, 0], oracle_lib.dense(P)[0, 0], rtol=1e-12, atol=1e-13)
+
+
+def test_dominant_key_is_always_drawn(oracle_lib):
+    rng = np.random.default_rng(4)
+    nk, d = 40, 8
+    K = rng.standard_normal((nk, 1, d)).astype(np.float32)
+    q = rng.standard_normal((1, d)).astype(np.float32)
+    K[17, 0] = 40.0 * q[0] / np.linalg.norm(q[0])       # softmax mass of key 17 ~ 1 - 1e-30
+    V = rng.standard_normal((nk, 1, d)).astype(np.float32)
+    P = make_problem(oracle_lib, q, K, V, scale=1.0)
+    for variant in ("iid", "stratified", "systematic"):
+        est, J, _ = oracle_lib.decode(P, variant, 32, seed=1)
+        assert set(J[0, 0].tolist()) == {17}
+        np.testing.assert_array_equal(est[0, 0], V[17, 0].astype(np.float64))
+
+
+# ---------------------------------------------------------------------------
+# unbiasedness (Prop. A.2, A.4) as exact integrals over the randomness
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("S", [1, 2, 3, 5, 8])
+def test_systematic_sampler_exact_expectation_is_attention(oracle_lib, S):
+    rng = np.random.default_rng(10 + S)
+    P = random_problem(oracle_lib, rng, 9, 6, spread=1.5)
+    _, p = oracle_lib.scores(P, 0, 0)
+    mu = oracle_lib.dense(P)[0, 0]
+
+    def est_at(u):
+        t = (np.arange(S) + u) / S
+        return oracle_lib.sample_head(P, 0, 0, t)[0]
+
+    E = analysis.expectation_over_offset(est_at, analysis.systematic_breakpoints(p, S))
+    np.testing.assert_allclose(E, mu, rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("S", [1, 3, 4, 7])
+def test_stratified_per_stratum_expectation(oracle_lib, S):
+    """E over each stratum from the oracle's inverse CDF (one threshold swept
+    over I_m) == the interval-overlap weights of the closed form; their mean
+    over strata == AV."""
+    rng = np.random.default_rng(20 + S)
+    P = random_problem(oracle_lib, rng, 11, 5, spread=1.5)
+    _, p = oracle_lib.scores(P, 0, 0)
+    V = values_of(P, 0, 0)
+    mu = oracle_lib.dense(P)[0, 0]
+    F = np.cumsum(p)
+    w = analysis.stratum_weights(p, S)
+    total = np.zeros(V.shape[1])
+    for m in range(S):
+        lo, hi = m / S, (m + 1) / S
+        cuts = np.unique(np.concatenate([[lo, hi], F[(F > lo) & (F < hi)]]))
+        Em = np.zeros(V.shape[1])
+        for a, b in zip(cuts[:-1], cuts[1:]):
+            Em += oracle_lib.sample_head(P, 0, 0, np.array([0.5 * (a + b)]))[0] * (b - a) * S
+        np.testing.assert_allclose(Em, w[m] @ V, rtol=1e-11, atol=1e-12)
+        total += Em
+    np.testing.assert_allclose(total / S, mu, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(analysis.stratified_mean(p, V, S), mu, rtol=1e-11, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# statistics over the Philox stream: mean, variance, dominance, tail
+# ---------------------------------------------------------------------------
+
+def _seed_estimates(oracle_lib, P, variant, S, n_seeds):
+    return np.stack([oracle_lib.decode(P, variant, S, seed=s)[0][0, 0] for s in range(n_seeds)])
+
+
+@pytest.mark.parametrize("variant", ["iid", "stratified", "systematic"])
+def test_mean_over_seeds_within_4_sigma(oracle_lib, variant):
+    rng = np.random.default_rng(30)
+    P = random_problem(oracle_lib, rng, 200, 8, spread=1.0)
+    _, p = oracle_lib.scores(P, 0, 0)
+    V = values_of(P, 0, 0)
+    S, R = 16, 3000
+    E = _seed_estimates(oracle_lib, P, variant, S, R)
+    mu = oracle_lib.dense(P)[0, 0]
+    if variant == "iid":
+        var = analysis.iid_coordinate_variance(p, V, S)
+    elif variant == "stratified":
+        var = analysis.stratified_coordinate_variance(p, V, S)
+    else:
+        var = E.var(axis=0, ddof=1)
+    sigma = np.sqrt(np.maximum(var, 1e-14) / R)
+    assert np.all(np.abs(E.mean(axis=0) - mu) <= 4.0 * sigma)
+
+
+@pytest.mark.parametrize("variant", ["iid", "stratified"])
+def test_empirical_variance_matches_closed_form(oracle_lib, variant):
+    rng = np.random.default_rng(31)
+    P = random_problem(oracle_lib, rng, 150, 6, spread=1.2)
+    _, p = oracle_lib.scores(P, 0, 0)
+    V = values_of(P, 0, 0)
+    S, R = 8, 4000
+    E = _seed_estimates(oracle_lib, P, variant, S, R)
+    emp = analysis.replicate_variance_trace(E)
+    closed = (analysis.iid_variance_trace(p, V, S) if variant == "iid"
+              else analysis.stratified_variance_trace(p, V, S))
+    # the trace estimate over R replicates has relative s.d. below ~sqrt(2/R)*few
+    assert abs(emp / closed - 1.0) < 6.0 * np.sqrt(2.0 / R)
+
+
+def test_stratified_variance_never_exceeds_iid(oracle_lib):
+    """Thm. A.6 / Cor. A.7 on the closed forms, and the ordering seen empirically."""
+    rng = np.random.default_rng(32)
+    for trial in range(20):
+        P = random_problem(oracle_lib, rng, int(rng.integers(5, 300)), 4, spread=float(rng.uniform(0.1, 3)))
+        _, p = oracle_lib.scores(P, 0, 0)
+        V = values_of(P, 0, 0)
+        for S in (1, 2, 5, 16, 64):
+            assert (analysis.stratified_variance_trace(p, V, S)
+                    <= analysis.iid_variance_trace(p, V, S) * (1 + 1e-12) + 1e-15)
+    P = random_problem(oracle_lib, rng, 120, 6, spread=1.0)
+    S, R = 8, 1500
+    v = {var: analysis.replicate_variance_trace(_seed_estimates(oracle_lib, P, var, S, R))
+         for var in ("iid", "stratified", "systematic")}
+    assert v["stratified"] < v["iid"] and v["systematic"] < v["iid"]
+
+
+def test_sampling_count_invariants(oracle_lib):
+    """Systematic counts are floor/ceil(S p_n); stratified within +-1 of them;
+    all counts sum to S; zero-mass keys never drawn."""
+    rng = np.random.default_rng(33)
+    P = random_problem(oracle_lib, rng, 300, 8, spread=2.5)
+    _, p = oracle_lib.scores(P, 0, 0)
+    S = 64
+    lo, hi = analysis.systematic_count_bounds(p, S)
+    for seed in range(200):
+        _, Js, _ = oracle_lib.decode(P, "systematic", S, seed=seed)
+        c = np.bincount(Js[0, 0], minlength=300)
+        assert c.sum() == S
+        assert np.all(c >= lo - 1e-9) and np.all(c <= hi + 1e-9)
+        _, Jt, _ = oracle_lib.decode(P, "stratified", S, seed=seed)
+        c = np.bincount(Jt[0, 0], minlength=300)
+        assert c.sum() == S
+        assert np.all(c >= np.maximum(0, lo - 1)) and np.all(c <= hi + 1)
+        assert np.all(np.diff(Js[0, 0]) >= 0) and np.all(np.diff(Jt[0, 0]) >= 0)
+
+
+def test_iid_bernstein_tail(oracle_lib):
+    """App. B, Thm. B.1: the error norm exceeds the delta-radius at most a
+    delta fraction of the time (checked with a binomial margin)."""
+    rng = np.random.default_rng(34)
+    P = random_problem(oracle_lib, rng, 100, 8, spread=1.0)
+    _, p = oracle_lib.scores(P, 0, 0)
+    V = values_of(P, 0, 0)
+    mu = oracle_lib.dense(P)[0, 0]
+    v = analysis.iid_variance_trace(p, V, 1)
+    vmax = float(np.max(np.linalg.norm(V - mu, axis=1)))
+    S, R, delta = 16, 2000, 0.05
+    r = analysis.bernstein_radius(v, vmax, S, delta)
+    E = _seed_estimates(oracle_lib, P, "iid", S, R)
+    frac = np.mean(np.linalg.norm(E - mu, axis=1) >= r)
+    assert frac <= delta + 3 * np.sqrt(delta * (1 - delta) / R)
+
+
+def test_decode_layout_ragged_and_padding(oracle_lib):
+    """Per-sequence budgets: rows beyond S_b are -1; each head equals a
+    single-head call."""
+    wl = synth.Workload("r", 3, 4, 2, 32, 200, "bf16", 24, "stratified", ragged=(50, 200))
+    inp = synth.generate(wl, 9)
+    Sp = np.array([24, 5, 13], np.int32)
+    P = oracle_lib.Problem.from_inputs(inp)
+    est, J, delta = oracle_lib.decode(P, "stratified", 24, seed=4, S_per_seq=Sp)
+    for b in range(3):
+        for h in range(4):
+            e1, J1, d1 = oracle_lib.decode_head(P, "stratified", int(Sp[b]), 4, b, h)
+            np.testing.assert_array_equal(J[b, h, :Sp[b]], J1)
+            np.testing.assert_array_equal(est[b, h], e1)
+            assert np.all(J[b, h, Sp[b]:] == -1)
+            assert J1.max() < inp.nk_per_seq[b]
