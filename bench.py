@@ -1,0 +1,458 @@
+#!/usr/bin/env python3
+"""S2ANTA decode-step benchmark (one JSON line on rank 0).
+
+A step is one pass of the whole operator (score pass, combine + thresholds,
+sample + gather) over one decode step of the workload, through the C ABI on
+device-resident inputs.  Protocol (after "Stochastic Sparse Attention for
+Memory-Bound Inference", App. Q): W untimed warm-up steps, then K timed steps,
+each preceded by an untimed in-place update of a 512 MiB fp32 buffer that
+evicts the 129 MB L2, each bracketed by CUDA events on the launching stream.
+
+    python bench.py [--steps K] [--warmup W] [--workload llama32k|qwen|ragged|tiny]
+    python bench.py --impl reference      # the CPU oracle, timed on host cores
+Multi-GPU (torchrun): every rank decodes its own copy of the workload
+(independent replicas, no collective on the data path; scaling "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "S²ANTA decode-attn µs/step and achieved HBM GB/s vs peak, 32K ctx bf16"
+UNIT = "us/step"
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 512 * 1024 * 1024
+SCORE_SOURCES = ["stochastic_sparse_decode_split_gb300/csrc/santa_score.cu",
+                 "stochastic_sparse_decode_split_gb300/csrc/santa_common.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "score_pass_traffic.json")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama32k", choices=["llama32k", "qwen", "ragged", "tiny"])
+    ap.add_argument("--nk", type=int, default=None, help="override keys per sequence (llama32k shape)")
+    ap.add_argument("--S", type=int, default=None)
+    ap.add_argument("--variant", default=None, choices=["iid", "stratified", "systematic"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample length")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def make_workload(args):
+    import synth
+    if args.workload == "llama32k":
+        wl = synth.llama32k(nk=args.nk or 32768, S=args.S or 256, variant=args.variant or "systematic")
+    elif args.workload == "qwen":
+        wl = synth.qwen_batched()
+    elif args.workload == "ragged":
+        wl = synth.ragged()
+    else:
+        wl = synth.tiny(args.variant or "systematic")
+    return wl
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+# ---------------------------------------------------------------------------
+# peaks, clocks, traffic record
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for k in ("hbm_gbs", "hbm_GBps", "hbm_copy_gbs"):
+            if k in d and d[k]:
+                return float(d[k]), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.idx = device_index
+
+    def start(self):
+        try:
+            cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "200"]
+            uuid = os.environ.get("SANTA_GPU_UUID")
+            if uuid:
+                cmd += ["--id=" + uuid]
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        rows = [r.split(",") for r in self.out.read().strip().splitlines() if r.strip()]
+        os.unlink(self.out.name)
+        rows = [[c.strip() for c in r] for r in rows if len(r) >= 9]
+        if not rows:
+            return None
+        by_gpu = {}
+        for r in rows:
+            by_gpu.setdefault(r[0], []).append(r)
+        # the busiest GPU (highest median power) is ours when several are listed
+        def med_power(rs):
+            vals = [float(r[3]) for r in rs if r[3].replace(".", "", 1).isdigit()]
+            return statistics.median(vals) if vals else 0.0
+        rs = max(by_gpu.values(), key=med_power)
+        sm = [float(r[1]) for r in rs if r[1].replace(".", "", 1).isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rs:
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": float(rs[0][2]) if rs[0][2].replace(".", "", 1).isdigit() else None,
+                "reasons": sorted(reasons), "samples": len(rs)}
+
+
+def source_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_name):
+    """dram read+write bytes per launch of the score pass from a committed ncu
+    summary, only while the kernel source is unchanged since the capture."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_hash") != source_hash(SCORE_SOURCES):
+        return None
+    if rec.get("workload") != workload_name:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# byte model (algorithmic bytes)
+# ---------------------------------------------------------------------------
+
+def esize(dtype):
+    return {"bf16": 2, "fp16": 2, "fp32": 4}[dtype]
+
+
+def score_pass_bytes(inp):
+    """K read once + q read + per-chunk (max, exp-sum) written.  The fp32
+    score stash is written to L2 and read back by the sampler there; it is
+    not counted (ncu dram bytes show whether it reaches HBM)."""
+    wl = inp.wl
+    es = esize(wl.dtype)
+    B, H, d = inp.q.shape
+    rows = int(inp.kv_offsets[-1])
+    chunks = sum((int(n) + 255) // 256 for n in inp.nk_per_seq)
+    return rows * wl.n_kv_heads * d * es + B * H * d * es + 2 * 4 * H * chunks
+
+
+def step_bytes(inp, unique_rows):
+    """Full K + deduplicated gathered V rows + q + out."""
+    wl = inp.wl
+    es = esize(wl.dtype)
+    B, H, d = inp.q.shape
+    rows = int(inp.kv_offsets[-1])
+    return rows * wl.n_kv_heads * d * es + unique_rows * d * es + B * H * d * es + B * H * d * 4
+
+
+def dense_bytes(inp):
+    wl = inp.wl
+    es = esize(wl.dtype)
+    B, H, d = inp.q.shape
+    rows = int(inp.kv_offsets[-1])
+    return 2 * rows * wl.n_kv_heads * d * es + B * H * d * es + B * H * d * 4
+
+
+def count_unique_rows(inp, idx):
+    """Distinct (sequence, KV head, key) triples drawn by any head of a group."""
+    import numpy as np
+    B, H, _ = inp.q.shape
+    G = inp.wl.group
+    total = 0
+    for b in range(B):
+        S_b = inp.S_of(b)
+        for kvh in range(inp.wl.n_kv_heads):
+            total += np.unique(idx[b, kvh * G:(kvh + 1) * G, :S_b]).size
+    return int(total)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_threads():
+    return max(1, os.cpu_count() or 1)
+
+
+def time_oracle_full_steps(inp, variant, seconds):
+    """Whole decode steps of the oracle (all heads, OpenMP over heads) until
+    `seconds` of wall time have passed; returns (us_per_step, steps, threads)."""
+    import oracle
+    P = oracle.Problem.from_inputs(inp)
+    n_thr = oracle_threads()
+    steps = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.decode(P, variant, inp.wl.S, seed=steps, S_per_seq=inp.S_per_seq, n_threads=n_thr)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or steps >= 1000:
+            break
+    return el / steps * 1e6, steps, n_thr
+
+
+def run_reference(args):
+    ws_, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import oracle
+    import synth
+    oracle.build()
+    wl = make_workload(args)
+    inp = synth.generate(wl, 0)
+    P = oracle.Problem.from_inputs(inp)
+    B, H, _ = inp.q.shape
+    heads = [(b, h) for b in range(B) for h in range(H)]
+    # one head's cost sizes the per-step sample so that the whole run stays near two minutes
+    t0 = time.perf_counter()
+    oracle.decode_head(P, wl.variant, inp.S_of(0), 0, 0, 0)
+    t_head = max(time.perf_counter() - t0, 1e-4)
+    total_steps = args.steps + args.warmup
+    per_step = int(max(1, min(len(heads), 120.0 / (total_steps * t_head))))
+    times = []
+    for i in range(total_steps):
+        sel = [heads[(i * per_step + k) % len(heads)] for k in range(per_step)]
+        t0 = time.perf_counter()
+        for (b, h) in sel:
+            oracle.decode_head(P, wl.variant, inp.S_of(b), i, b, h)
+        el = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(el * len(heads) / per_step)   # scaled to a whole decode step
+    us = statistics.mean(times) * 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "variant": wl.variant, "S": wl.S, "nk": wl.nk},
+        "cpu_baseline": {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{per_step} of {len(heads)} heads per step (single thread), "
+                                   f"time scaled to all heads"},
+        "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import synth
+    import stochastic_sparse_decode_split_gb300 as santa
+
+    world, rank, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    santa.library()   # fails loudly if the CUDA library was not built
+
+    wl = make_workload(args)
+    inp = synth.generate(wl, 0)
+    t = synth.to_torch(inp, dev)
+    ragged = wl.ragged is not None
+    nk_bound = int(inp.nk_per_seq.max()) if ragged else None
+    kw = dict(nk=nk_bound, kv_offsets=t["kv_offsets"] if ragged else None)
+    S_max = inp.S_max
+    B, H, d = inp.q.shape
+
+    dec = santa.Decoder(t["q"], t["K"], t["V"], S=S_max, variant=wl.variant, seed=0, S_per_seq=t["S_per_seq"],
+                        **kw)
+    # sampled rows of the timed step (same seed and step), for the byte model
+    idx = torch.full((B, H, S_max), -1, dtype=torch.int32, device=dev)
+    santa.santa_decode(t["q"], t["K"], t["V"], S=S_max, variant=wl.variant, seed=0, step=0,
+                       S_per_seq=t["S_per_seq"], sample_idx=idx, **kw)
+    torch.cuda.synchronize()
+    unique_rows = count_unique_rows(inp, idx.cpu().numpy())
+    if santa.get_error(dec.workspace):
+        raise RuntimeError("device flagged bad metadata")
+
+    flush = torch.zeros(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def timed_loop(fn, n, warm):
+        for _ in range(warm):
+            flush.add_(1.0)
+            fn()
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        for i in range(n):
+            flush.add_(1.0)
+            starts[i].record(stream)
+            fn()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+    sampler = ClockSampler(local_rank).start()
+    time.sleep(0.3)
+    ms = timed_loop(lambda: dec(step=0), args.steps, args.warmup)
+    clocks = sampler.stop()
+
+    total_ms = sum(ms)
+    if world > 1:
+        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    mean_ms = total_ms / args.steps
+    med_ms = statistics.median(ms)
+
+    # per-stage times (events recorded between the three stages, same stream)
+    n_prof = min(args.steps, 1000)
+    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_prof)]
+    for _ in range(args.warmup):
+        flush.add_(1.0)
+        dec.profiled(ev_sets[0])
+    torch.cuda.synchronize()
+    for i in range(n_prof):
+        flush.add_(1.0)
+        dec.profiled(ev_sets[i])
+    torch.cuda.synchronize()
+    stage_ms = [statistics.mean(e[k].elapsed_time(e[k + 1]) for e in ev_sets) for k in range(3)]
+
+    # dense comparator, same protocol
+    dense = santa.Decoder(t["q"], t["K"], t["V"], S=1, variant=wl.variant, dense=True, **kw)
+    n_dense = min(args.steps, 1000)
+    dms = timed_loop(lambda: dense(), n_dense, args.warmup)
+
+    # end to end through the public API with host buffers: H2D of q, K, V from
+    # pinned memory, the decode, D2H of the output, all inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hq, hK, hV = (x.cpu().pin_memory() for x in (t["q"], t["K"], t["V"]))
+        hout = torch.empty((B, H, d), dtype=torch.float32).pin_memory()
+        dq, dK, dV = torch.empty_like(t["q"]), torch.empty_like(t["K"]), torch.empty_like(t["V"])
+        dec_e = santa.Decoder(dq, dK, dV, S=S_max, variant=wl.variant, seed=0, S_per_seq=t["S_per_seq"], **kw)
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dK.copy_(hK, non_blocking=True)
+            dV.copy_(hV, non_blocking=True)
+            o = dec_e(step=0)
+            hout.copy_(o, non_blocking=True)
+
+        n_e2e = min(args.steps, 200)
+        ems = timed_loop(e2e_step, n_e2e, 3)
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hK, hV))
+        e2e = {"value": statistics.mean(ems) * 1e3 / world, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": hout.numel() * hout.element_size()}
+
+    peak, peak_kind = hbm_peak()
+    sb = score_pass_bytes(inp)
+    stb = step_bytes(inp, unique_rows)
+    achieved = sb / (stage_ms[0] * 1e-3) / 1e9
+    step_achieved = stb / (mean_ms * 1e-3) / 1e9
+    value_us = mean_ms * 1e3 / world   # whole job: time per decode step over all ranks' steps
+
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        us_cpu, n_cpu, thr = time_oracle_full_steps(inp, wl.variant, args.cpu_seconds)
+        cpu_baseline = {"value": us_cpu, "unit": UNIT, "cores": thr, "kind": "oracle",
+                        "sample": f"{n_cpu} whole decode steps of {wl.name} (float64, OpenMP over heads), "
+                                  f"{args.cpu_seconds:.0f} s budget"}
+
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value_us, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "variant": wl.variant, "S": S_max, "nk": wl.nk, "batch": B,
+                   "n_q_heads": H, "n_kv_heads": wl.n_kv_heads, "head_dim": d,
+                   "l2": "512 MiB fp32 in-place update before every timed step (untimed)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "median_us": med_ms * 1e3,
+        "roofline": {"bound": "hbm", "kernel": "score_chunks_kernel", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": recorded_traffic(wl.name),
+                     "peak_kind": f"of {peak_kind}", "alg_bytes_per_launch": sb,
+                     "us_per_launch": stage_ms[0] * 1e3},
+        "step": {"alg_bytes": stb, "unique_v_rows": unique_rows, "achieved_GBps": step_achieved,
+                 "frac": step_achieved / peak, "stage_us": {"score": stage_ms[0] * 1e3,
+                                                            "combine": stage_ms[1] * 1e3,
+                                                            "sample_gather": stage_ms[2] * 1e3}},
+        "dense": {"us_per_step": statistics.mean(dms) * 1e3, "alg_bytes": dense_bytes(inp),
+                  "achieved_GBps": dense_bytes(inp) / (statistics.mean(dms) * 1e-3) / 1e9,
+                  "speedup_santa_vs_dense": statistics.mean(dms) / mean_ms},
+        "cpu_baseline": cpu_baseline,
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,164 @@
+/*
+ * santa.h -- C ABI of the GB300 (sm_103a) SANTA / S2ANTA decode-step attention
+ * library (libsanta.so).
+ *
+ * The operator, per query head h of sequence b ("Stochastic Sparse Attention
+ * for Memory-Bound Inference", arXiv:2605.01910):
+ *   s_n = scale * q[b,h] . K[b,n,kvh]       scores over the whole key cache (Sec. 2, Eq. 1)
+ *   A   = softmax(s)                         post-softmax distribution     (Sec. 2, Eq. 1)
+ *   J_j = F^-1(t_j), j = 0..S-1              inverse-CDF draws              (App. A.4)
+ *         t_j = u_j          (SANTA, i.i.d.; Eq. 4, Def. A.1)
+ *         t_j = (j + u_j)/S  (S2ANTA-strat; Sec. 2.1)
+ *         t_j = (j + u)/S    (S2ANTA-sys;   Sec. 2.1)
+ *   out = (1/S) * sum_n c_n V[b,n,kvh]       count-weighted gather-and-add (Eq. 4, Fig. 1)
+ * with kvh = h / (n_q_heads / n_kv_heads) (grouped-query attention).  The
+ * uniforms u come from Philox4x32-10 (Salmon et al., SC'11): number r of head
+ * (b, h) is word r%4 of the block at counter (r/4, h, b, step) under key
+ * (seed_lo, seed_hi), mapped to [0,1) as (word >> 8) * 2^-24.  The pages name
+ * no generator; this keying by (seed, batch, head, step) is this library's.
+ *
+ * Layouts (row-major, sequence-major caches as in App. Q of the paper):
+ *   q    [batch, n_q_heads, head_dim]               dtype
+ *   K, V [total_rows, n_kv_heads, head_dim]         dtype; rows of sequence b are
+ *        [kv_offsets[b], kv_offsets[b+1]) (or [b*nk, (b+1)*nk) when kv_offsets is NULL)
+ *   out  [batch, n_q_heads, head_dim]               float32
+ *
+ * Ownership and threading: the caller owns every buffer (device memory unless
+ * stated) including the workspace; the library allocates nothing and keeps no
+ * state outside the workspace.  All work is enqueued asynchronously on the
+ * caller's stream; calls that share a workspace must be ordered on one stream.
+ *
+ * Errors: arguments are validated on the host before any launch and reported
+ * as a status.  Conditions only visible on the device (a ragged length above
+ * the stated bound, a per-sequence budget out of range) set an error word in
+ * the workspace and leave that head's output zero; santa_get_error reports it.
+ * Kernels never trap.
+ */
+#ifndef SANTA_H
+#define SANTA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* santa_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  SANTA_IID = 0,        /* SANTA: S i.i.d. draws from Categorical(A) (Eq. 4) */
+  SANTA_STRATIFIED = 1, /* S2ANTA-strat: one independent draw per equal-mass stratum (Sec. 2.1) */
+  SANTA_SYSTEMATIC = 2  /* S2ANTA-sys: one offset shared by all strata (Sec. 2.1) */
+} santa_variant_t;
+
+typedef enum { SANTA_BF16 = 0, SANTA_FP16 = 1, SANTA_FP32 = 2 } santa_dtype_t;
+
+typedef enum {
+  SANTA_OK = 0,
+  SANTA_ERR_INVALID_ARG = 1, /* NULL pointer, bad shape, misalignment, S or nk out of range */
+  SANTA_ERR_UNSUPPORTED = 2, /* head_dim / dtype / group size this build does not provide */
+  SANTA_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned or smaller than *_workspace_size */
+  SANTA_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch, copy, sync) */
+  SANTA_ERR_DEVICE = 5       /* the device flagged bad ragged metadata (see santa_get_error) */
+} santa_status_t;
+
+typedef struct {
+  int32_t batch;             /* >= 1 */
+  int32_t n_q_heads;         /* H >= 1 */
+  int32_t n_kv_heads;        /* H_kv >= 1, H % H_kv == 0, group H/H_kv <= 8 */
+  int32_t head_dim;          /* 64 or 128 */
+  int32_t dtype;             /* santa_dtype_t, shared by q, K and V */
+  const int64_t* kv_offsets; /* device [batch+1] row offsets, non-decreasing from 0; NULL = uniform */
+  int64_t nk;                /* keys per sequence; with kv_offsets, an upper bound on every nk_b */
+  int32_t S;                 /* sample budget >= 1; with S_per_seq, an upper bound on every S_b */
+  const int32_t* S_per_seq;  /* device [batch] budgets S_b in [1, S], or NULL */
+  float scale;               /* score scale; <= 0 selects 1/sqrt(head_dim) (Eq. 1) */
+  uint64_t seed;             /* Philox key */
+  uint32_t step;             /* decode step, part of the Philox counter */
+} santa_params_t;
+
+/* Limits of this build. */
+#define SANTA_MAX_S 4096        /* S (and every S_b) */
+#define SANTA_MAX_NK (1 << 21)  /* keys per sequence */
+#define SANTA_MAX_GROUP 8       /* n_q_heads / n_kv_heads */
+#define SANTA_CHUNK 256         /* keys per score / sampling chunk */
+
+/* Byte size of the workspace santa_decode needs for these parameters
+ * (0 when the parameters are invalid).  The variant does not change it. */
+size_t santa_workspace_size(const santa_params_t* p);
+
+/* Clears the workspace's control words (error word and hand-off counters).
+ * Call once after allocating a workspace, before its first use. */
+santa_status_t santa_workspace_init(void* workspace, size_t ws_bytes, santa_stream_t stream);
+
+/* One S2ANTA / SANTA decode step (all of Sec. 2 / 2.1 above) on `stream`.
+ *   q, K, V    device, 16-byte aligned, layouts above.
+ *   out        device float32 [batch, n_q_heads, head_dim], overwritten.
+ *   workspace  device, 256-byte aligned, >= santa_workspace_size(p) bytes.
+ *   sample_idx optional device int32 [batch, n_q_heads, S]: the drawn key index
+ *              (within its sequence) of every sorted threshold j; entries
+ *              j >= S_b are -1.  NULL skips it.
+ * Stages: score pass with per-chunk (max, exp-sum) and a score stash; per-head
+ * combine into chunk mass prefixes and Philox thresholds; per-chunk inverse
+ * CDF, GQA row union and V gather-add with a deterministic reduction. */
+santa_status_t santa_decode(const santa_params_t* p, int32_t variant, const void* q, const void* K,
+                            const void* V, float* out, void* workspace, size_t ws_bytes,
+                            santa_stream_t stream, int32_t* sample_idx);
+
+/* santa_decode that also records stage_events[i] (cudaEvent_t, created by the
+ * caller) on `stream` before stage i (0 score pass, 1 combine, 2 sample and
+ * gather) and stage_events[3] after the last stage, so a caller can time each
+ * stage on the launching stream.  stage_events may be NULL (then identical to
+ * santa_decode). */
+santa_status_t santa_decode_profiled(const santa_params_t* p, int32_t variant, const void* q, const void* K,
+                                     const void* V, float* out, void* workspace, size_t ws_bytes,
+                                     santa_stream_t stream, int32_t* sample_idx, void* const* stage_events);
+
+/* santa_decode with caller-supplied uniforms in place of Philox: device float64
+ * u[batch, n_q_heads, S] in [0,1) (only u[...,0] is read for SANTA_SYSTEMATIC).
+ * For checking the sampler against hand-made cases such as the nk = 3 worked
+ * example of Sec. 1 (Eq. 2-3). */
+santa_status_t santa_decode_with_uniforms(const santa_params_t* p, int32_t variant, const void* q,
+                                          const void* K, const void* V, const double* uniforms,
+                                          float* out, void* workspace, size_t ws_bytes,
+                                          santa_stream_t stream, int32_t* sample_idx);
+
+/* Exact decode attention softmax(q K^T * scale) V (Eq. 1) by split-KV partials
+ * (max, exp-sum, partial output) per 256-key chunk and a per-head merge.  This
+ * library's own dense comparator.  Same argument rules as santa_decode;
+ * S, S_per_seq, seed and step are ignored. */
+size_t santa_dense_workspace_size(const santa_params_t* p);
+santa_status_t santa_dense_decode(const santa_params_t* p, const void* q, const void* K, const void* V,
+                                  float* out, void* workspace, size_t ws_bytes, santa_stream_t stream);
+
+/* Byte offsets of the intermediate arrays inside a santa_decode workspace, for
+ * inspection by tests and tools after the stream has synchronised:
+ *   stash     float32 [batch, n_q_heads, nk]        scaled scores s_n
+ *   tile_max  float32 [batch, n_q_heads, chunks]    per-chunk max of s_n
+ *   tile_sum  float32 [batch, n_q_heads, chunks]    per-chunk sum of exp(s_n - tile_max)
+ *   prefix    float64 [batch, n_q_heads, chunks+1]  chunk mass prefix, relative to the head max
+ *   thresh    float64 [batch, n_q_heads, S]         sorted thresholds t_j * Z
+ *   head_max  float32 [batch, n_q_heads]            max_n s_n
+ * with chunks = ceil(nk / SANTA_CHUNK).  Returns 0 on success. */
+typedef struct {
+  size_t stash, tile_max, tile_sum, prefix, thresh, head_max;
+  int64_t chunks;
+} santa_ws_layout_t;
+int32_t santa_workspace_layout(const santa_params_t* p, santa_ws_layout_t* layout);
+
+/* Synchronises `stream`, reads and clears the workspace error word.
+ * Returns SANTA_OK, SANTA_ERR_DEVICE (device flagged bad metadata; *code gets
+ * the flag bits when code != NULL) or SANTA_ERR_CUDA. */
+santa_status_t santa_get_error(void* workspace, santa_stream_t stream, int32_t* code);
+
+/* Static description of a status code. */
+const char* santa_status_string(santa_status_t status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t santa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SANTA_H */

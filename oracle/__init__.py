@@ -78,10 +78,11 @@ def _load():
             lib.santa_oracle_tile_stats.argtypes = [P, i32, i32, i32, vp, vp]
             lib.santa_oracle_sample_head.argtypes = [P, i32, i32, i32, vp, vp, vp, vp]
             lib.santa_oracle_dense_head.argtypes = [P, i32, i32, vp]
+            lib.santa_oracle_gather.argtypes = [P, i32, i32, i32, vp, vp]
             lib.santa_oracle_decode.argtypes = [P, i32, i32, vp, i32, u64, u32, vp, vp, vp, i32]
             lib.santa_oracle_dense.argtypes = [P, vp, i32]
             for fn in ("santa_oracle_scores", "santa_oracle_tile_stats", "santa_oracle_sample_head",
-                       "santa_oracle_dense_head", "santa_oracle_decode", "santa_oracle_dense"):
+                       "santa_oracle_dense_head", "santa_oracle_gather", "santa_oracle_decode", "santa_oracle_dense"):
                 getattr(lib, fn).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -165,6 +166,15 @@ def sample_head(P: Problem, b: int, h: int, t: np.ndarray):
                                         _ptr(delta)):
         raise ValueError("oracle sample: bad arguments")
     return est, J, delta
+
+
+def gather(P: Problem, b: int, h: int, J) -> np.ndarray:
+    """Eq. (4) for a given index multiset: (1/S) * sum_j V[J_j]."""
+    J = np.ascontiguousarray(J, dtype=np.int32)
+    est = np.zeros(P.shape[3], np.float64)
+    if _load().santa_oracle_gather(ctypes.byref(P.c), b, h, J.shape[0], _ptr(J), _ptr(est)):
+        raise ValueError("oracle gather: bad arguments")
+    return est
 
 
 def dense_head(P: Problem, b: int, h: int) -> np.ndarray:

@@ -247,6 +247,24 @@ int santa_oracle_sample_head(const oracle_problem* P, int32_t b, int32_t h, int3
   return 0;
 }
 
+/* Eq. (4) for a given index multiset: est = (1/S) * sum_j V[J_j]. */
+int santa_oracle_gather(const oracle_problem* P, int32_t b, int32_t h, int32_t S, const int32_t* J,
+                        double* est) {
+  if (check_head(P, b, h) || S <= 0) return -1;
+  const int64_t nk = nk_of(P, b);
+  const int32_t d = P->head_dim, Hkv = P->n_kv_heads;
+  const int32_t kvh = h / (P->n_q_heads / Hkv);
+  const int64_t row0 = P->kv_offsets[b];
+  for (int32_t k = 0; k < d; ++k) est[k] = 0.0;
+  for (int32_t j = 0; j < S; ++j) {
+    if (J[j] < 0 || J[j] >= nk) return -1;
+    const int64_t base = ((row0 + J[j]) * Hkv + kvh) * (int64_t)d;
+    for (int32_t k = 0; k < d; ++k) est[k] += load_elem(P->dtype, P->V, base + k);
+  }
+  for (int32_t k = 0; k < d; ++k) est[k] *= 1.0 / (double)S;
+  return 0;
+}
+
 int santa_oracle_dense_head(const oracle_problem* P, int32_t b, int32_t h, double* out) {
   if (check_head(P, b, h)) return -1;
   const int64_t nk = nk_of(P, b);

@@ -64,6 +64,10 @@ int santa_oracle_tile_stats(const oracle_problem* P, int32_t b, int32_t h, int32
 int santa_oracle_sample_head(const oracle_problem* P, int32_t b, int32_t h, int32_t S,
                              const double* t, double* est, int32_t* J, double* delta);
 
+/* Eq. (4) for a given index multiset J[0..S): est = (1/S) sum_j V[J_j]. */
+int santa_oracle_gather(const oracle_problem* P, int32_t b, int32_t h, int32_t S, const int32_t* J,
+                        double* est);
+
 /* Exact attention of one head: sum_n p_n V_n. */
 int santa_oracle_dense_head(const oracle_problem* P, int32_t b, int32_t h, double* out);
 

@@ -1,0 +1,286 @@
+"""GB300 (sm_103a) SANTA / S2ANTA decode-step attention.
+
+Thin Python binding over the C ABI in ``include/santa.h`` (``libsanta.so``,
+built in-tree by ``stochastic_sparse_decode_split_gb300.build``).  The binding
+only marshals arguments: PyTorch tensors supply device memory and the current
+CUDA stream, and every step of the operator runs in the library's kernels.
+There is no CPU fallback: if the library is missing or a call fails, an
+exception is raised.
+
+Operator ("Stochastic Sparse Attention for Memory-Bound Inference", Sec. 2,
+Eq. 1 and 4; Sec. 2.1): per query head, exact scores and softmax over the whole
+key cache, S draws from the post-softmax distribution (i.i.d., stratified or
+systematic; Philox4x32-10 keyed by seed, batch, head, step), and the estimate
+(1/S) * sum of the drawn V rows computed as a count-weighted gather-and-add.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+from typing import Optional
+
+import torch
+
+from .build import LIB as _LIB_PATH
+
+__all__ = [
+    "SantaError", "Params", "library", "santa_decode", "santa_decode_with_uniforms", "santa_dense_decode",
+    "workspace_size", "dense_workspace_size", "workspace_layout", "get_error", "Decoder", "exported_symbols",
+    "VARIANTS", "DTYPES",
+]
+
+VARIANTS = {"iid": 0, "stratified": 1, "systematic": 2}
+DTYPES = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "santa.h")
+
+SANTA_OK, SANTA_ERR_DEVICE = 0, 5
+
+
+class SantaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {library().santa_status_string(status).decode()} (status {status})")
+
+
+class Params(ctypes.Structure):
+    """Mirror of santa_params_t."""
+    _fields_ = [
+        ("batch", ctypes.c_int32),
+        ("n_q_heads", ctypes.c_int32),
+        ("n_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+        ("kv_offsets", ctypes.c_void_p),
+        ("nk", ctypes.c_int64),
+        ("S", ctypes.c_int32),
+        ("S_per_seq", ctypes.c_void_p),
+        ("scale", ctypes.c_float),
+        ("seed", ctypes.c_uint64),
+        ("step", ctypes.c_uint32),
+    ]
+
+
+class WsLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in ("stash", "tile_max", "tile_sum", "prefix", "thresh", "head_max")] + [
+        ("chunks", ctypes.c_int64)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library():
+    """Loads libsanta.so (raises if it was not built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(f"{_LIB_PATH} is missing: build it with "
+                                   "`python -m stochastic_sparse_decode_split_gb300.build`")
+            lib = ctypes.CDLL(_LIB_PATH)
+            vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32
+            P = ctypes.POINTER(Params)
+            lib.santa_workspace_size.argtypes = [P]
+            lib.santa_workspace_size.restype = sz
+            lib.santa_dense_workspace_size.argtypes = [P]
+            lib.santa_dense_workspace_size.restype = sz
+            lib.santa_workspace_init.argtypes = [vp, sz, vp]
+            lib.santa_decode.argtypes = [P, i32, vp, vp, vp, vp, vp, sz, vp, vp]
+            lib.santa_decode_profiled.argtypes = [P, i32, vp, vp, vp, vp, vp, sz, vp, vp, vp]
+            lib.santa_decode_with_uniforms.argtypes = [P, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp]
+            lib.santa_dense_decode.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
+            lib.santa_workspace_layout.argtypes = [P, ctypes.POINTER(WsLayout)]
+            lib.santa_get_error.argtypes = [vp, vp, ctypes.POINTER(i32)]
+            lib.santa_status_string.argtypes = [i32]
+            lib.santa_status_string.restype = ctypes.c_char_p
+            lib.santa_version.restype = i32
+            for fn in ("santa_workspace_init", "santa_decode", "santa_decode_profiled", "santa_decode_with_uniforms", "santa_dense_decode",
+                       "santa_workspace_layout", "santa_get_error"):
+                getattr(lib, fn).restype = i32
+            _lib = lib
+    return _lib
+
+
+def exported_symbols():
+    """Function names declared in include/santa.h."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(santa_[a-z_]+)\s*\(", text)))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def make_params(q: torch.Tensor, K: torch.Tensor, S: int, seed: int = 0, step: int = 0, nk: Optional[int] = None,
+                kv_offsets: Optional[torch.Tensor] = None, S_per_seq: Optional[torch.Tensor] = None,
+                scale: float = 0.0) -> Params:
+    if q.dim() != 3 or K.dim() != 3:
+        raise ValueError("q must be [B, H, d] and K [rows, H_kv, d]")
+    B, H, d = q.shape
+    Hkv = K.shape[1]
+    if q.dtype not in DTYPES or K.dtype != q.dtype:
+        raise ValueError("q, K, V must share one of bf16 / fp16 / fp32")
+    if nk is None:
+        if kv_offsets is not None:
+            raise ValueError("give nk (an upper bound on every sequence length) with kv_offsets")
+        if K.shape[0] % B:
+            raise ValueError("uniform batch: K rows must be a multiple of the batch")
+        nk = K.shape[0] // B
+    p = Params()
+    p.batch, p.n_q_heads, p.n_kv_heads, p.head_dim = B, H, Hkv, d
+    p.dtype = DTYPES[q.dtype]
+    p.kv_offsets = None if kv_offsets is None else kv_offsets.data_ptr()
+    p.nk = int(nk)
+    p.S = int(S)
+    p.S_per_seq = None if S_per_seq is None else S_per_seq.data_ptr()
+    p.scale = float(scale)
+    p.seed = int(seed) & 0xFFFFFFFFFFFFFFFF
+    p.step = int(step) & 0xFFFFFFFF
+    return p
+
+
+def workspace_size(p: Params) -> int:
+    return int(library().santa_workspace_size(ctypes.byref(p)))
+
+
+def dense_workspace_size(p: Params) -> int:
+    return int(library().santa_dense_workspace_size(ctypes.byref(p)))
+
+
+def workspace_layout(p: Params) -> dict:
+    lay = WsLayout()
+    if library().santa_workspace_layout(ctypes.byref(p), ctypes.byref(lay)) != 0:
+        raise ValueError("invalid parameters")
+    return {n: getattr(lay, n) for n, _ in WsLayout._fields_}
+
+
+def alloc_workspace(nbytes: int, device) -> torch.Tensor:
+    """Device workspace (uint8, 256-byte aligned, control words cleared)."""
+    ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    ws = ws[off:off + nbytes]
+    st = library().santa_workspace_init(_ptr(ws), nbytes, _stream())
+    if st != SANTA_OK:
+        raise SantaError(st, "santa_workspace_init")
+    return ws
+
+
+def get_error(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronises the stream and returns (then clears) the device error flags."""
+    code = ctypes.c_int32(0)
+    st = library().santa_get_error(_ptr(workspace), _stream(stream), ctypes.byref(code))
+    if st not in (SANTA_OK, SANTA_ERR_DEVICE):
+        raise SantaError(st, "santa_get_error")
+    return int(code.value)
+
+
+def _check_tensors(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def santa_decode(q, K, V, S: int, variant: str = "systematic", seed: int = 0, step: int = 0, out=None,
+                 nk: Optional[int] = None, kv_offsets=None, S_per_seq=None, scale: float = 0.0, workspace=None,
+                 sample_idx=None, stream=None) -> torch.Tensor:
+    """One S2ANTA / SANTA decode step; returns out [B, H, d] float32."""
+    _check_tensors(q, K, V, out, kv_offsets, S_per_seq, sample_idx)
+    p = make_params(q, K, S, seed, step, nk, kv_offsets, S_per_seq, scale)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(workspace_size(p), q.device)
+    st = library().santa_decode(ctypes.byref(p), VARIANTS[variant], _ptr(q), _ptr(K), _ptr(V), _ptr(out),
+                                _ptr(workspace), workspace.numel(), _stream(stream), _ptr(sample_idx))
+    if st != SANTA_OK:
+        raise SantaError(st, "santa_decode")
+    return out
+
+
+def santa_decode_with_uniforms(q, K, V, uniforms, S: int, variant: str, out=None, nk=None, kv_offsets=None,
+                               S_per_seq=None, scale: float = 0.0, workspace=None, sample_idx=None,
+                               stream=None) -> torch.Tensor:
+    """santa_decode with explicit float64 uniforms [B, H, S] in place of Philox."""
+    _check_tensors(q, K, V, uniforms, out, kv_offsets, S_per_seq, sample_idx)
+    if uniforms.dtype != torch.float64:
+        raise ValueError("uniforms must be float64")
+    p = make_params(q, K, S, 0, 0, nk, kv_offsets, S_per_seq, scale)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(workspace_size(p), q.device)
+    st = library().santa_decode_with_uniforms(ctypes.byref(p), VARIANTS[variant], _ptr(q), _ptr(K), _ptr(V),
+                                              _ptr(uniforms), _ptr(out), _ptr(workspace), workspace.numel(),
+                                              _stream(stream), _ptr(sample_idx))
+    if st != SANTA_OK:
+        raise SantaError(st, "santa_decode_with_uniforms")
+    return out
+
+
+def santa_dense_decode(q, K, V, out=None, nk=None, kv_offsets=None, scale: float = 0.0, workspace=None,
+                       stream=None) -> torch.Tensor:
+    """Exact decode attention (this library's split-KV comparator)."""
+    _check_tensors(q, K, V, out, kv_offsets)
+    p = make_params(q, K, 1, 0, 0, nk, kv_offsets, None, scale)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(dense_workspace_size(p), q.device)
+    st = library().santa_dense_decode(ctypes.byref(p), _ptr(q), _ptr(K), _ptr(V), _ptr(out), _ptr(workspace),
+                                      workspace.numel(), _stream(stream))
+    if st != SANTA_OK:
+        raise SantaError(st, "santa_dense_decode")
+    return out
+
+
+class Decoder:
+    """Reusable decode call for fixed shapes: holds the parameter block, the
+    workspace and the output, so a step is one C-ABI call."""
+
+    def __init__(self, q, K, V, S: int, variant: str = "systematic", seed: int = 0, nk=None, kv_offsets=None,
+                 S_per_seq=None, scale: float = 0.0, dense: bool = False, sample_idx=None):
+        _check_tensors(q, K, V, kv_offsets, S_per_seq, sample_idx)
+        self.q, self.K, self.V = q, K, V
+        self.kv_offsets, self.S_per_seq, self.sample_idx = kv_offsets, S_per_seq, sample_idx
+        self.dense = dense
+        self.variant = VARIANTS[variant]
+        self.p = make_params(q, K, S, seed, 0, nk, kv_offsets, S_per_seq, scale)
+        n = dense_workspace_size(self.p) if dense else workspace_size(self.p)
+        if n == 0:
+            raise ValueError("invalid decode parameters")
+        self.workspace = alloc_workspace(n, q.device)
+        self.out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        self._args = None
+
+    def profiled(self, events, step: int = 0, stream=None) -> torch.Tensor:
+        """One step recording 4 torch.cuda.Event objects around the three stages."""
+        arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+        self.p.step = step
+        st = library().santa_decode_profiled(ctypes.byref(self.p), self.variant, _ptr(self.q), _ptr(self.K),
+                                             _ptr(self.V), _ptr(self.out), _ptr(self.workspace),
+                                             self.workspace.numel(), _stream(stream), _ptr(self.sample_idx), arr)
+        if st != SANTA_OK:
+            raise SantaError(st, "santa_decode_profiled")
+        return self.out
+
+    def __call__(self, step: int = 0, stream=None) -> torch.Tensor:
+        lib = library()
+        self.p.step = step
+        if self.dense:
+            st = lib.santa_dense_decode(ctypes.byref(self.p), _ptr(self.q), _ptr(self.K), _ptr(self.V),
+                                        _ptr(self.out), _ptr(self.workspace), self.workspace.numel(),
+                                        _stream(stream))
+        else:
+            st = lib.santa_decode(ctypes.byref(self.p), self.variant, _ptr(self.q), _ptr(self.K), _ptr(self.V),
+                                  _ptr(self.out), _ptr(self.workspace), self.workspace.numel(), _stream(stream),
+                                  _ptr(self.sample_idx))
+        if st != SANTA_OK:
+            raise SantaError(st, "santa_dense_decode" if self.dense else "santa_decode")
+        return self.out

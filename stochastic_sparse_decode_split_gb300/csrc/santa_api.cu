@@ -1,0 +1,234 @@
+// santa_api.cu -- C ABI of libsanta.so: host-side validation, workspace
+// layout and the launch sequence of one decode step.  Every check here runs
+// before any CUDA call, so argument errors never reach the device.
+#include <math.h>
+#include <string.h>
+
+#include "../../include/santa.h"
+#include "santa_common.cuh"
+#include "santa_launch.h"
+
+static_assert(SANTA_MAX_GROUP == SANTA_MAX_GROUP_DEV, "group limit");
+static_assert(SANTA_CHUNK == santa::CHUNK, "chunk length");
+
+namespace {
+
+constexpr size_t ALIGN = 256;
+constexpr size_t HEADER = 256;  // error word + padding
+
+size_t up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
+
+struct Layout {
+  size_t counters, stash, tile_max, tile_sum, prefix, thresh, jstart, head_max, part_o, total;
+  int64_t chunks, groups;
+};
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+santa_status_t check_params(const santa_params_t* p, bool need_S) {
+  if (!p) return SANTA_ERR_INVALID_ARG;
+  if (p->batch < 1 || p->n_q_heads < 1 || p->n_kv_heads < 1) return SANTA_ERR_INVALID_ARG;
+  if (p->n_q_heads % p->n_kv_heads) return SANTA_ERR_INVALID_ARG;
+  if (p->batch > 65535 || p->n_kv_heads > 65535 || p->n_q_heads > 65535) return SANTA_ERR_INVALID_ARG;
+  if (p->nk < 1 || p->nk > SANTA_MAX_NK) return SANTA_ERR_INVALID_ARG;
+  if (p->dtype < SANTA_BF16 || p->dtype > SANTA_FP32) return SANTA_ERR_UNSUPPORTED;
+  if (p->head_dim != 64 && p->head_dim != 128) return SANTA_ERR_UNSUPPORTED;
+  if (p->n_q_heads / p->n_kv_heads > SANTA_MAX_GROUP) return SANTA_ERR_UNSUPPORTED;
+  if (need_S && (p->S < 1 || p->S > SANTA_MAX_S)) return SANTA_ERR_INVALID_ARG;
+  if (!(p->scale == p->scale) || isinf(p->scale)) return SANTA_ERR_INVALID_ARG;
+  return SANTA_OK;
+}
+
+Layout santa_layout(const santa_params_t* p) {
+  Layout L;
+  const size_t B = (size_t)p->batch, H = (size_t)p->n_q_heads, Hkv = (size_t)p->n_kv_heads;
+  const size_t D = (size_t)p->head_dim, nk = (size_t)p->nk, S = (size_t)p->S;
+  L.chunks = (p->nk + SANTA_CHUNK - 1) / SANTA_CHUNK;
+  L.groups = (L.chunks + santa::GROUP_CHUNKS - 1) / santa::GROUP_CHUNKS;
+  size_t off = HEADER;
+  L.counters = off; off += up(B * Hkv * sizeof(unsigned));
+  L.stash = off;    off += up(B * H * nk * sizeof(float));
+  L.tile_max = off; off += up(B * H * (size_t)L.chunks * sizeof(float));
+  L.tile_sum = off; off += up(B * H * (size_t)L.chunks * sizeof(float));
+  L.prefix = off;   off += up(B * H * ((size_t)L.chunks + 1) * sizeof(double));
+  L.thresh = off;   off += up(B * H * S * sizeof(double));
+  L.jstart = off;   off += up(B * H * ((size_t)L.chunks + 1) * sizeof(int32_t));
+  L.head_max = off; off += up(B * H * sizeof(float));
+  L.part_o = off;   off += up(B * H * (size_t)L.groups * D * sizeof(float));
+  L.total = off;
+  return L;
+}
+
+Layout dense_layout(const santa_params_t* p) {
+  Layout L;
+  memset(&L, 0, sizeof L);
+  const size_t B = (size_t)p->batch, H = (size_t)p->n_q_heads, D = (size_t)p->head_dim;
+  L.chunks = (p->nk + SANTA_CHUNK - 1) / SANTA_CHUNK;
+  size_t off = HEADER;
+  L.tile_max = off; off += up(B * H * (size_t)L.chunks * sizeof(float));
+  L.tile_sum = off; off += up(B * H * (size_t)L.chunks * sizeof(float));
+  L.part_o = off;   off += up(B * H * (size_t)L.chunks * D * sizeof(float));
+  L.total = off;
+  return L;
+}
+
+santa_status_t check_buffers(const void* q, const void* K, const void* V, const void* out, const void* ws,
+                             size_t ws_bytes, size_t need) {
+  if (!q || !K || !V || !out) return SANTA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(out, 16)) return SANTA_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, ALIGN) || ws_bytes < need) return SANTA_ERR_WORKSPACE;
+  return SANTA_OK;
+}
+
+santa::LaunchArgs base_args(const santa_params_t* p, const Layout& L, const void* q, const void* K, const void* V,
+                            float* out, void* ws, cudaStream_t stream) {
+  santa::LaunchArgs a;
+  memset(&a, 0, sizeof a);
+  unsigned char* w = static_cast<unsigned char*>(ws);
+  a.dtype = p->dtype;
+  a.D = p->head_dim;
+  a.B = p->batch;
+  a.H = p->n_q_heads;
+  a.Hkv = p->n_kv_heads;
+  a.nk_max = p->nk;
+  a.chunks_max = (int)L.chunks;
+  a.groups_max = (int)L.groups;
+  a.S_max = p->S;
+  a.scale = p->scale > 0.f ? p->scale : (float)(1.0 / sqrt((double)p->head_dim));
+  a.seed = p->seed;
+  a.step = p->step;
+  a.q = q;
+  a.K = K;
+  a.V = V;
+  a.kv_offsets = p->kv_offsets;
+  a.S_per_seq = p->S_per_seq;
+  a.out = out;
+  a.err = reinterpret_cast<int*>(w);
+  a.tile_max = reinterpret_cast<float*>(w + L.tile_max);
+  a.tile_sum = reinterpret_cast<float*>(w + L.tile_sum);
+  a.part_o = reinterpret_cast<float*>(w + L.part_o);
+  a.stream = stream;
+  return a;
+}
+
+santa_status_t decode_impl(const santa_params_t* p, int32_t variant, const void* q, const void* K, const void* V,
+                           const double* uniforms, float* out, void* ws, size_t ws_bytes, santa_stream_t stream,
+                           int32_t* sample_idx, void* const* events = nullptr) {
+  santa_status_t st = check_params(p, true);
+  if (st != SANTA_OK) return st;
+  if (variant < SANTA_IID || variant > SANTA_SYSTEMATIC) return SANTA_ERR_INVALID_ARG;
+  const Layout L = santa_layout(p);
+  st = check_buffers(q, K, V, out, ws, ws_bytes, L.total);
+  if (st != SANTA_OK) return st;
+  if (sample_idx && !aligned(sample_idx, 4)) return SANTA_ERR_INVALID_ARG;
+  if (uniforms && !aligned(uniforms, 8)) return SANTA_ERR_INVALID_ARG;
+
+  santa::LaunchArgs a = base_args(p, L, q, K, V, out, ws, (cudaStream_t)stream);
+  unsigned char* w = static_cast<unsigned char*>(ws);
+  a.variant = variant;
+  a.uniforms = uniforms;
+  a.sample_idx = sample_idx;
+  a.counters = reinterpret_cast<unsigned*>(w + L.counters);
+  a.stash = reinterpret_cast<float*>(w + L.stash);
+  a.prefix = reinterpret_cast<double*>(w + L.prefix);
+  a.thresh = reinterpret_cast<double*>(w + L.thresh);
+  a.jstart = reinterpret_cast<int32_t*>(w + L.jstart);
+  a.head_max = reinterpret_cast<float*>(w + L.head_max);
+
+  auto mark = [&](int i) {
+    return !events || cudaEventRecord((cudaEvent_t)events[i], (cudaStream_t)stream) == cudaSuccess;
+  };
+  if (!mark(0) || santa::launch_score(a) != cudaSuccess) return SANTA_ERR_CUDA;
+  if (!mark(1) || santa::launch_combine(a) != cudaSuccess) return SANTA_ERR_CUDA;
+  if (!mark(2) || santa::launch_sample_gather(a) != cudaSuccess) return SANTA_ERR_CUDA;
+  if (!mark(3)) return SANTA_ERR_CUDA;
+  return SANTA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t santa_workspace_size(const santa_params_t* p) {
+  if (check_params(p, true) != SANTA_OK) return 0;
+  return santa_layout(p).total;
+}
+
+santa_status_t santa_workspace_init(void* workspace, size_t ws_bytes, santa_stream_t stream) {
+  if (!workspace || !aligned(workspace, ALIGN) || ws_bytes < HEADER) return SANTA_ERR_WORKSPACE;
+  return cudaMemsetAsync(workspace, 0, HEADER, (cudaStream_t)stream) == cudaSuccess ? SANTA_OK : SANTA_ERR_CUDA;
+}
+
+santa_status_t santa_decode(const santa_params_t* p, int32_t variant, const void* q, const void* K, const void* V,
+                            float* out, void* workspace, size_t ws_bytes, santa_stream_t stream,
+                            int32_t* sample_idx) {
+  return decode_impl(p, variant, q, K, V, nullptr, out, workspace, ws_bytes, stream, sample_idx);
+}
+
+santa_status_t santa_decode_profiled(const santa_params_t* p, int32_t variant, const void* q, const void* K,
+                                     const void* V, float* out, void* workspace, size_t ws_bytes,
+                                     santa_stream_t stream, int32_t* sample_idx, void* const* stage_events) {
+  return decode_impl(p, variant, q, K, V, nullptr, out, workspace, ws_bytes, stream, sample_idx, stage_events);
+}
+
+santa_status_t santa_decode_with_uniforms(const santa_params_t* p, int32_t variant, const void* q, const void* K,
+                                          const void* V, const double* uniforms, float* out, void* workspace,
+                                          size_t ws_bytes, santa_stream_t stream, int32_t* sample_idx) {
+  if (!uniforms) return SANTA_ERR_INVALID_ARG;
+  return decode_impl(p, variant, q, K, V, uniforms, out, workspace, ws_bytes, stream, sample_idx);
+}
+
+size_t santa_dense_workspace_size(const santa_params_t* p) {
+  if (check_params(p, false) != SANTA_OK) return 0;
+  return dense_layout(p).total;
+}
+
+santa_status_t santa_dense_decode(const santa_params_t* p, const void* q, const void* K, const void* V, float* out,
+                                  void* workspace, size_t ws_bytes, santa_stream_t stream) {
+  santa_status_t st = check_params(p, false);
+  if (st != SANTA_OK) return st;
+  const Layout L = dense_layout(p);
+  st = check_buffers(q, K, V, out, workspace, ws_bytes, L.total);
+  if (st != SANTA_OK) return st;
+  santa::LaunchArgs a = base_args(p, L, q, K, V, out, workspace, (cudaStream_t)stream);
+  return santa::launch_dense(a) == cudaSuccess ? SANTA_OK : SANTA_ERR_CUDA;
+}
+
+int32_t santa_workspace_layout(const santa_params_t* p, santa_ws_layout_t* layout) {
+  if (!layout || check_params(p, true) != SANTA_OK) return -1;
+  const Layout L = santa_layout(p);
+  layout->stash = L.stash;
+  layout->tile_max = L.tile_max;
+  layout->tile_sum = L.tile_sum;
+  layout->prefix = L.prefix;
+  layout->thresh = L.thresh;
+  layout->head_max = L.head_max;
+  layout->chunks = L.chunks;
+  return 0;
+}
+
+santa_status_t santa_get_error(void* workspace, santa_stream_t stream, int32_t* code) {
+  if (!workspace || !aligned(workspace, ALIGN)) return SANTA_ERR_WORKSPACE;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return SANTA_ERR_CUDA;
+  int32_t word = 0;
+  if (cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return SANTA_ERR_CUDA;
+  if (word && cudaMemset(workspace, 0, sizeof word) != cudaSuccess) return SANTA_ERR_CUDA;
+  if (code) *code = word;
+  return word ? SANTA_ERR_DEVICE : SANTA_OK;
+}
+
+const char* santa_status_string(santa_status_t status) {
+  switch (status) {
+    case SANTA_OK: return "ok";
+    case SANTA_ERR_INVALID_ARG: return "invalid argument";
+    case SANTA_ERR_UNSUPPORTED: return "unsupported head_dim, dtype or group size";
+    case SANTA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case SANTA_ERR_CUDA: return "CUDA runtime error";
+    case SANTA_ERR_DEVICE: return "device flagged bad ragged metadata";
+    default: return "unknown status";
+  }
+}
+
+int32_t santa_version(void) { return 100; }
+
+}  // extern "C"

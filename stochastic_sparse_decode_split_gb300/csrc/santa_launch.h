@@ -1,0 +1,51 @@
+// santa_launch.h -- internal interface between the C ABI (santa_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define SANTA_MAX_GROUP_DEV 8
+
+namespace santa {
+
+// Everything one decode call needs, already validated and carved out of the workspace.
+struct LaunchArgs {
+  int dtype;       // 0 bf16, 1 fp16, 2 fp32
+  int D;           // head_dim (64 or 128)
+  int B, H, Hkv;
+  int64_t nk_max;
+  int chunks_max;  // ceil(nk_max / CHUNK)
+  int groups_max;  // ceil(chunks_max / GROUP_CHUNKS)
+  int S_max;
+  int variant;
+  float scale;
+  uint64_t seed;
+  uint32_t step;
+  const void* q;
+  const void* K;
+  const void* V;
+  const int64_t* kv_offsets;
+  const int32_t* S_per_seq;
+  const double* uniforms;  // optional debug uniforms [B, H, S_max]
+  float* out;
+  int32_t* sample_idx;     // optional [B, H, S_max]
+  // workspace views
+  int* err;
+  unsigned* counters;      // [B * Hkv]
+  float* stash;            // [B, H, nk_max]
+  float* tile_max;         // [B, H, chunks_max]
+  float* tile_sum;         // [B, H, chunks_max]
+  double* prefix;          // [B, H, chunks_max + 1]
+  double* thresh;          // [B, H, S_max]
+  int32_t* jstart;         // [B, H, chunks_max + 1]
+  float* head_max;         // [B, H]
+  float* part_o;           // santa: [B, H, groups_max, D]; dense: [B, H, chunks_max, D]
+  cudaStream_t stream;
+};
+
+cudaError_t launch_score(const LaunchArgs& a);
+cudaError_t launch_combine(const LaunchArgs& a);
+cudaError_t launch_sample_gather(const LaunchArgs& a);
+cudaError_t launch_dense(const LaunchArgs& a);
+
+}  // namespace santa

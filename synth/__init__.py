@@ -204,3 +204,20 @@ def generate(wl: Workload, data_seed: int = 0) -> Inputs:
 def thrash_bytes_default() -> int:
     """Size of the buffer written between timed iterations (well above a 129 MB L2)."""
     return 512 * 1024 * 1024
+
+
+def to_torch(inp: Inputs, device="cuda"):
+    """Copies the storage arrays to torch tensors on `device` (bytes unchanged):
+    returns dict(q, K, V, kv_offsets, S_per_seq)."""
+    import torch
+    tdt = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[inp.wl.dtype]
+
+    def conv(a):
+        if inp.wl.dtype == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(tdt).to(device)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+    out = {"q": conv(inp.q), "K": conv(inp.K), "V": conv(inp.V),
+           "kv_offsets": torch.from_numpy(inp.kv_offsets.copy()).to(device),
+           "S_per_seq": None if inp.S_per_seq is None else torch.from_numpy(inp.S_per_seq.copy()).to(device)}
+    return out

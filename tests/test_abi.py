@@ -1,0 +1,104 @@
+"""C-ABI checks that need no GPU: the library builds for sm_103a, loads,
+exports every function include/santa.h declares, and rejects bad arguments on
+the host (before any CUDA call) with the documented status codes."""
+import ctypes
+import subprocess
+
+import pytest
+
+import stochastic_sparse_decode_split_gb300 as santa
+from stochastic_sparse_decode_split_gb300 import build as santa_build
+
+OK, INVALID, UNSUPPORTED, WORKSPACE = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    santa_build.build()
+    return santa.library()
+
+
+def params(**kw):
+    p = santa.Params()
+    p.batch, p.n_q_heads, p.n_kv_heads, p.head_dim = 1, 32, 8, 128
+    p.dtype, p.nk, p.S, p.scale, p.seed, p.step = 0, 32768, 256, 0.0, 0, 0
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = santa.exported_symbols()
+    assert {"santa_decode", "santa_dense_decode", "santa_workspace_size", "santa_get_error"} <= set(names)
+    out = subprocess.run(["nm", "-D", "--defined-only", santa_build.LIB], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    missing = [n for n in names if n not in exported]
+    assert not missing, f"declared but not exported: {missing}"
+    for n in names:
+        assert hasattr(lib, n)
+
+
+def test_status_strings_and_version(lib):
+    for code in range(6):
+        assert lib.santa_status_string(code)
+    assert lib.santa_status_string(99) == b"unknown status"
+    assert lib.santa_version() >= 100
+
+
+def test_workspace_size_valid_and_invalid(lib):
+    p = params()
+    n = santa.workspace_size(p)
+    # stash alone is B*H*nk fp32
+    assert n >= 32 * 32768 * 4
+    assert n % 256 == 0
+    assert santa.workspace_size(params(n_kv_heads=5)) == 0          # H % H_kv != 0
+    assert santa.workspace_size(params(head_dim=96)) == 0           # unsupported head_dim
+    assert santa.workspace_size(params(S=0)) == 0
+    assert santa.workspace_size(params(S=4097)) == 0
+    assert santa.workspace_size(params(nk=0)) == 0
+    assert santa.workspace_size(params(nk=(1 << 21) + 1)) == 0
+    assert santa.workspace_size(params(n_q_heads=72, n_kv_heads=8)) == 0   # group 9 > 8
+    assert santa.dense_workspace_size(params(S=0)) > 0                   # dense ignores S
+    lay = santa.workspace_layout(p)
+    assert lay["chunks"] == 128
+    offs = sorted(lay[k] for k in ("stash", "tile_max", "tile_sum", "prefix", "thresh", "head_max"))
+    assert offs[0] >= 256 and offs[-1] < n and all(o % 256 == 0 for o in offs)
+
+
+def _decode(lib, p, variant=2, q=256, K=256, V=256, out=256, ws=None, nbytes=0):
+    vp = ctypes.c_void_p
+    return lib.santa_decode(ctypes.byref(p), variant, vp(q), vp(K), vp(V), vp(out), vp(ws), nbytes, None, None)
+
+
+def test_host_validation_statuses(lib):
+    """Every case below fails a host check that precedes all CUDA calls."""
+    good = params()
+    n = santa.workspace_size(good)
+    assert _decode(lib, params(n_kv_heads=3)) == INVALID
+    assert _decode(lib, params(batch=0)) == INVALID
+    assert _decode(lib, params(S=0)) == INVALID
+    assert _decode(lib, params(head_dim=80)) == UNSUPPORTED
+    assert _decode(lib, params(dtype=7)) == UNSUPPORTED
+    assert _decode(lib, params(scale=float("nan"))) == INVALID
+    assert _decode(lib, good, variant=3) == INVALID
+    assert _decode(lib, good, q=0) == INVALID                     # NULL q
+    assert _decode(lib, good, K=264) == INVALID                   # K not 16-byte aligned
+    assert _decode(lib, good, ws=None, nbytes=n) == WORKSPACE     # no workspace
+    assert _decode(lib, good, ws=512 + 16, nbytes=n) == WORKSPACE  # misaligned workspace
+    assert _decode(lib, good, ws=512, nbytes=n - 256) == WORKSPACE  # too small
+    vp = ctypes.c_void_p
+    assert lib.santa_decode_with_uniforms(ctypes.byref(good), 2, vp(256), vp(256), vp(256), None, vp(256), vp(512),
+                                          n, None, None) == INVALID
+    assert lib.santa_dense_decode(ctypes.byref(params(head_dim=32)), vp(256), vp(256), vp(256), vp(256), vp(512),
+                                  1 << 30, None) == UNSUPPORTED
+    assert lib.santa_workspace_init(None, 1024, None) == WORKSPACE
+    assert lib.santa_get_error(vp(512 + 8), None, None) == WORKSPACE
+
+
+def test_python_binding_rejects_cpu_tensors():
+    import torch
+    q = torch.zeros(1, 4, 64, dtype=torch.bfloat16)
+    K = torch.zeros(16, 1, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        santa.santa_decode(q, K, K, S=4)

@@ -1,0 +1,320 @@
+"""GPU parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+Contract (SANTA / S2ANTA, "Stochastic Sparse Attention for Memory-Bound
+Inference"): on the same generated inputs and Philox seed, every drawn key
+index equals the oracle's except draws whose threshold lies within 1e-6 of a
+CDF edge (counted, and checked to be admissible); outputs agree within 1e-3
+relative L2 per head (against the oracle's gather of the GPU's own indices
+where a boundary draw differs); over 10^4 seeds the mean estimate lies within
+4 sigma of the exact attention output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import stochastic_sparse_decode_split_gb300 as santa
+from oracle import analysis
+
+pytestmark = pytest.mark.gpu
+BAND = 1e-6      # boundary band of the CDF (absolute, normalised mass)
+OUT_TOL = 1e-3   # relative L2 per head
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    santa.library()   # raises if the CUDA library was not built
+
+
+def wl_of(name, B, H, Hkv, d, nk, dtype, S, variant, **kw):
+    return synth.Workload(name, B, H, Hkv, d, nk, dtype, S, variant, **kw)
+
+
+def run_gpu(inp, variant, seed=0, step=0, workspace=None):
+    t = synth.to_torch(inp)
+    B, H, _ = inp.q.shape
+    ragged = inp.wl.ragged is not None
+    S_max = inp.S_max
+    idx = torch.full((B, H, S_max), -7, dtype=torch.int32, device="cuda")
+    nk = int(inp.nk_per_seq.max()) if ragged else None
+    out = santa.santa_decode(t["q"], t["K"], t["V"], S=S_max, variant=variant, seed=seed, step=step, nk=nk,
+                             kv_offsets=t["kv_offsets"] if ragged else None, S_per_seq=t["S_per_seq"],
+                             sample_idx=idx, workspace=workspace)
+    torch.cuda.synchronize()
+    return out.double().cpu().numpy(), idx.cpu().numpy()
+
+
+def check_parity(inp, variant, seed, out, idx, step=0, tol=OUT_TOL):
+    """Index-exact (outside the band) and output parity for every head."""
+    P = oracle.Problem.from_inputs(inp)
+    est, J, delta = oracle.decode(P, variant, inp.wl.S, seed, step, S_per_seq=inp.S_per_seq)
+    B, H, _ = inp.q.shape
+    n_draws = n_boundary = n_diff = 0
+    worst = 0.0
+    for b in range(B):
+        S_b = inp.S_of(b)
+        assert np.all(idx[b, :, S_b:] == -1)
+        for h in range(H):
+            Jg, Jo, dl = idx[b, h, :S_b], J[b, h, :S_b], delta[b, h, :S_b]
+            strict = dl > BAND
+            bad = np.nonzero(strict & (Jg != Jo))[0]
+            assert bad.size == 0, (f"(b={b}, h={h}) draws {bad[:8]} differ away from a CDF edge: "
+                                   f"gpu {Jg[bad[:8]]} oracle {Jo[bad[:8]]} delta {dl[bad[:8]]}")
+            diff = np.nonzero(Jg != Jo)[0]
+            n_draws += S_b
+            n_boundary += int((~strict).sum())
+            n_diff += diff.size
+            if diff.size:
+                t = oracle.thresholds(variant, S_b, seed, b, h, step)
+                _, p = oracle.scores(P, b, h)
+                F = np.cumsum(p)
+                for j in diff:
+                    n = int(Jg[j])
+                    lo = F[n - 1] if n > 0 else 0.0
+                    assert 0 <= n < inp.nk_per_seq[b] and lo - BAND <= t[j] < F[n] + BAND
+                ref = oracle.gather(P, b, h, Jg)
+            else:
+                ref = est[b, h]
+            rel = np.linalg.norm(out[b, h] - ref) / max(np.linalg.norm(ref), 1e-30)
+            worst = max(worst, rel)
+            assert rel <= tol, f"(b={b}, h={h}) relative L2 {rel:.3e}"
+    return {"draws": n_draws, "boundary": n_boundary, "differing": n_diff, "worst_rel_l2": worst}
+
+
+# ---------------------------------------------------------------------------
+# worked example, tiny workload, stage-level parity
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("variant,u", [("iid", [0.8, 0.1, 0.3]), ("systematic", [0.3, 0.0, 0.0]),
+                                       ("stratified", [0.3, 0.9, 0.4])])
+def test_worked_example_nk3(variant, u):
+    """Sec. 1, Eq. (2)-(3): draws e1, e1, e3 over nk = 3 give (V1 + V1 + V3)/3."""
+    import json, os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "worked_example_nk3.json")))
+    d = 64
+    q = torch.zeros(1, 1, d, dtype=torch.float32)
+    q[0, 0, 0] = 1.0
+    K = torch.zeros(3, 1, d, dtype=torch.float32)
+    K[:, 0, 0] = torch.log(torch.tensor(g["p"], dtype=torch.float64)).float()
+    V = torch.zeros(3, 1, d, dtype=torch.float32)
+    V[:, 0, :4] = torch.tensor(g["V"], dtype=torch.float32)
+    uni = torch.tensor(u, dtype=torch.float64).view(1, 1, 3).cuda()
+    idx = torch.full((1, 1, 3), -7, dtype=torch.int32, device="cuda")
+    out = santa.santa_decode_with_uniforms(q.cuda(), K.cuda(), V.cuda(), uni, S=3, variant=variant, scale=1.0,
+                                           sample_idx=idx)
+    torch.cuda.synchronize()
+    assert (idx.cpu().numpy()[0, 0] + 1).tolist() == g["sampled_keys_one_based"]
+    Vd = np.array(g["V"], np.float64)
+    np.testing.assert_allclose(out.cpu().numpy()[0, 0, :4], (Vd[0] + Vd[0] + Vd[2]) / 3, rtol=1e-6, atol=1e-6)
+    assert np.all(out.cpu().numpy()[0, 0, 4:] == 0)
+
+
+@pytest.mark.parametrize("variant", ["iid", "stratified", "systematic"])
+def test_tiny_workload(variant):
+    inp = synth.generate(synth.tiny(variant), 0)
+    for seed in range(20):
+        out, idx = run_gpu(inp, variant, seed)
+        rep = check_parity(inp, variant, seed, out, idx)
+        assert rep["differing"] == 0
+
+
+def test_score_stage_and_chunk_stats():
+    """Stash = fp32 scores (Eq. 1) and per-chunk (max, exp-sum) (App. O, Alg. 3)."""
+    wl = wl_of("stage", 2, 8, 2, 128, 1100, "bf16", 64, "systematic")
+    inp = synth.generate(wl, 5)
+    t = synth.to_torch(inp)
+    p = santa.make_params(t["q"], t["K"], 64)
+    ws = santa.alloc_workspace(santa.workspace_size(p), "cuda")
+    run_gpu(inp, "systematic", 3, workspace=ws)
+    lay = santa.workspace_layout(p)
+    C = lay["chunks"]
+    wsn = ws.cpu().numpy()
+    stash = wsn[lay["stash"]:lay["stash"] + 2 * 8 * 1100 * 4].view(np.float32).reshape(2, 8, 1100)
+    tmax = wsn[lay["tile_max"]:lay["tile_max"] + 2 * 8 * C * 4].view(np.float32).reshape(2, 8, C)
+    tsum = wsn[lay["tile_sum"]:lay["tile_sum"] + 2 * 8 * C * 4].view(np.float32).reshape(2, 8, C)
+    hmax = wsn[lay["head_max"]:lay["head_max"] + 2 * 8 * 4].view(np.float32).reshape(2, 8)
+    P = oracle.Problem.from_inputs(inp)
+    for b in range(2):
+        for h in range(8):
+            s, _ = oracle.scores(P, b, h)
+            np.testing.assert_allclose(stash[b, h], s, rtol=2e-6, atol=2e-6)
+            m, l = oracle.tile_stats(P, b, h, santa_chunk())
+            np.testing.assert_allclose(tmax[b, h], m, rtol=2e-6, atol=2e-6)
+            np.testing.assert_allclose(tsum[b, h], l, rtol=1e-5)
+            assert abs(hmax[b, h] - s.max()) <= 2e-6 * (1 + abs(s.max()))
+
+
+def santa_chunk():
+    return 256
+
+
+# ---------------------------------------------------------------------------
+# parity grid: dtypes, head dims, group sizes, ragged tails, budgets
+# ---------------------------------------------------------------------------
+
+GRID = [
+    # B, H, Hkv, d, nk, dtype, S, variant
+    (2, 8, 2, 128, 3000, "bf16", 64, "systematic"),
+    (2, 8, 2, 128, 3000, "bf16", 256, "stratified"),
+    (1, 8, 2, 128, 3000, "bf16", 37, "iid"),
+    (2, 14, 2, 128, 2000, "fp16", 256, "systematic"),   # group 7 (two head passes)
+    (1, 16, 2, 64, 1500, "bf16", 16, "stratified"),     # group 8, d = 64
+    (1, 4, 2, 128, 700, "fp32", 8, "iid"),
+    (1, 2, 2, 64, 513, "fp16", 1, "systematic"),        # S = 1, group 1
+    (1, 8, 2, 128, 1, "bf16", 5, "systematic"),         # a single key
+    (1, 4, 1, 128, 257, "bf16", 4096, "stratified"),    # maximum S
+    (1, 6, 2, 128, 2049, "bf16", 100, "iid"),           # group 3
+    (3, 10, 2, 64, 777, "fp32", 33, "stratified"),      # group 5
+]
+
+
+@pytest.mark.parametrize("B,H,Hkv,d,nk,dtype,S,variant", GRID)
+def test_parity_grid(B, H, Hkv, d, nk, dtype, S, variant):
+    inp = synth.generate(wl_of("grid", B, H, Hkv, d, nk, dtype, S, variant), 11)
+    for seed in (0, 1, 12345):
+        out, idx = run_gpu(inp, variant, seed, step=seed % 3)
+        check_parity(inp, variant, seed, out, idx, step=seed % 3)
+
+
+def test_ragged_batch_with_per_sequence_budgets():
+    wl = wl_of("ragged_small", 6, 8, 2, 128, 3000, "bf16", 300, "stratified", ragged=(1, 3000))
+    inp = synth.generate(wl, 2)
+    # force the interesting lengths: 1, 255, 256, 257 keys
+    lens = np.array([1, 255, 256, 257, 1000, 3000])
+    inp = _with_lengths(inp, lens)
+    inp.S_per_seq = np.array([1, 7, 256, 300, 64, 129], np.int32)
+    for variant in ("iid", "stratified", "systematic"):
+        out, idx = run_gpu(inp, variant, 9)
+        check_parity(inp, variant, 9, out, idx)
+
+
+def _with_lengths(inp, lens):
+    offs = np.zeros(len(lens) + 1, np.int64)
+    offs[1:] = np.cumsum(lens)
+    inp.kv_offsets = offs
+    inp.K = np.ascontiguousarray(inp.K[:offs[-1]])
+    inp.V = np.ascontiguousarray(inp.V[:offs[-1]])
+    inp.wl.ragged = (int(lens.min()), int(lens.max()))
+    return inp
+
+
+def test_determinism_and_step_keying():
+    inp = synth.generate(wl_of("det", 1, 8, 2, 128, 4000, "bf16", 256, "systematic"), 4)
+    o1, i1 = run_gpu(inp, "systematic", 7, step=0)
+    o2, i2 = run_gpu(inp, "systematic", 7, step=0)
+    assert np.array_equal(i1, i2) and np.array_equal(o1, o2)
+    o3, i3 = run_gpu(inp, "systematic", 7, step=1)
+    assert not np.array_equal(i1, i3)
+    o4, i4 = run_gpu(inp, "systematic", 8, step=0)
+    assert not np.array_equal(i1, i4)
+
+
+def test_device_flags_bad_ragged_metadata():
+    """A sequence longer than the stated bound or a budget out of range is
+    flagged in the workspace error word; its heads come out zero and the
+    other sequences are unaffected."""
+    wl = wl_of("flags", 3, 4, 2, 128, 600, "bf16", 32, "systematic", ragged=(600, 600))
+    inp = synth.generate(wl, 1)
+    t = synth.to_torch(inp)
+    S_per = torch.tensor([32, 0, 16], dtype=torch.int32, device="cuda")    # S_1 = 0 is out of range
+    offs = torch.tensor([0, 600, 1200, 1800], dtype=torch.int64, device="cuda")
+    p = santa.make_params(t["q"], t["K"], 32, nk=500, kv_offsets=offs, S_per_seq=S_per)  # bound 500 < 600
+    ws = santa.alloc_workspace(santa.workspace_size(p), "cuda")
+    out = santa.santa_decode(t["q"], t["K"], t["V"], S=32, nk=500, kv_offsets=offs, S_per_seq=S_per, workspace=ws)
+    code = santa.get_error(ws)
+    assert code & 1 and code & 2
+    assert torch.count_nonzero(out) == 0
+    assert santa.get_error(ws) == 0        # cleared by the read
+    offs_ok = torch.tensor([0, 600, 1000, 1800], dtype=torch.int64, device="cuda")
+    out = santa.santa_decode(t["q"], t["K"], t["V"], S=32, nk=800, kv_offsets=offs_ok,
+                             S_per_seq=torch.tensor([32, 0, 16], dtype=torch.int32, device="cuda"))
+    assert torch.count_nonzero(out[1]) == 0 and torch.count_nonzero(out[0]) > 0
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads (every head checked)
+# ---------------------------------------------------------------------------
+
+def test_full_size_llama32k_systematic():
+    inp = synth.generate(synth.llama32k(), 0)
+    out, idx = run_gpu(inp, "systematic", 0)
+    rep = check_parity(inp, "systematic", 0, out, idx)
+    print("llama32k parity:", rep)
+
+
+@pytest.mark.slow
+def test_full_size_qwen_batched():
+    inp = synth.generate(synth.qwen_batched(), 0)
+    out, idx = run_gpu(inp, "systematic", 0)
+    rep = check_parity(inp, "systematic", 0, out, idx)
+    print("qwen batched parity:", rep)
+
+
+@pytest.mark.slow
+def test_full_size_ragged_batch():
+    inp = synth.generate(synth.ragged(), 0)
+    out, idx = run_gpu(inp, "stratified", 0)
+    rep = check_parity(inp, "stratified", 0, out, idx)
+    print("ragged parity:", rep)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("nk,S,variant", [(4096, 1024, "stratified"), (131072, 64, "systematic"),
+                                          (65536, 256, "stratified")])
+def test_sweep_points(nk, S, variant):
+    inp = synth.generate(synth.llama32k(nk=nk, S=S, variant=variant), 0)
+    out, idx = run_gpu(inp, variant, 1)
+    check_parity(inp, variant, 1, out, idx)
+
+
+# ---------------------------------------------------------------------------
+# statistics over 10^4 Philox seeds
+# ---------------------------------------------------------------------------
+
+def _seed_sweep(inp, variant, R):
+    t = synth.to_torch(inp)
+    dec = santa.Decoder(t["q"], t["K"], t["V"], S=inp.wl.S, variant=variant)
+    s1 = torch.zeros(inp.q.shape, dtype=torch.float64, device="cuda")
+    s2 = torch.zeros_like(s1)
+    for seed in range(R):
+        dec.p.seed = seed
+        o = dec(step=0).double()
+        s1 += o
+        s2 += o * o
+    torch.cuda.synchronize()
+    mean = (s1 / R).cpu().numpy()
+    var = ((s2 - s1 * s1 / R) / (R - 1)).clamp_min(0).cpu().numpy()
+    return mean, var
+
+
+@pytest.mark.parametrize("variant", ["iid", "stratified", "systematic"])
+@pytest.mark.parametrize("which", ["tiny", "llama_heads"])
+def test_mean_over_10k_seeds_within_4_sigma(variant, which):
+    if which == "tiny":
+        inp = synth.generate(synth.tiny(variant), 0)
+    else:
+        inp = synth.generate(wl_of("stat", 1, 8, 2, 128, 2048, "bf16", 64, variant), 6)
+    R = 10000
+    mean, var_emp = _seed_sweep(inp, variant, R)
+    P = oracle.Problem.from_inputs(inp)
+    mu = oracle.dense(P)
+    B, H, _ = inp.q.shape
+    for b in range(B):
+        for h in range(H):
+            _, p = oracle.scores(P, b, h)
+            kvh = h // inp.wl.group
+            V = synth.storage_to_f64(inp.V[inp.kv_offsets[b]:inp.kv_offsets[b + 1], kvh], inp.wl.dtype)
+            S = inp.S_of(b)
+            if variant == "iid":
+                var = analysis.iid_coordinate_variance(p, V, S)
+            elif variant == "stratified":
+                var = analysis.stratified_coordinate_variance(p, V, S)
+            else:
+                var = var_emp[b, h]   # replicate estimate (no closed form for systematic)
+            # standard error of the mean, floored by fp32 rounding of one estimate
+            se = np.sqrt(var / R + (2e-6 * np.abs(V).max()) ** 2)
+            dev = np.abs(mean[b, h] - mu[b, h])
+            assert np.all(dev <= 4 * se), f"(b={b}, h={h}) max z {np.max(dev / se):.2f}"

@@ -128,6 +128,10 @@ def test_worked_example_nk3(oracle_lib):
     assert {str(k + 1): int(c) for k, c in enumerate(counts)} == g["counts_one_based"]
     np.testing.assert_allclose(est, (V[0] + V[0] + V[2]) / 3.0, rtol=1e-15, atol=1e-15)
     assert delta.min() > 0.05
+    # the same estimate from the index multiset alone (Eq. 2-3 by distributivity)
+    idx = np.array(g["sampled_keys_one_based"]) - 1
+    np.testing.assert_allclose(oracle_lib.gather(P, 0, 0, idx), (V[0] + V[0] + V[2]) / 3.0, rtol=1e-15,
+                               atol=1e-15)
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
