@@ -82,13 +82,13 @@ typedef struct {
 #define SANTA_MAX_S 4096        /* S (and every S_b) */
 #define SANTA_MAX_NK (1 << 21)  /* keys per sequence */
 #define SANTA_MAX_GROUP 8       /* n_q_heads / n_kv_heads */
-#define SANTA_CHUNK 256         /* keys per score / sampling chunk */
+#define SANTA_CHUNK 16          /* keys per statistics chunk */
 
 /* Byte size of the workspace santa_decode needs for these parameters
  * (0 when the parameters are invalid).  The variant does not change it. */
 size_t santa_workspace_size(const santa_params_t* p);
 
-/* Clears the workspace's control words (error word and hand-off counters).
+/* Clears the workspace's control word (the device error word).
  * Call once after allocating a workspace, before its first use. */
 santa_status_t santa_workspace_init(void* workspace, size_t ws_bytes, santa_stream_t stream);
 
@@ -101,7 +101,10 @@ santa_status_t santa_workspace_init(void* workspace, size_t ws_bytes, santa_stre
  *              j >= S_b are -1.  NULL skips it.
  * Stages: score pass with per-chunk (max, exp-sum) and a score stash; per-head
  * combine into chunk mass prefixes and Philox thresholds; per-chunk inverse
- * CDF, GQA row union and V gather-add with a deterministic reduction. */
+ * CDF, GQA row union and V gather-add.  The drawn indices are a deterministic
+ * function of (inputs, seed, step); the fp32 partial sums of the gather are
+ * added into out in an unspecified order, so its last bits may vary between
+ * runs. */
 santa_status_t santa_decode(const santa_params_t* p, int32_t variant, const void* q, const void* K,
                             const void* V, float* out, void* workspace, size_t ws_bytes,
                             santa_stream_t stream, int32_t* sample_idx);
@@ -115,8 +118,16 @@ santa_status_t santa_decode_profiled(const santa_params_t* p, int32_t variant, c
                                      const void* V, float* out, void* workspace, size_t ws_bytes,
                                      santa_stream_t stream, int32_t* sample_idx, void* const* stage_events);
 
+/* Only the first stage of santa_decode: scores over the whole cache (Sec. 2,
+ * Eq. 1) and the per-chunk statistics of App. O, Alg. 3, written to the
+ * workspace (stash and tile statistics, see santa_workspace_layout).  Same
+ * argument rules as santa_decode.  For timing or inspecting that stage. */
+santa_status_t santa_score_pass(const santa_params_t* p, const void* q, const void* K, void* workspace,
+                                size_t ws_bytes, santa_stream_t stream);
+
 /* santa_decode with caller-supplied uniforms in place of Philox: device float64
- * u[batch, n_q_heads, S] in [0,1) (only u[...,0] is read for SANTA_SYSTEMATIC).
+ * u[batch, n_q_heads, S] in [0,1) (only u[...,0] is read for SANTA_SYSTEMATIC;
+ * SANTA_IID sorts them at the 2^-24 resolution of the Philox uniforms).
  * For checking the sampler against hand-made cases such as the nk = 3 worked
  * example of Sec. 1 (Eq. 2-3). */
 santa_status_t santa_decode_with_uniforms(const santa_params_t* p, int32_t variant, const void* q,
@@ -137,8 +148,9 @@ santa_status_t santa_dense_decode(const santa_params_t* p, const void* q, const 
  *   stash     float32 [batch, n_q_heads, nk]        scaled scores s_n
  *   tile_max  float32 [batch, n_q_heads, chunks]    per-chunk max of s_n
  *   tile_sum  float32 [batch, n_q_heads, chunks]    per-chunk sum of exp(s_n - tile_max)
- *   prefix    float64 [batch, n_q_heads, chunks+1]  chunk mass prefix, relative to the head max
- *   thresh    float64 [batch, n_q_heads, S]         sorted thresholds t_j * Z
+ *   prefix    int64   [batch, n_q_heads, chunks+1]  chunk mass prefix in units of 2^-40 of the
+ *                                                   head-max key's mass (exact integer sums)
+ *   thresh    int64   [batch, n_q_heads, S]         sorted thresholds t_j * Z, same units
  *   head_max  float32 [batch, n_q_heads]            max_n s_n
  * with chunks = ceil(nk / SANTA_CHUNK).  Returns 0 on success. */
 typedef struct {

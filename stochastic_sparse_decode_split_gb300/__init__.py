@@ -89,6 +89,7 @@ def library():
             lib.santa_workspace_init.argtypes = [vp, sz, vp]
             lib.santa_decode.argtypes = [P, i32, vp, vp, vp, vp, vp, sz, vp, vp]
             lib.santa_decode_profiled.argtypes = [P, i32, vp, vp, vp, vp, vp, sz, vp, vp, vp]
+            lib.santa_score_pass.argtypes = [P, vp, vp, vp, sz, vp]
             lib.santa_decode_with_uniforms.argtypes = [P, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp]
             lib.santa_dense_decode.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
             lib.santa_workspace_layout.argtypes = [P, ctypes.POINTER(WsLayout)]
@@ -96,7 +97,8 @@ def library():
             lib.santa_status_string.argtypes = [i32]
             lib.santa_status_string.restype = ctypes.c_char_p
             lib.santa_version.restype = i32
-            for fn in ("santa_workspace_init", "santa_decode", "santa_decode_profiled", "santa_decode_with_uniforms", "santa_dense_decode",
+            for fn in ("santa_workspace_init", "santa_decode", "santa_decode_profiled", "santa_score_pass",
+                       "santa_decode_with_uniforms", "santa_dense_decode",
                        "santa_workspace_layout", "santa_get_error"):
                 getattr(lib, fn).restype = i32
             _lib = lib
@@ -259,8 +261,18 @@ class Decoder:
         self.out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
         self._args = None
 
+    def score_pass(self, stream=None) -> None:
+        """Only the score pass (stash and chunk statistics in the workspace)."""
+        st = library().santa_score_pass(ctypes.byref(self.p), _ptr(self.q), _ptr(self.K), _ptr(self.workspace),
+                                        self.workspace.numel(), _stream(stream))
+        if st != SANTA_OK:
+            raise SantaError(st, "santa_score_pass")
+
     def profiled(self, events, step: int = 0, stream=None) -> torch.Tensor:
-        """One step recording 4 torch.cuda.Event objects around the three stages."""
+        """One step recording 4 torch.cuda.Event objects around the three stages
+        (each event must have been recorded once so that it exists)."""
+        if any(e.cuda_event == 0 for e in events):
+            raise ValueError("record each event once before passing it (torch creates events lazily)")
         arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
         self.p.step = step
         st = library().santa_decode_profiled(ctypes.byref(self.p), self.variant, _ptr(self.q), _ptr(self.K),

@@ -9,7 +9,7 @@
 #include "santa_launch.h"
 
 static_assert(SANTA_MAX_GROUP == SANTA_MAX_GROUP_DEV, "group limit");
-static_assert(SANTA_CHUNK == santa::CHUNK, "chunk length");
+static_assert(SANTA_CHUNK == santa::SUB, "chunk length");
 
 namespace {
 
@@ -19,11 +19,23 @@ constexpr size_t HEADER = 256;  // error word + padding
 size_t up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
 
 struct Layout {
-  size_t counters, stash, tile_max, tile_sum, prefix, thresh, jstart, head_max, part_o, total;
+  size_t stash, tile_max, tile_sum, prefix, thresh, jstart, head_max, part_o, total;
   int64_t chunks, groups;
 };
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Multiprocessor count of the current device, cached per device.
+int device_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64 && cached[dev]) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev < 64) cached[dev] = n;
+  return n;
+}
 
 santa_status_t check_params(const santa_params_t* p, bool need_S) {
   if (!p) return SANTA_ERR_INVALID_ARG;
@@ -41,20 +53,19 @@ santa_status_t check_params(const santa_params_t* p, bool need_S) {
 
 Layout santa_layout(const santa_params_t* p) {
   Layout L;
-  const size_t B = (size_t)p->batch, H = (size_t)p->n_q_heads, Hkv = (size_t)p->n_kv_heads;
-  const size_t D = (size_t)p->head_dim, nk = (size_t)p->nk, S = (size_t)p->S;
+  const size_t B = (size_t)p->batch, H = (size_t)p->n_q_heads;
+  const size_t nk = (size_t)p->nk, S = (size_t)p->S;
   L.chunks = (p->nk + SANTA_CHUNK - 1) / SANTA_CHUNK;
-  L.groups = (L.chunks + santa::GROUP_CHUNKS - 1) / santa::GROUP_CHUNKS;
+  L.groups = ((p->nk + santa::WIN - 1) / santa::WIN + santa::SPC - 1) / santa::SPC;
   size_t off = HEADER;
-  L.counters = off; off += up(B * Hkv * sizeof(unsigned));
   L.stash = off;    off += up(B * H * nk * sizeof(float));
   L.tile_max = off; off += up(B * H * (size_t)L.chunks * sizeof(float));
   L.tile_sum = off; off += up(B * H * (size_t)L.chunks * sizeof(float));
-  L.prefix = off;   off += up(B * H * ((size_t)L.chunks + 1) * sizeof(double));
-  L.thresh = off;   off += up(B * H * S * sizeof(double));
+  L.prefix = off;   off += up(B * H * ((size_t)L.chunks + 1) * sizeof(long long));
+  L.thresh = off;   off += up(B * H * S * sizeof(long long));
   L.jstart = off;   off += up(B * H * ((size_t)L.chunks + 1) * sizeof(int32_t));
   L.head_max = off; off += up(B * H * sizeof(float));
-  L.part_o = off;   off += up(B * H * (size_t)L.groups * D * sizeof(float));
+  L.part_o = 0;
   L.total = off;
   return L;
 }
@@ -63,7 +74,7 @@ Layout dense_layout(const santa_params_t* p) {
   Layout L;
   memset(&L, 0, sizeof L);
   const size_t B = (size_t)p->batch, H = (size_t)p->n_q_heads, D = (size_t)p->head_dim;
-  L.chunks = (p->nk + SANTA_CHUNK - 1) / SANTA_CHUNK;
+  L.chunks = (p->nk + santa::DCHUNK - 1) / santa::DCHUNK;
   size_t off = HEADER;
   L.tile_max = off; off += up(B * H * (size_t)L.chunks * sizeof(float));
   L.tile_sum = off; off += up(B * H * (size_t)L.chunks * sizeof(float));
@@ -93,6 +104,8 @@ santa::LaunchArgs base_args(const santa_params_t* p, const Layout& L, const void
   a.nk_max = p->nk;
   a.chunks_max = (int)L.chunks;
   a.groups_max = (int)L.groups;
+  a.tiles_max = (int)((p->nk + santa::TILE - 1) / santa::TILE);
+  a.num_sms = device_sms();
   a.S_max = p->S;
   a.scale = p->scale > 0.f ? p->scale : (float)(1.0 / sqrt((double)p->head_dim));
   a.seed = p->seed;
@@ -113,12 +126,13 @@ santa::LaunchArgs base_args(const santa_params_t* p, const Layout& L, const void
 
 santa_status_t decode_impl(const santa_params_t* p, int32_t variant, const void* q, const void* K, const void* V,
                            const double* uniforms, float* out, void* ws, size_t ws_bytes, santa_stream_t stream,
-                           int32_t* sample_idx, void* const* events = nullptr) {
+                           int32_t* sample_idx, void* const* events = nullptr, bool score_only = false) {
   santa_status_t st = check_params(p, true);
   if (st != SANTA_OK) return st;
   if (variant < SANTA_IID || variant > SANTA_SYSTEMATIC) return SANTA_ERR_INVALID_ARG;
   const Layout L = santa_layout(p);
-  st = check_buffers(q, K, V, out, ws, ws_bytes, L.total);
+  st = score_only ? check_buffers(q, K, K, K, ws, ws_bytes, L.total)
+                  : check_buffers(q, K, V, out, ws, ws_bytes, L.total);
   if (st != SANTA_OK) return st;
   if (sample_idx && !aligned(sample_idx, 4)) return SANTA_ERR_INVALID_ARG;
   if (uniforms && !aligned(uniforms, 8)) return SANTA_ERR_INVALID_ARG;
@@ -128,16 +142,16 @@ santa_status_t decode_impl(const santa_params_t* p, int32_t variant, const void*
   a.variant = variant;
   a.uniforms = uniforms;
   a.sample_idx = sample_idx;
-  a.counters = reinterpret_cast<unsigned*>(w + L.counters);
   a.stash = reinterpret_cast<float*>(w + L.stash);
-  a.prefix = reinterpret_cast<double*>(w + L.prefix);
-  a.thresh = reinterpret_cast<double*>(w + L.thresh);
+  a.prefix = reinterpret_cast<long long*>(w + L.prefix);
+  a.thresh = reinterpret_cast<long long*>(w + L.thresh);
   a.jstart = reinterpret_cast<int32_t*>(w + L.jstart);
   a.head_max = reinterpret_cast<float*>(w + L.head_max);
 
   auto mark = [&](int i) {
     return !events || cudaEventRecord((cudaEvent_t)events[i], (cudaStream_t)stream) == cudaSuccess;
   };
+  if (score_only) return santa::launch_score(a) == cudaSuccess ? SANTA_OK : SANTA_ERR_CUDA;
   if (!mark(0) || santa::launch_score(a) != cudaSuccess) return SANTA_ERR_CUDA;
   if (!mark(1) || santa::launch_combine(a) != cudaSuccess) return SANTA_ERR_CUDA;
   if (!mark(2) || santa::launch_sample_gather(a) != cudaSuccess) return SANTA_ERR_CUDA;
@@ -163,6 +177,12 @@ santa_status_t santa_decode(const santa_params_t* p, int32_t variant, const void
                             float* out, void* workspace, size_t ws_bytes, santa_stream_t stream,
                             int32_t* sample_idx) {
   return decode_impl(p, variant, q, K, V, nullptr, out, workspace, ws_bytes, stream, sample_idx);
+}
+
+santa_status_t santa_score_pass(const santa_params_t* p, const void* q, const void* K, void* workspace,
+                                size_t ws_bytes, santa_stream_t stream) {
+  return decode_impl(p, SANTA_SYSTEMATIC, q, K, K, nullptr, nullptr, workspace, ws_bytes, stream, nullptr, nullptr,
+                     true);
 }
 
 santa_status_t santa_decode_profiled(const santa_params_t* p, int32_t variant, const void* q, const void* K,

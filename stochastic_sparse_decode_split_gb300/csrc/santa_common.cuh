@@ -9,11 +9,17 @@
 namespace santa {
 
 constexpr unsigned FULL = 0xffffffffu;
-constexpr int CHUNK = 256;          // keys per score / sampling chunk
-constexpr int WARPS = 8;            // warps per CTA in the chunked kernels
+constexpr int SUB = 16;             // keys per statistics chunk (one tensor-core m-tile)
+constexpr int WIN = 32;             // keys per sampling window (two statistics chunks, one key per lane)
+constexpr int TILE = 256;           // keys per stage of the streaming score pass
+constexpr int DCHUNK = 256;         // keys per partial of the dense comparator
+constexpr int CHUNK = DCHUNK;
+constexpr int WARPS = 8;            // warps per CTA
 constexpr int THREADS = WARPS * 32;
+constexpr int STAGES = 3;           // shared-memory ring depth of the streaming score pass
+constexpr int WIN_PER_WARP = 2;     // sampling windows per warp in the sampler
+constexpr int SPC = WARPS * WIN_PER_WARP;  // sampling windows per sampler CTA
 constexpr int HP = 4;               // query heads handled per pass over a loaded K tile
-constexpr int GROUP_CHUNKS = 8;     // chunks per sampling CTA (one warp each)
 
 // Device error flags (OR-ed into the workspace error word).
 constexpr int ERR_NK_BOUND = 1;     // a ragged nk_b above the stated bound, or negative
@@ -104,75 +110,146 @@ struct Tile {
   static_assert(ITERS == LPK, "tile geometry");
 };
 
-// Transpose-reduction over the LPK lanes of a key group.  On entry each lane
-// holds N partial sums; at every halving stage a lane keeps one half of its
-// values, ships the other half to its partner and adds what it receives.  On
-// exit lane `sub` holds the complete sums of original indices
-// sub*(N/LPK) + i, i < N/LPK.  Costs N*(1 - 1/LPK) shuffles instead of N*log2(LPK).
-template <int O, int N>
-struct TransposeReduce {
-  static __device__ __forceinline__ void run(float* v, int lane) {
-    const bool upper = (lane & O) != 0;
-#pragma unroll
-    for (int i = 0; i < N / 2; ++i) {
-      const float send = upper ? v[i] : v[i + N / 2];
-      const float keep = upper ? v[i + N / 2] : v[i];
-      v[i] = keep + __shfl_xor_sync(FULL, send, O);
-    }
-    TransposeReduce<O / 2, N / 2>::run(v, lane);
-  }
-};
-template <int N>
-struct TransposeReduce<0, N> {
-  static __device__ __forceinline__ void run(float*, int) {}
+// ---------------------------------------------------------------------------
+// Shared-memory staging of key / value rows.  Rows are copied with cp.async
+// (16 bytes per request, no registers held while in flight).  Row r's 16-byte
+// chunk s is stored at chunk (s & ~7) | ((s ^ r) & 7) of the row: eight
+// consecutive rows read at the same logical chunk then fall on eight distinct
+// 16-byte bank groups, so a warp reading one row per lane is conflict-free.
+// ---------------------------------------------------------------------------
+template <typename T, int D>
+struct Rows {
+  static constexpr int ES = Elem<T>::size;
+  static constexpr int ROWB = D * ES;     // bytes per row (128, 256 or 512)
+  static constexpr int NCH = ROWB / 16;   // 16-byte chunks per row
+  static constexpr int EPC = 16 / ES;     // elements per chunk
+  static_assert(NCH >= 8 && ROWB % 128 == 0, "row layout");
 };
 
-// Scores of 32 consecutive keys for up to HP heads, one warp.
-// Kw points at element 0 of key 0 of this warp's tile for the KV head;
-// consecutive keys are row_stride elements apart; keys >= nvalid are not read.
-// qreg[g][e] holds this lane's slice of (scale * q_g).  On return the lane owns
-// key index my_key() (0..31) and s[g] is its score for head g (garbage when
-// the key is not valid).
-template <typename T, int D>
-struct WarpScores {
-  using TL = Tile<T, D>;
-  static __device__ __forceinline__ int my_key(int lane) {
-    return (lane % TL::LPK) * TL::KPI + lane / TL::LPK;
+__device__ __forceinline__ int swz(int r, int s) { return (s & ~7) | ((s ^ r) & 7); }
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+// Copies rows [0, nrows) (row r starts at src + r * stride elements) into the
+// swizzled tile at `base`; NT threads cooperate.  stage_rows_async leaves the
+// copies in the current commit group; stage_rows closes it.
+template <typename T, int D, int NT>
+__device__ __forceinline__ void stage_rows_async(uint32_t base, const T* __restrict__ src, int64_t stride,
+                                                 int nrows) {
+  using R = Rows<T, D>;
+  for (int q = threadIdx.x; q < nrows * R::NCH; q += NT) {
+    const int r = q / R::NCH, s = q % R::NCH;
+    cp_async16(base + r * R::ROWB + swz(r, s) * 16, src + (int64_t)r * stride + s * R::EPC);
   }
-  static __device__ __forceinline__ void load(const T* __restrict__ Kw, int64_t row_stride, int nvalid,
-                                              int lane, uint4 (&kv)[TL::ITERS][TL::NVEC]) {
-    const int slot = lane / TL::LPK, sub = lane % TL::LPK;
-#pragma unroll
-    for (int it = 0; it < TL::ITERS; ++it) {
-      const int k = it * TL::KPI + slot;
-      const T* src = Kw + (int64_t)k * row_stride + sub * TL::EPL;
-#pragma unroll
-      for (int v = 0; v < TL::NVEC; ++v) {
-        kv[it][v] = (k < nvalid) ? ld_stream(src + v * (16 / TL::ES)) : make_uint4(0, 0, 0, 0);
-      }
-    }
-  }
-  static __device__ __forceinline__ void dot(const uint4 (&kv)[TL::ITERS][TL::NVEC],
-                                             const float (&qreg)[HP][TL::EPL], int lane, float (&s)[HP]) {
-    float v[TL::ITERS * HP];
-#pragma unroll
-    for (int it = 0; it < TL::ITERS; ++it) {
-      float kf[TL::EPL];
-#pragma unroll
-      for (int w = 0; w < TL::NVEC; ++w) Elem<T>::widen(kv[it][w], kf + w * (16 / TL::ES));
-#pragma unroll
-      for (int g = 0; g < HP; ++g) {
-        float acc = 0.f;
-#pragma unroll
-        for (int e = 0; e < TL::EPL; ++e) acc = fmaf(qreg[g][e], kf[e], acc);
-        v[it * HP + g] = acc;
-      }
-    }
-    TransposeReduce<TL::LPK / 2, TL::ITERS * HP>::run(v, lane);
-#pragma unroll
-    for (int g = 0; g < HP; ++g) s[g] = v[g];
+}
+template <typename T, int D, int NT>
+__device__ __forceinline__ void stage_rows(uint32_t base, const T* __restrict__ src, int64_t stride, int nrows) {
+  stage_rows_async<T, D, NT>(base, src, stride, nrows);
+  cp_async_commit();
+}
+// Waits until at most N of this thread's most recent commit groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Warp-level tensor-core tiles for the score contraction S[keys x heads] =
+// K[keys x d] . Q^T[d x heads] with 16-bit inputs and fp32 accumulation
+// (mma.m16n8k16: a 16-key x 16-dim A tile, a 16-dim x 8-head B tile).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+template <typename T> struct Mma;
+template <> struct Mma<bf16_t> {
+  static __device__ __forceinline__ void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
   }
 };
+template <> struct Mma<fp16_t> {
+  static __device__ __forceinline__ void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Packed fp32 pairs (sm_100+ fma.rn.f32x2): one instruction, two lanes of
+// fp32 fused multiply-add, each rounded as a scalar fmaf would be.
+// ---------------------------------------------------------------------------
+typedef unsigned long long f2x;
+__device__ __forceinline__ f2x pack2(float x, float y) {
+  f2x r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+  return r;
+}
+__device__ __forceinline__ float2 unpack2(f2x r) {
+  float2 a;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(r));
+  return a;
+}
+__device__ __forceinline__ f2x ffma2(f2x a, f2x b, f2x c) {
+  f2x d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// A 16-byte chunk of storage elements widened to EPC/2 fp32 pairs.
+template <typename T> struct Pairs;
+template <> struct Pairs<bf16_t> {
+  static __device__ __forceinline__ void get(const uint4& v, f2x* p) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[i] = pack2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+  }
+};
+template <> struct Pairs<fp16_t> {
+  static __device__ __forceinline__ void get(const uint4& v, f2x* p) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __half2 h;
+      memcpy(&h, &w[i], 4);
+      const float2 f = __half22float2(h);
+      p[i] = pack2(f.x, f.y);
+    }
+  }
+};
+template <> struct Pairs<float> {
+  static __device__ __forceinline__ void get(const uint4& v, f2x* p) {
+    p[0] = pack2(__uint_as_float(v.x), __uint_as_float(v.y));
+    p[1] = pack2(__uint_as_float(v.z), __uint_as_float(v.w));
+  }
+};
+
+// e^x from the hardware base-2 exponential (relative error ~2^-22; e^-inf = 0).
+__device__ __forceinline__ float fast_exp(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * 1.4426950408889634f));
+  return y;
+}
 
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
@@ -208,5 +285,18 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 __device__ __forceinline__ double word_to_unit(uint32_t w) { return (double)(w >> 8) * (1.0 / 16777216.0); }
 
 __device__ __forceinline__ void flag_error(int* err, int bits) { atomicOr(err, bits); }
+
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while its predecessor is still running; it must
+// wait here before touching anything the predecessor writes.  Without that
+// launch attribute both are no-ops.
+__device__ __forceinline__ void wait_for_predecessor() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// out[i..i+3] += v with one vectorised fp32 reduction (no return value).
+__device__ __forceinline__ void red_add_v4(float* out, float4 v) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(out), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
 
 }  // namespace santa

@@ -14,8 +14,10 @@ struct LaunchArgs {
   int D;           // head_dim (64 or 128)
   int B, H, Hkv;
   int64_t nk_max;
-  int chunks_max;  // ceil(nk_max / CHUNK)
-  int groups_max;  // ceil(chunks_max / GROUP_CHUNKS)
+  int chunks_max;  // santa: ceil(nk_max / SUB) statistics chunks; dense: ceil(nk_max / DCHUNK)
+  int groups_max;  // santa: ceil(ceil(nk_max / WIN) / SPC) sampler CTAs per (b, kv head)
+  int tiles_max;   // ceil(nk_max / TILE) score-pass tiles per (b, kv head)
+  int num_sms;     // streaming multiprocessors of the device (persistent grid size)
   int S_max;
   int variant;
   float scale;
@@ -31,15 +33,14 @@ struct LaunchArgs {
   int32_t* sample_idx;     // optional [B, H, S_max]
   // workspace views
   int* err;
-  unsigned* counters;      // [B * Hkv]
   float* stash;            // [B, H, nk_max]
   float* tile_max;         // [B, H, chunks_max]
   float* tile_sum;         // [B, H, chunks_max]
-  double* prefix;          // [B, H, chunks_max + 1]
-  double* thresh;          // [B, H, S_max]
+  long long* prefix;       // [B, H, chunks_max + 1] chunk-mass prefix, units of 2^-40 of the head max
+  long long* thresh;       // [B, H, S_max] sorted thresholds, same units
   int32_t* jstart;         // [B, H, chunks_max + 1]
   float* head_max;         // [B, H]
-  float* part_o;           // santa: [B, H, groups_max, D]; dense: [B, H, chunks_max, D]
+  float* part_o;           // dense: [B, H, chunks_max, D] chunk partial outputs
   cudaStream_t stream;
 };
 

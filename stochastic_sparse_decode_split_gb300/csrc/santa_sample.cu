@@ -2,7 +2,7 @@
 // sampling and the GQA-deduplicated V gather-add, for sm_103a.
 //
 // "Stochastic Sparse Attention for Memory-Bound Inference":
-//   combine   m* = max_t m_t, W_t = e^{m_t - m*} l_t, Z = sum_t W_t   (App. O, Alg. 4, lines 2-3)
+//   combine   m* = max_t m_t, W_t = e^{m_t - m*} l_t, Z = sum_t W_t   (App. O, Alg. 4)
 //   samplers  i.i.d. / stratified / systematic thresholds            (Sec. 2.1; Eq. 4)
 //   inverse CDF, left-closed: F(n-1) <= t < F(n)                     (App. A.4)
 //   gather    O_h = (1/S) sum_n c_{h,n} V_n over the union of rows
@@ -11,8 +11,10 @@
 // Difference from the pages' kernels: Alg. 4 rounds per-tile budgets by
 // largest remainder and then samples each tile systematically on its own.
 // Here every head's S thresholds are placed globally (prefix of chunk masses)
-// and resolved inside the chunk that holds them, which reproduces the global
-// i.i.d. / stratified / systematic estimators exactly.
+// and resolved inside the 32-key window that holds them, which reproduces the
+// global i.i.d. / stratified / systematic estimators exactly.
+#include <climits>
+
 #include "santa_common.cuh"
 #include "santa_launch.h"
 
@@ -41,13 +43,26 @@ __device__ __forceinline__ HeadCtx head_ctx(const LaunchArgs& a, int b) {
   return c;
 }
 
-// Chunk masses are summed as fixed-point integers (units of 2^-40 of the head
-// max's own mass): integer prefix sums are exact in any association, so the
-// chunk prefix is monotone however the block scan groups the additions.
-constexpr double MASS_ONE = 1099511627776.0;  // 2^40
-__device__ __forceinline__ long long mass_fixed(float w) { return __double2ll_rn((double)w * MASS_ONE); }
+// Probability masses are handled as fixed-point integers in units of 2^-40 of
+// the head-max key's mass (a key's mass relative to the max is <= 1).  Integer
+// sums are exact in any association, so every prefix is exactly monotone and
+// no FP64 arithmetic (slow on this part) is needed in any loop.  Conversion
+// truncates; masses below 2^-40 of the max key count as zero.
+constexpr int MASS_SHIFT = 40;
 
-// Inclusive block-wide scan of one int64 per thread (THREADS threads).
+// w * 2^40 rounded toward zero, for finite w in [0, 2^20], by integer operations.
+__device__ __forceinline__ long long mass_fixed(float w) {
+  const uint32_t bits = __float_as_uint(w);
+  const int e = (int)((bits >> 23) & 0xffu);
+  if (e == 0 || e == 0xff || (bits >> 31)) return 0;          // zero, subnormal, non-finite, negative
+  const long long m = (long long)((bits & 0x7fffffu) | 0x800000u);
+  const int sh = e - 127 - 23 + MASS_SHIFT;                  // w * 2^40 = m * 2^sh
+  if (sh >= 0) return m << min(sh, 39);
+  return sh > -64 ? (m >> -sh) : 0;
+}
+
+// Inclusive block-wide scan of one int64 per thread (NT threads).
+template <int NT>
 __device__ __forceinline__ long long block_inclusive_scan(long long v, long long* warp_tot) {
   const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
 #pragma unroll
@@ -63,39 +78,68 @@ __device__ __forceinline__ long long block_inclusive_scan(long long v, long long
   return v + off;
 }
 
+// Inclusive warp scan of one int64 per lane.
+__device__ __forceinline__ long long warp_inclusive_scan(long long v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long n = __shfl_up_sync(FULL, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
 // ---------------------------------------------------------------------------
-// Combine + thresholds.  grid = (H, B), block = 256.
-// dynamic smem: prefix double[chunks_max + 1] | theta double[S_pow2]
+// Combine + thresholds.  grid = (H, B), block = 256.  Three passes over the
+// head's chunk statistics (max; per-thread run sums and a block scan; the
+// prefix and first-threshold index of every chunk).
+// dynamic smem: theta int64[S_max] | ukey uint32[S_pow2]
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(THREADS)
 combine_kernel(LaunchArgs a, int S_pow2) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  double* P = reinterpret_cast<double*>(smem_raw);
-  double* theta = P + (a.chunks_max + 1);
+  long long* theta = reinterpret_cast<long long*>(smem_raw);
+  uint32_t* ukey = reinterpret_cast<uint32_t*>(theta + a.S_max);
   __shared__ float red[WARPS];
   __shared__ long long warp_tot[WARPS];
+  __shared__ long long s_Z;
+  __shared__ double s_invS;
 
   const int h = blockIdx.x, b = blockIdx.y;
-  const int G = a.H / a.Hkv;
   const int64_t bh = (int64_t)b * a.H + h;
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+  wait_for_predecessor();   // the score pass has completed and its writes are visible
+  allow_dependents();
   const HeadCtx hc = head_ctx(a, b);
-
-  if (h % G == 0 && tid == 0) a.counters[b * a.Hkv + h / G] = 0u;  // hand-off counter of the gather
   if (hc.err) {
     if (tid == 0 && h == 0) flag_error(a.err, hc.err);
     if (a.sample_idx)
       for (int j = tid; j < a.S_max; j += THREADS) a.sample_idx[bh * a.S_max + j] = -1;
     return;
   }
-  const int C = (int)((hc.nk + CHUNK - 1) / CHUNK);
+  const int C = (int)((hc.nk + SUB - 1) / SUB);
   const int S = hc.S;
   const float* tmax = a.tile_max + bh * a.chunks_max;
   const float* tsum = a.tile_sum + bh * a.chunks_max;
 
-  // m* = max over chunks
+  // each thread owns a contiguous run of chunks; its statistics are loaded once
+  // (kept in registers for runs of up to PMAX chunks)
+  constexpr int PMAX = 16;
+  const int per = (C + THREADS - 1) / THREADS;
+  const int c_lo = min(C, tid * per), c_hi = min(C, c_lo + per);
+  const bool in_regs = per <= PMAX;
+  float lm[PMAX], ll[PMAX];
   float m = -INFINITY;
-  for (int c = tid; c < C; c += THREADS) m = fmaxf(m, tmax[c]);
+  if (in_regs) {
+#pragma unroll
+    for (int i = 0; i < PMAX; ++i) {
+      const int c = c_lo + i;
+      lm[i] = (c < c_hi) ? tmax[c] : -INFINITY;
+      ll[i] = (c < c_hi) ? tsum[c] : 0.f;
+      m = fmaxf(m, lm[i]);
+    }
+  } else {
+    for (int c = c_lo; c < c_hi; ++c) m = fmaxf(m, tmax[c]);
+  }
   m = warp_max(m);
   if (lane == 0) red[warp] = m;
   __syncthreads();
@@ -103,28 +147,34 @@ combine_kernel(LaunchArgs a, int S_pow2) {
 #pragma unroll
   for (int w = 1; w < WARPS; ++w) mstar = fmaxf(mstar, red[w]);
 
-  // exclusive prefix of chunk masses W_c = e^{m_c - m*} l_c, each thread a contiguous run
-  const int per = (C + THREADS - 1) / THREADS;
-  const int c_lo = min(C, tid * per), c_hi = min(C, c_lo + per);
+  // chunk masses W_c = e^{m_c - m*} l_c over the run, block scan
+  auto mass = [&](int i, int c) -> long long {
+    return in_regs ? ((c < c_hi) ? mass_fixed(expf(lm[i] - mstar) * ll[i]) : 0)
+                   : mass_fixed(expf(tmax[c] - mstar) * tsum[c]);
+  };
   long long local = 0;
-  for (int c = c_lo; c < c_hi; ++c) local += mass_fixed(expf(tmax[c] - mstar) * tsum[c]);
-  const long long incl = block_inclusive_scan(local, warp_tot);
-  long long run = incl - local;
-  for (int c = c_lo; c < c_hi; ++c) {
-    P[c] = (double)run * (1.0 / MASS_ONE);
-    run += mass_fixed(expf(tmax[c] - mstar) * tsum[c]);
+  if (in_regs) {
+#pragma unroll
+    for (int i = 0; i < PMAX; ++i) local += mass(i, c_lo + i);
+  } else {
+    for (int c = c_lo; c < c_hi; ++c) local += mass(0, c);
   }
-  if (tid == THREADS - 1) P[C] = (double)incl * (1.0 / MASS_ONE);
+  const long long incl = block_inclusive_scan<THREADS>(local, warp_tot);
+  if (tid == THREADS - 1) s_Z = incl;
+  if (tid == 0) s_invS = 1.0 / (double)S;  // one fp64 division per head
   __syncthreads();
-  const double Z = P[C];
+  const double Z = (double)s_Z;
+  const double invS = s_invS;
 
-  // thresholds t_j (Sec. 2.1) scaled to mass units: theta_j = t_j * Z
+  // thresholds t_j (Sec. 2.1) in mass units: theta_j = t_j * Z.  Uniforms are
+  // 24-bit integers k (u = k * 2^-24); t_j = (j + u) / S is formed in fp64
+  // once per threshold (the only fp64 arithmetic, S operations per head).
   const uint32_t k0 = (uint32_t)a.seed, k1 = (uint32_t)(a.seed >> 32);
   if (a.variant == 2) {  // systematic: one offset
     double u;
     if (a.uniforms) u = a.uniforms[bh * a.S_max];
     else u = word_to_unit(philox4x32_10(make_uint4(0u, (uint32_t)h, (uint32_t)b, a.step), k0, k1).x);
-    for (int j = tid; j < S; j += THREADS) theta[j] = (((double)j + u) / (double)S) * Z;
+    for (int j = tid; j < S; j += THREADS) theta[j] = (long long)(((double)j + u) * invS * Z);
   } else {
     for (int i = tid; i < (S + 3) / 4; i += THREADS) {
       double u4[4];
@@ -142,44 +192,59 @@ combine_kernel(LaunchArgs a, int S_pow2) {
       for (int r = 0; r < 4; ++r) {
         const int j = 4 * i + r;
         if (j >= S) break;
-        const double t = (a.variant == 1) ? ((double)j + u4[r]) / (double)S : u4[r];
-        theta[j] = t * Z;
+        if (a.variant == 1) theta[j] = (long long)(((double)j + u4[r]) * invS * Z);
+        else ukey[j] = (uint32_t)(u4[r] * 16777216.0);   // exact: u has 24 fraction bits
       }
     }
   }
-  if (a.variant == 0) {  // i.i.d. draws are unordered: sort them (bitonic, +inf padding)
-    for (int j = S + tid; j < S_pow2; j += THREADS) theta[j] = INFINITY;
+  if (a.variant == 0) {  // i.i.d. draws are unordered: sort the 24-bit keys (bitonic, integer compares)
+    for (int j = S + tid; j < S_pow2; j += THREADS) ukey[j] = 0xffffffffu;
     __syncthreads();
     for (int k = 2; k <= S_pow2; k <<= 1) {
       for (int jj = k >> 1; jj > 0; jj >>= 1) {
         for (int i = tid; i < S_pow2; i += THREADS) {
           const int ixj = i ^ jj;
           if (ixj > i) {
-            const double x = theta[i], y = theta[ixj];
+            const uint32_t x = ukey[i], y = ukey[ixj];
             const bool up = (i & k) == 0;
             if ((x > y) == up) {
-              theta[i] = y;
-              theta[ixj] = x;
+              ukey[i] = y;
+              ukey[ixj] = x;
             }
           }
         }
         __syncthreads();
       }
     }
+    for (int j = tid; j < S; j += THREADS) theta[j] = (long long)((double)ukey[j] * (1.0 / 16777216.0) * Z);
   }
   __syncthreads();
 
-  // first threshold of every chunk: jstart[c] = #{j : theta_j < P_c}
-  for (int c = tid; c <= C; c += THREADS) {
-    const double pc = P[c];
+  // prefix P_c and first threshold jstart[c] = #{j : theta_j < P_c} of every chunk
+  long long run = incl - local;
+  long long* pref = a.prefix + bh * (a.chunks_max + 1);
+  int32_t* js = a.jstart + bh * (a.chunks_max + 1);
+  auto emit = [&](int c, long long w) {
     int lo = 0, hi = S;
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
-      if (theta[mid] < pc) lo = mid + 1;
+      if (theta[mid] < run) lo = mid + 1;
       else hi = mid;
     }
-    a.jstart[bh * (a.chunks_max + 1) + c] = lo;
-    a.prefix[bh * (a.chunks_max + 1) + c] = pc;
+    pref[c] = run;
+    js[c] = lo;
+    run += w;
+  };
+  if (in_regs) {
+#pragma unroll
+    for (int i = 0; i < PMAX; ++i)
+      if (c_lo + i < c_hi) emit(c_lo + i, mass(i, c_lo + i));
+  } else {
+    for (int c = c_lo; c < c_hi; ++c) emit(c, mass(0, c));
+  }
+  if (tid == THREADS - 1) {
+    pref[C] = s_Z;
+    js[C] = S;  // every threshold lies below the total mass
   }
   for (int j = tid; j < S; j += THREADS) a.thresh[bh * a.S_max + j] = theta[j];
   if (a.sample_idx)
@@ -188,199 +253,235 @@ combine_kernel(LaunchArgs a, int S_pow2) {
 }
 
 // ---------------------------------------------------------------------------
-// Sample + gather.  grid = (groups_max, H_kv, B), block = 256; warp w owns
-// chunk blockIdx.x * 8 + w.  dynamic smem per warp:
-//   pref double[CHUNK] | cnt uint32[G][CHUNK] | rows int32[CHUNK];
-// then wbuf float[WARPS][G][D].
+// Sample + gather.  grid = (H_kv, groups_max, B), block = 256 (8 warps);
+// warp w owns sampling windows blockIdx.y * SPC + w * 2 + {0, 1} (32 keys
+// each, one key per lane, i.e. two 16-key statistics chunks) for all heads of
+// the KV group.
+//
+// Per (window, head) with thresholds: the lane's key mass e^{s - m*} in fixed
+// point, an exact warp scan gives each key's inclusive prefix F_lane, and the
+// thresholds x_j = theta_j - P_w (sorted, one per lane, batches of 32) are
+// searched by shuffles: key `lane` is drawn by the thresholds with
+// F_{lane-1} <= x_j < F_lane.  Windows without thresholds read nothing but
+// their threshold range.  The rows drawn by any head form the union (each V
+// row read once per KV head); the gather adds count * V in fp32.
+//
+// dynamic smem: counts int[8 warps][2][GM][32] | rows int[8 warps][64] | wbuf float[8 warps][G][D]
 // ---------------------------------------------------------------------------
-template <typename T, int D>
-__global__ void __launch_bounds__(THREADS)
+constexpr int SG_WARPS = WARPS;
+constexpr int SG_THREADS = SG_WARPS * 32;
+constexpr int SG_NSW = WIN_PER_WARP;   // sampling windows per warp
+static_assert(SG_NSW * SG_WARPS == SPC, "windows per CTA");
+static_assert(WIN == 32 && WIN == 2 * SUB, "a window is one key per lane, two statistics chunks");
+
+template <int GM>
+__host__ __device__ constexpr size_t sample_gather_smem(int G, int D) {
+  return (size_t)SG_WARPS * SG_NSW * GM * 32 * sizeof(int) + (size_t)SG_WARPS * SG_NSW * 32 * sizeof(int) +
+         (size_t)SG_WARPS * G * D * sizeof(float);
+}
+
+// lower_bound of v among the sorted values x held one per lane (lanes >= n hold +inf)
+__device__ __forceinline__ int lane_lower_bound(long long x, int n, long long v) {
+  int lo = 0, hi = n;
+#pragma unroll
+  for (int it = 0; it < 6; ++it) {
+    const int mid = (lo + hi) >> 1;
+    const long long xm = __shfl_sync(FULL, x, mid & 31);
+    if (lo < hi) {
+      if (xm < v) lo = mid + 1;
+      else hi = mid;
+    }
+  }
+  return lo;
+}
+
+template <typename T, int D, int GM>
+__global__ void __launch_bounds__(SG_THREADS)
 sample_gather_kernel(LaunchArgs a) {
-  using TL = Tile<T, D>;
-  constexpr int GM = SANTA_MAX_GROUP_DEV;
+  using TL = Tile<T, D>;   // V row split: LPK lanes per row, KPI rows per load instruction
+  constexpr int NSW = SG_NSW;
   extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ int has_rows[SG_WARPS];
   const int G = a.H / a.Hkv;
-  const int grp = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int kvh = blockIdx.x, grp = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
-  const size_t warp_bytes = (size_t)CHUNK * (8 + 4 * G + 4);
-  unsigned char* wbase = smem_raw + warp * warp_bytes;
-  double* pref = reinterpret_cast<double*>(wbase);
-  unsigned* cnt = reinterpret_cast<unsigned*>(wbase + CHUNK * 8);
-  int* rows = reinterpret_cast<int*>(wbase + CHUNK * (8 + 4 * G));
-  float* wbuf = reinterpret_cast<float*>(smem_raw + WARPS * warp_bytes);
-  __shared__ double lane_tot[WARPS][32];
-  __shared__ int s_last;
-
+  int* cnt_s = reinterpret_cast<int*>(smem_raw) + warp * (NSW * GM * 32);                 // [NSW][GM][32]
+  int* rows = reinterpret_cast<int*>(smem_raw) + SG_WARPS * NSW * GM * 32 + warp * (NSW * 32);
+  float* wbuf = reinterpret_cast<float*>(smem_raw + (size_t)SG_WARPS * NSW * (GM + 1) * 32 * sizeof(int));
+  wait_for_predecessor();   // the combine has completed and its writes are visible
   const HeadCtx hc = head_ctx(a, b);
-  if (hc.err) {
-    if (grp == 0)
-      for (int i = tid; i < G * D; i += THREADS) a.out[((int64_t)b * a.H + kvh * G) * D + i] = 0.f;
-    return;
-  }
-  const int C = (int)((hc.nk + CHUNK - 1) / CHUNK);
-  const int NG = (C + GROUP_CHUNKS - 1) / GROUP_CHUNKS;
+  const int64_t bh0 = (int64_t)b * a.H + kvh * G;
+  if (hc.err) return;       // out was cleared by the score pass
+  const int C = (int)((hc.nk + SUB - 1) / SUB);
+  const int NW = (int)((hc.nk + WIN - 1) / WIN);
+  const int NG = (NW + SPC - 1) / SPC;
   if (grp >= NG) return;
-  const int c = grp * GROUP_CHUNKS + warp;
-  const bool active = c < C;
-  const int len = active ? (int)min((int64_t)CHUNK, hc.nk - (int64_t)c * CHUNK) : 0;
+  const int w0 = grp * SPC + warp * NSW;   // first window of this warp
+  const int cm1 = a.chunks_max + 1;
 
-  for (int i = lane; i < G * CHUNK; i += 32) cnt[i] = 0u;
-
-  // thresholds of every head that fall in this chunk, and the stash rows they need
-  int j0[GM], j1[GM];
-  float sv[GM][8];
+  // round 1: threshold range [js, je) and mass prefix of every (head, window)
+  int js[GM][NSW], je[GM][NSW];
+  long long pb[GM][NSW];
+  float mst[GM];
 #pragma unroll
   for (int g = 0; g < GM; ++g) {
-    j0[g] = j1[g] = 0;
-    if (g < G && active) {
-      const int64_t bh = (int64_t)b * a.H + kvh * G + g;
-      const int32_t* js = a.jstart + bh * (a.chunks_max + 1) + c;
-      j0[g] = js[0];
-      j1[g] = js[1];
-      if (j1[g] > j0[g]) {
-        const float* st = a.stash + bh * a.nk_max + (int64_t)c * CHUNK;
+    mst[g] = (g < G) ? a.head_max[bh0 + g] : 0.f;
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const int k = lane * 8 + r;
-          sv[g][r] = (k < len) ? st[k] : -INFINITY;
-        }
-      }
+    for (int i = 0; i < NSW; ++i) {
+      const int w = w0 + i;
+      const bool act = g < G && w < NW;
+      const int64_t base = (bh0 + g) * cm1;
+      js[g][i] = act ? a.jstart[base + 2 * w] : 0;
+      je[g][i] = act ? a.jstart[base + min(2 * w + 2, C)] : 0;
+      pb[g][i] = act ? a.prefix[base + 2 * w] : 0;
     }
   }
-  __syncwarp();
-
-#pragma unroll
-  for (int g = 0; g < GM; ++g) {
-    if (g >= G || j1[g] <= j0[g]) continue;  // warp-uniform
-    const int64_t bh = (int64_t)b * a.H + kvh * G + g;
-    const float mstar = a.head_max[bh];
-    // in-chunk masses relative to the head max and their inclusive prefix (fp64)
-    double loc[8];
-    double run = 0.0;
-    int lastpos = -1;
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const float w = (lane * 8 + r < len) ? expf(sv[g][r] - mstar) : 0.f;
-      run += (double)w;
-      loc[r] = run;
-      if (w > 0.f) lastpos = lane * 8 + r;
-    }
-    lane_tot[warp][lane] = run;
-    __syncwarp();
-    double excl = 0.0;
-    for (int l = 0; l < lane; ++l) excl += lane_tot[warp][l];  // serial: keeps the prefix monotone
-#pragma unroll
-    for (int r = 0; r < 8; ++r) pref[lane * 8 + r] = excl + loc[r];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lastpos = max(lastpos, __shfl_xor_sync(FULL, lastpos, o));
-    __syncwarp();
-    const double base = a.prefix[bh * (a.chunks_max + 1) + c];
-    for (int j = j0[g] + lane; j < j1[g]; j += 32) {
-      const double x = a.thresh[bh * a.S_max + j] - base;
-      int lo = 0, hi = len;
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (pref[mid] <= x) lo = mid + 1;
-        else hi = mid;
-      }
-      const int idx = (lo < len) ? lo : max(lastpos, 0);  // rounding past the chunk mass
-      atomicAdd(&cnt[g * CHUNK + idx], 1u);
-      if (a.sample_idx) a.sample_idx[bh * a.S_max + j] = c * CHUNK + idx;
-    }
-    __syncwarp();
-  }
-
-  // union of the rows drawn by any head of the group (each V row read once)
-  int nrows = 0;
-#pragma unroll
-  for (int r = 0; r < 8; ++r) {
-    const int k = r * 32 + lane;
-    bool any = false;
-    for (int g = 0; g < G; ++g) any |= cnt[g * CHUNK + k] != 0u;
-    const unsigned bal = __ballot_sync(FULL, any);
-    if (any) rows[nrows + __popc(bal & ((1u << lane) - 1u))] = k;
-    nrows += __popc(bal);
-  }
-  __syncwarp();
-
-  // count-weighted gather-and-add, fp32 accumulation
-  const int slot = lane / TL::LPK, sub = lane % TL::LPK;
-  float acc[GM][TL::EPL];
+  // round 2: scores and first 32 thresholds of the (head, window) pairs that draw
+  float sv[GM][NSW];
+  long long th[GM][NSW];
 #pragma unroll
   for (int g = 0; g < GM; ++g)
 #pragma unroll
-    for (int e = 0; e < TL::EPL; ++e) acc[g][e] = 0.f;
-  const T* Vbase = reinterpret_cast<const T*>(a.V) + ((hc.row0 + (int64_t)c * CHUNK) * a.Hkv + kvh) * (int64_t)D;
-  constexpr int UNR = 4;
-  for (int i0 = slot; i0 < nrows; i0 += UNR * TL::KPI) {
-    uint4 vv[UNR][TL::NVEC];
-    int key[UNR];
-#pragma unroll
-    for (int u = 0; u < UNR; ++u) {
-      const int i = i0 + u * TL::KPI;
-      key[u] = (i < nrows) ? rows[i] : -1;
-#pragma unroll
-      for (int v = 0; v < TL::NVEC; ++v)
-        vv[u][v] = (key[u] >= 0)
-                       ? ld_stream(Vbase + (int64_t)key[u] * a.Hkv * D + sub * TL::EPL + v * (16 / TL::ES))
-                       : make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < NSW; ++i) {
+      const int64_t bh = bh0 + g;
+      const int64_t key = (int64_t)(w0 + i) * WIN + lane;
+      const bool draws = je[g][i] > js[g][i];
+      sv[g][i] = (draws && key < hc.nk) ? a.stash[bh * a.nk_max + key] : -INFINITY;
+      th[g][i] = (js[g][i] + lane < je[g][i]) ? a.thresh[bh * a.S_max + js[g][i] + lane] : LLONG_MAX;
     }
+
+  // sampling: counts per (window, head, key) into shared memory
+  unsigned drawn[NSW];
 #pragma unroll
-    for (int u = 0; u < UNR; ++u) {
-      if (key[u] < 0) continue;
-      float vf[TL::EPL];
+  for (int i = 0; i < NSW; ++i) {
+    drawn[i] = 0u;
 #pragma unroll
-      for (int v = 0; v < TL::NVEC; ++v) Elem<T>::widen(vv[u][v], vf + v * (16 / TL::ES));
-#pragma unroll
-      for (int g = 0; g < GM; ++g) {
-        if (g >= G) break;
-        const float cg = (float)cnt[g * CHUNK + key[u]];
-#pragma unroll
-        for (int e = 0; e < TL::EPL; ++e) acc[g][e] = fmaf(cg, vf[e], acc[g][e]);
+    for (int g = 0; g < GM; ++g) {
+      int cnt = 0;
+      const int nt = je[g][i] - js[g][i];
+      if (nt > 0) {  // warp-uniform
+        const int64_t bh = bh0 + g;
+        const long long w = mass_fixed(expf(sv[g][i] - mst[g]));   // e^{-inf} = 0 past the sequence end
+        const long long F = warp_inclusive_scan(w, lane);
+        const long long total = __shfl_sync(FULL, F, 31);
+        const unsigned nz = __ballot_sync(FULL, w > 0);
+        const int last_nz = nz ? 31 - __clz(nz) : 0;             // rounding past the total goes here
+        int lb = 0, lb_total = 0;
+        for (int base = 0; base < nt; base += 32) {
+          const int n = min(32, nt - base);
+          long long x = (base == 0) ? th[g][i]
+                                    : ((lane < n) ? a.thresh[bh * a.S_max + js[g][i] + base + lane] : LLONG_MAX);
+          x = (lane < n) ? x - pb[g][i] : LLONG_MAX;
+          lb += lane_lower_bound(x, n, F);
+          lb_total += lane_lower_bound(x, n, total);
+        }
+        const int lb_up = __shfl_up_sync(FULL, lb, 1);
+        const int lb_prev = (lane == 0) ? 0 : lb_up;
+        cnt = lb - lb_prev;                                        // F_{lane-1} <= x < F_lane
+        if (lane == last_nz) cnt += nt - lb_total;                  // x >= the window's total
+        if (a.sample_idx) {
+          int32_t* dst = a.sample_idx + bh * a.S_max + js[g][i];
+          const int key = (w0 + i) * WIN + lane;
+          for (int j = lb_prev; j < lb; ++j) dst[j] = key;
+          if (lane == last_nz)
+            for (int j = lb_total; j < nt; ++j) dst[j] = key;
+        }
       }
+      cnt_s[(i * GM + g) * 32 + lane] = cnt;
+      drawn[i] |= __ballot_sync(FULL, cnt > 0);
     }
   }
+
+  // union of the rows drawn by any head: compact list of (window, key) per warp
+  int nrows = 0;
 #pragma unroll
-  for (int o = TL::LPK; o < 32; o <<= 1)
+  for (int i = 0; i < NSW; ++i) {
+    if (drawn[i] & (1u << lane)) rows[nrows + __popc(drawn[i] & ((1u << lane) - 1u))] = i * 32 + lane;
+    nrows += __popc(drawn[i]);
+  }
+  if (lane == 0) has_rows[warp] = nrows > 0;
+  __syncwarp();
+
+  // count-weighted gather-and-add (each drawn V row read once, fp32 accumulation)
+  if (nrows > 0) {
+    const int slot = lane / TL::LPK, sub = lane % TL::LPK;
+    float acc[GM][TL::EPL];
 #pragma unroll
     for (int g = 0; g < GM; ++g)
 #pragma unroll
-      for (int e = 0; e < TL::EPL; ++e) acc[g][e] += __shfl_xor_sync(FULL, acc[g][e], o);
-  if (slot == 0) {
+      for (int e = 0; e < TL::EPL; ++e) acc[g][e] = 0.f;
+    const T* Vbase = reinterpret_cast<const T*>(a.V) + (hc.row0 * a.Hkv + kvh) * (int64_t)D + sub * TL::EPL;
+    constexpr int UNR = 8;
+    for (int i0 = slot; i0 < nrows; i0 += UNR * TL::KPI) {
+      uint4 vv[UNR][TL::NVEC];
+      int rk[UNR];
 #pragma unroll
-    for (int g = 0; g < GM; ++g) {
-      if (g >= G) break;
+      for (int u = 0; u < UNR; ++u) {
+        const int i = i0 + u * TL::KPI;
+        rk[u] = (i < nrows) ? rows[i] : -1;
+        const int64_t key = (int64_t)(w0 + (rk[u] >> 5)) * WIN + (rk[u] & 31);
 #pragma unroll
-      for (int e = 0; e < TL::EPL; ++e) wbuf[(warp * G + g) * D + sub * TL::EPL + e] = acc[g][e];
+        for (int v = 0; v < TL::NVEC; ++v)
+          vv[u][v] = (rk[u] >= 0) ? ld_stream(Vbase + key * a.Hkv * D + v * (16 / TL::ES)) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        if (rk[u] < 0) continue;
+        float vf[TL::EPL];
+#pragma unroll
+        for (int v = 0; v < TL::NVEC; ++v) Elem<T>::widen(vv[u][v], vf + v * (16 / TL::ES));
+        const int* cr = cnt_s + (rk[u] >> 5) * GM * 32 + (rk[u] & 31);
+#pragma unroll
+        for (int g = 0; g < GM; ++g) {
+          if (g < G) {
+            const float cg = (float)cr[g * 32];
+#pragma unroll
+            for (int e = 0; e < TL::EPL; ++e) acc[g][e] = fmaf(cg, vf[e], acc[g][e]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int o = TL::LPK; o < 32; o <<= 1)
+#pragma unroll
+      for (int g = 0; g < GM; ++g)
+#pragma unroll
+        for (int e = 0; e < TL::EPL; ++e) acc[g][e] += __shfl_xor_sync(FULL, acc[g][e], o);
+    if (slot == 0) {
+#pragma unroll
+      for (int g = 0; g < GM; ++g)
+        if (g < G)
+#pragma unroll
+          for (int e = 0; e < TL::EPL; ++e) wbuf[(warp * G + g) * D + sub * TL::EPL + e] = acc[g][e];
     }
   }
   __syncthreads();
 
-  // this CTA's partial sum per head, then the last CTA of the group reduces
-  // all partials in a fixed order (deterministic) and applies 1/S.
-  const int64_t bh0 = (int64_t)b * a.H + kvh * G;
-  for (int i = tid; i < G * D; i += THREADS) {
-    float s = 0.f;
+  // this CTA's sum per head, times 1/S, added into out (cleared by the score
+  // pass) with vectorised fp32 reductions; warps that drew nothing are
+  // skipped.  The order of the additions across CTAs is not fixed, so the last
+  // bits of out may differ between runs; the drawn indices never do.
+  unsigned warps_with_rows = 0u;
 #pragma unroll
-    for (int w = 0; w < WARPS; ++w) s += wbuf[w * G * D + i];
-    const int g = i / D, col = i % D;
-    a.part_o[((bh0 + g) * a.groups_max + grp) * D + col] = s;
-  }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(&a.counters[b * a.Hkv + kvh], 1u) == (unsigned)(NG - 1));
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
+  for (int w = 0; w < SG_WARPS; ++w) warps_with_rows |= has_rows[w] ? (1u << w) : 0u;
+  if (!warps_with_rows) return;
   const float inv_S = 1.0f / (float)hc.S;
-  for (int i = tid; i < G * D; i += THREADS) {
-    const int g = i / D, col = i % D;
-    const float* src = a.part_o + (bh0 + g) * a.groups_max * D + col;
-    float s = 0.f;
-    for (int q = 0; q < NG; ++q) s += __ldcg(src + (int64_t)q * D);
-    a.out[(bh0 + g) * D + col] = s * inv_S;
+  for (int i4 = tid; i4 < G * D / 4; i4 += SG_THREADS) {
+    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < SG_WARPS; ++w) {
+      if (warps_with_rows & (1u << w)) {
+        const float4 v = reinterpret_cast<const float4*>(wbuf)[w * G * D / 4 + i4];
+        sum.x += v.x;
+        sum.y += v.y;
+        sum.z += v.z;
+        sum.w += v.w;
+      }
+    }
+    if (sum.x != 0.f || sum.y != 0.f || sum.z != 0.f || sum.w != 0.f)
+      red_add_v4(a.out + bh0 * D + 4 * i4,
+                 make_float4(sum.x * inv_S, sum.y * inv_S, sum.z * inv_S, sum.w * inv_S));
   }
-  if (tid == 0) a.counters[b * a.Hkv + kvh] = 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -392,33 +493,48 @@ static int next_pow2(int x) {
   return p;
 }
 
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while its predecessor finishes and waits in wait_for_predecessor().
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 cudaError_t launch_combine(const LaunchArgs& a) {
   const int S_pow2 = next_pow2(a.S_max);
-  const size_t smem = sizeof(double) * ((size_t)a.chunks_max + 1 + (size_t)S_pow2);
-  if (smem > 48 * 1024) {
+  const size_t smem = sizeof(long long) * (size_t)a.S_max + sizeof(uint32_t) * S_pow2;
+  if (smem + 1024 > 48 * 1024) {  // plus a little static shared memory
     cudaError_t e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  combine_kernel<<<dim3((unsigned)a.H, (unsigned)a.B), THREADS, smem, a.stream>>>(a, S_pow2);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3((unsigned)a.H, (unsigned)a.B), dim3(THREADS), smem, a.stream, a, S_pow2);
 }
 
-size_t sample_gather_smem(int G, int D) {
-  return (size_t)WARPS * CHUNK * (8 + 4 * G + 4) + (size_t)WARPS * G * D * sizeof(float);
+template <typename T, int D, int GM>
+static cudaError_t launch_sample_gather_g(const LaunchArgs& a) {
+  const int G = a.H / a.Hkv;
+  const size_t smem = sample_gather_smem<GM>(G, D);
+  cudaError_t e = cudaFuncSetAttribute(sample_gather_kernel<T, D, GM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(sample_gather_kernel<T, D, GM>, dim3((unsigned)a.Hkv, (unsigned)a.groups_max, (unsigned)a.B),
+                    dim3(SG_THREADS), smem, a.stream, a);
 }
 
 template <typename T, int D>
 static cudaError_t launch_sample_gather_t(const LaunchArgs& a) {
-  const int G = a.H / a.Hkv;
-  const size_t smem = sample_gather_smem(G, D);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(sample_gather_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-  }
-  sample_gather_kernel<T, D><<<dim3((unsigned)a.groups_max, (unsigned)a.Hkv, (unsigned)a.B), THREADS, smem,
-                               a.stream>>>(a);
-  return cudaGetLastError();
+  return (a.H / a.Hkv <= 4) ? launch_sample_gather_g<T, D, 4>(a) : launch_sample_gather_g<T, D, 8>(a);
 }
 
 cudaError_t launch_sample_gather(const LaunchArgs& a) {
