@@ -60,7 +60,8 @@ typedef enum {
   SANTA_ERR_UNSUPPORTED = 2, /* head_dim / dtype / group size this build does not provide */
   SANTA_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned or smaller than *_workspace_size */
   SANTA_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch, copy, sync) */
-  SANTA_ERR_DEVICE = 5       /* the device flagged bad ragged metadata (see santa_get_error) */
+  SANTA_ERR_DEVICE = 5,      /* the device flagged bad ragged metadata (see santa_get_error) */
+  SANTA_ERR_SCRATCH_LIMIT = 6 /* santa_decode_static: the problem needs more than SANTA_STATIC_SCRATCH_BYTES */
 } santa_status_t;
 
 typedef struct {
@@ -163,6 +164,33 @@ int32_t santa_workspace_layout(const santa_params_t* p, santa_ws_layout_t* layou
  * Returns SANTA_OK, SANTA_ERR_DEVICE (device flagged bad metadata; *code gets
  * the flag bits when code != NULL) or SANTA_ERR_CUDA. */
 santa_status_t santa_get_error(void* workspace, santa_stream_t stream, int32_t* code);
+
+/* santa_decode without a caller-supplied workspace, for callers that cannot
+ * allocate device memory: for example a plug-in that its host framework hands
+ * only tensors and a stream (all device memory belongs to the framework's own
+ * pool), or code that must not call cudaMalloc in the middle of a run because
+ * the call synchronises the device and may fail once the pool holds the rest
+ * of the GPU.  The paper has no counterpart; this entry point is a property of
+ * this library's interface, not of the method.
+ *
+ * Arguments, layouts and results are those of santa_decode.  The workspace is
+ * a fixed array of SANTA_STATIC_SCRATCH_BYTES bytes in the library's own
+ * device memory (every GPU that loads the library holds it until the process
+ * exits).  Problems whose santa_workspace_size exceeds it are rejected with
+ * SANTA_ERR_SCRATCH_LIMIT before any CUDA call; invalid parameters get the
+ * statuses santa_decode gives.  No allocation is made: the first call on a
+ * device (the caller's current device) looks up the array's device address
+ * once with cudaGetSymbolAddress, so make that first call before any stream
+ * capture begins.  Each call clears the array's error word on `stream` first;
+ * ragged metadata the device rejects leaves those heads' outputs zero (and
+ * their sample_idx entries -1), as in santa_decode, but the flag itself is not
+ * reported here (use santa_decode with a workspace and santa_get_error).
+ * All calls share the one array, which keeps the last call's contents: calls
+ * whose work overlaps on the GPU (different streams, or several host threads
+ * without ordering) race on it and give wrong results. */
+#define SANTA_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
+santa_status_t santa_decode_static(const santa_params_t* p, int32_t variant, const void* q, const void* K,
+                                   const void* V, float* out, santa_stream_t stream, int32_t* sample_idx);
 
 /* Static description of a status code. */
 const char* santa_status_string(santa_status_t status);

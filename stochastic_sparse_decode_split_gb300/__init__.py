@@ -28,7 +28,7 @@ from .build import LIB as _LIB_PATH
 __all__ = [
     "SantaError", "Params", "library", "santa_decode", "santa_decode_with_uniforms", "santa_dense_decode",
     "workspace_size", "dense_workspace_size", "workspace_layout", "get_error", "Decoder", "exported_symbols",
-    "VARIANTS", "DTYPES",
+    "VARIANTS", "DTYPES", "santa_decode_static", "static_scratch_bytes",
 ]
 
 VARIANTS = {"iid": 0, "stratified": 1, "systematic": 2}
@@ -92,13 +92,14 @@ def library():
             lib.santa_score_pass.argtypes = [P, vp, vp, vp, sz, vp]
             lib.santa_decode_with_uniforms.argtypes = [P, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp]
             lib.santa_dense_decode.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
+            lib.santa_decode_static.argtypes = [P, i32, vp, vp, vp, vp, vp, vp]
             lib.santa_workspace_layout.argtypes = [P, ctypes.POINTER(WsLayout)]
             lib.santa_get_error.argtypes = [vp, vp, ctypes.POINTER(i32)]
             lib.santa_status_string.argtypes = [i32]
             lib.santa_status_string.restype = ctypes.c_char_p
             lib.santa_version.restype = i32
             for fn in ("santa_workspace_init", "santa_decode", "santa_decode_profiled", "santa_score_pass",
-                       "santa_decode_with_uniforms", "santa_dense_decode",
+                       "santa_decode_with_uniforms", "santa_dense_decode", "santa_decode_static",
                        "santa_workspace_layout", "santa_get_error"):
                 getattr(lib, fn).restype = i32
             _lib = lib
@@ -223,6 +224,31 @@ def santa_decode_with_uniforms(q, K, V, uniforms, S: int, variant: str, out=None
                                               _stream(stream), _ptr(sample_idx))
     if st != SANTA_OK:
         raise SantaError(st, "santa_decode_with_uniforms")
+    return out
+
+
+def static_scratch_bytes() -> int:
+    """SANTA_STATIC_SCRATCH_BYTES from include/santa.h: the largest workspace
+    santa_decode_static can serve."""
+    m = re.search(r"#define SANTA_STATIC_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)", open(HEADER).read())
+    return int(m.group(1)) << int(m.group(2))
+
+
+def santa_decode_static(q, K, V, S: int, variant: str = "systematic", seed: int = 0, step: int = 0, out=None,
+                        nk: Optional[int] = None, kv_offsets=None, S_per_seq=None, scale: float = 0.0,
+                        sample_idx=None, stream=None) -> torch.Tensor:
+    """santa_decode through the C entry point that allocates nothing: its
+    workspace is the library's fixed device array (for callers that cannot
+    allocate device memory; see include/santa.h).  `out` is the caller's; pass
+    it to keep this call free of allocation on the Python side as well."""
+    _check_tensors(q, K, V, out, kv_offsets, S_per_seq, sample_idx)
+    p = make_params(q, K, S, seed, step, nk, kv_offsets, S_per_seq, scale)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    st = library().santa_decode_static(ctypes.byref(p), VARIANTS[variant], _ptr(q), _ptr(K), _ptr(V), _ptr(out),
+                                       _stream(stream), _ptr(sample_idx))
+    if st != SANTA_OK:
+        raise SantaError(st, "santa_decode_static")
     return out
 
 

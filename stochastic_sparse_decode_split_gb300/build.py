@@ -19,7 +19,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libsanta.so")
-SOURCES = ["santa_api.cu", "santa_score.cu", "santa_sample.cu"]
+SOURCES = ["santa_api.cu", "santa_score.cu", "santa_sample.cu", "santa_static.cu"]
 HEADERS = ["santa_common.cuh", "santa_launch.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -245,6 +245,7 @@ const char* santa_status_string(santa_status_t status) {
     case SANTA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case SANTA_ERR_CUDA: return "CUDA runtime error";
     case SANTA_ERR_DEVICE: return "device flagged bad ragged metadata";
+    case SANTA_ERR_SCRATCH_LIMIT: return "problem needs more than the SANTA_STATIC_SCRATCH_BYTES of santa_decode_static";
     default: return "unknown status";
   }
 }
