@@ -3,10 +3,12 @@
 
 A step is one pass of the whole operator (score pass, combine + thresholds,
 sample + gather) over one decode step of the workload, through the C ABI on
-device-resident inputs.  Protocol (after "Stochastic Sparse Attention for
-Memory-Bound Inference", App. Q): W untimed warm-up steps, then K timed steps,
-each preceded by an untimed in-place update of a 512 MiB fp32 buffer that
-evicts the 129 MB L2, each bracketed by CUDA events on the launching stream.
+device-resident inputs; for 16-bit caches it is a single cooperative launch.
+Protocol (after "Stochastic Sparse Attention for Memory-Bound Inference",
+App. Q): W untimed warm-up steps, then K timed steps, each bracketed by CUDA
+events on the launching stream.  Inputs are larger than L2: the steps rotate
+over R copies of the K/V cache (R * |K, V| >= 512 MiB), so every step reads its
+cache from HBM; workloads too small for that flush L2 between steps instead.
 
     python bench.py [--steps K] [--warmup W] [--workload llama32k|qwen|ragged|tiny]
     python bench.py --impl reference      # the CPU oracle, timed on host cores
@@ -33,9 +35,11 @@ METRIC = "S²ANTA decode-attn µs/step and achieved HBM GB/s vs peak, 32K ctx bf
 UNIT = "us/step"
 FALLBACK_HBM_GBS = 6800.0
 FLUSH_BYTES = 512 * 1024 * 1024
-SCORE_SOURCES = ["stochastic_sparse_decode_split_gb300/csrc/santa_score.cu",
-                 "stochastic_sparse_decode_split_gb300/csrc/santa_common.cuh"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "score_pass_traffic.json")
+KERNEL_SOURCES = ["stochastic_sparse_decode_split_gb300/csrc/santa_fused.cu",
+                  "stochastic_sparse_decode_split_gb300/csrc/santa_stream.cuh",
+                  "stochastic_sparse_decode_split_gb300/csrc/santa_window.cuh",
+                  "stochastic_sparse_decode_split_gb300/csrc/santa_common.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fused_decode_traffic.json")
 
 
 def parse_args():
@@ -155,14 +159,14 @@ def source_hash(paths):
 
 
 def recorded_traffic(workload_name):
-    """dram read+write bytes per launch of the score pass from a committed ncu
-    summary, only while the kernel source is unchanged since the capture."""
+    """dram read+write bytes per launch of the decode kernel from a committed
+    ncu summary, only while the kernel source is unchanged since the capture."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    if rec.get("source_hash") != source_hash(SCORE_SOURCES):
+    if rec.get("source_hash") != source_hash(KERNEL_SOURCES):
         return None
     if rec.get("workload") != workload_name:
         return None
@@ -185,7 +189,7 @@ def score_pass_bytes(inp):
     es = esize(wl.dtype)
     B, H, d = inp.q.shape
     rows = int(inp.kv_offsets[-1])
-    chunks = sum((int(n) + 255) // 256 for n in inp.nk_per_seq)
+    chunks = sum((int(n) + 15) // 16 for n in inp.nk_per_seq)
     return rows * wl.n_kv_heads * d * es + B * H * d * es + 2 * 4 * H * chunks
 
 
@@ -398,21 +402,26 @@ def run_ours(args):
     torch.cuda.synchronize()
     stage_ms = [statistics.mean(e[k].elapsed_time(e[k + 1]) for e in ev_sets) for k in range(3)]
 
-    # duration of one score-pass launch: launches issued back to back over the
-    # rotating replicas between one pair of events (launch latency overlapped)
-    score_launch_ms = None
-    if flush is None:
-        n_back = min(args.steps, 400)
+    # duration of one decode launch, and of the staged path's score pass alone:
+    # launches issued back to back over the rotating replicas between one pair
+    # of events (launch latency overlapped)
+    def back_to_back(fn, n):
         for i in range(args.warmup):
-            decs[i % R].score_pass()
+            fn(i)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         e0.record(stream)
-        for i in range(n_back):
-            decs[i % R].score_pass()
+        for i in range(n):
+            fn(i)
         e1.record(stream)
         torch.cuda.synchronize()
-        score_launch_ms = e0.elapsed_time(e1) / n_back
+        return e0.elapsed_time(e1) / n
+
+    launch_ms = score_launch_ms = None
+    if flush is None:
+        n_back = min(args.steps, 400)
+        launch_ms = back_to_back(lambda i: decs[i % R](step=0), n_back)
+        score_launch_ms = back_to_back(lambda i: decs[i % R].score_pass(), n_back)
 
     # dense comparator, same protocol
     denses = [santa.Decoder(t["q"], Kr, Vr, S=1, variant=wl.variant, dense=True, **kw) for (Kr, Vr) in reps]
@@ -444,8 +453,9 @@ def run_ours(args):
     peak, peak_kind = hbm_peak()
     sb = score_pass_bytes(inp)
     stb = step_bytes(inp, unique_rows)
-    kernel_ms = score_launch_ms if score_launch_ms is not None else stage_ms[0]
-    achieved = sb / (kernel_ms * 1e-3) / 1e9
+    single = wl.dtype != "fp32"          # 16-bit caches: the whole step is one launch
+    kernel_ms = launch_ms if launch_ms is not None else mean_ms
+    achieved = stb / (kernel_ms * 1e-3) / 1e9
     step_achieved = stb / (mean_ms * 1e-3) / 1e9
     value_us = mean_ms * 1e3 / world   # whole job: time per decode step over all ranks' steps
 
@@ -467,22 +477,25 @@ def run_ours(args):
                    "l2": l2_note,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "median_us": med_ms * 1e3,
-        "roofline": {"bound": "hbm", "kernel": "score_stream_kernel", "achieved": achieved, "peak": peak,
-                     "unit": "GB/s", "frac": achieved / peak, "traffic": recorded_traffic(wl.name),
-                     "peak_kind": f"of {peak_kind}", "alg_bytes_per_launch": sb,
+        "roofline": {"bound": "hbm", "kernel": "fused_decode_kernel" if single else "staged path",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": recorded_traffic(wl.name) if single else None,
+                     "peak_kind": f"of {peak_kind}", "alg_bytes_per_launch": stb,
                      "us_per_launch": kernel_ms * 1e3,
-                     "timing": ("back-to-back launches over rotating replicas" if score_launch_ms is not None
-                                else "events around the stage inside a step")},
+                     "timing": ("back-to-back launches over rotating replicas" if launch_ms is not None
+                                else "events around each step")},
         "step": {"alg_bytes": stb, "unique_v_rows": unique_rows, "achieved_GBps": step_achieved,
-                 "frac": step_achieved / peak, "stage_us": {"score": stage_ms[0] * 1e3,
-                                                            "combine": stage_ms[1] * 1e3,
-                                                            "sample_gather": stage_ms[2] * 1e3}},
+                 "frac": step_achieved / peak},
+        "staged_path": {"stage_us": {"score": stage_ms[0] * 1e3, "combine": stage_ms[1] * 1e3,
+                                     "sample_gather": stage_ms[2] * 1e3},
+                        "score_pass_us_per_launch": score_launch_ms * 1e3 if score_launch_ms else None,
+                        "score_pass_GBps": sb / (score_launch_ms * 1e-3) / 1e9 if score_launch_ms else None},
         "dense": {"us_per_step": statistics.mean(dms) * 1e3, "alg_bytes": dense_bytes(inp),
                   "achieved_GBps": dense_bytes(inp) / (statistics.mean(dms) * 1e-3) / 1e9,
                   "speedup_santa_vs_dense": statistics.mean(dms) / mean_ms},
         "cpu_baseline": cpu_baseline,
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (1 if single else 3) * args.steps,
         "clocks": clocks,
     }
     print(json.dumps(line))

@@ -14,12 +14,13 @@ static_assert(SANTA_CHUNK == santa::SUB, "chunk length");
 namespace {
 
 constexpr size_t ALIGN = 256;
-constexpr size_t HEADER = 256;  // error word + padding
+constexpr size_t HEADER = 256;  // error word, grid-barrier counter and generation, padding
+constexpr size_t BAR_COUNT = 64, BAR_GEN = 128;  // header offsets of the grid-barrier words
 
 size_t up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
 
 struct Layout {
-  size_t stash, tile_max, tile_sum, prefix, thresh, jstart, head_max, part_o, total;
+  size_t stash, tile_max, tile_sum, prefix, thresh, jstart, head_max, part_o, agg_m, agg_l, ukeys, rcp_S, total;
   int64_t chunks, groups;
 };
 
@@ -65,6 +66,10 @@ Layout santa_layout(const santa_params_t* p) {
   L.thresh = off;   off += up(B * H * S * sizeof(long long));
   L.jstart = off;   off += up(B * H * ((size_t)L.chunks + 1) * sizeof(int32_t));
   L.head_max = off; off += up(B * H * sizeof(float));
+  L.agg_m = off;    off += up(B * H * santa::MAX_CTAS * sizeof(float));
+  L.agg_l = off;    off += up(B * H * santa::MAX_CTAS * sizeof(float));
+  L.ukeys = off;    off += up(B * H * S * sizeof(uint32_t));
+  L.rcp_S = off;    off += up(B * sizeof(unsigned long long));
   L.part_o = 0;
   L.total = off;
   return L;
@@ -147,6 +152,18 @@ santa_status_t decode_impl(const santa_params_t* p, int32_t variant, const void*
   a.thresh = reinterpret_cast<long long*>(w + L.thresh);
   a.jstart = reinterpret_cast<int32_t*>(w + L.jstart);
   a.head_max = reinterpret_cast<float*>(w + L.head_max);
+  a.agg_m = reinterpret_cast<float*>(w + L.agg_m);
+  a.agg_l = reinterpret_cast<float*>(w + L.agg_l);
+  a.ukeys = reinterpret_cast<uint32_t*>(w + L.ukeys);
+  a.rcp_S = reinterpret_cast<unsigned long long*>(w + L.rcp_S);
+
+  // 16-bit caches with Philox uniforms: the whole step in one cooperative
+  // launch; otherwise (fp32, caller uniforms, per-stage events) three stages.
+  if (!score_only && !events && !uniforms && p->dtype != SANTA_FP32)
+    return santa::launch_fused(a, reinterpret_cast<unsigned*>(w + BAR_COUNT),
+                               reinterpret_cast<unsigned*>(w + BAR_GEN)) == cudaSuccess
+               ? SANTA_OK
+               : SANTA_ERR_CUDA;
 
   auto mark = [&](int i) {
     return !events || cudaEventRecord((cudaEvent_t)events[i], (cudaStream_t)stream) == cudaSuccess;

@@ -21,10 +21,16 @@ constexpr int WIN_PER_WARP = 2;     // sampling windows per warp in the sampler
 constexpr int SPC = WARPS * WIN_PER_WARP;  // sampling windows per sampler CTA
 constexpr int HP = 4;               // query heads handled per pass over a loaded K tile
 
+// Sampling variants (santa_variant_t).
+constexpr int VAR_IID = 0;
+constexpr int VAR_STRAT = 1;
+constexpr int VAR_SYS = 2;
+
 // Device error flags (OR-ed into the workspace error word).
 constexpr int ERR_NK_BOUND = 1;     // a ragged nk_b above the stated bound, or negative
 constexpr int ERR_S_RANGE = 2;      // a per-sequence budget outside [1, S]
 constexpr int ERR_EMPTY = 4;        // a sequence with no keys
+constexpr int ERR_TIMEOUT = 8;      // a grid-wide barrier wait ran out of time
 
 struct bf16_t { uint16_t bits; };
 struct fp16_t { uint16_t bits; };
@@ -133,6 +139,18 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
 }
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// cp_async16 whose source lines are marked for early eviction from L2 under
+// `policy` (createpolicy): for data read once per step, so that it does not
+// displace what the step reads again (scores, statistics).
+__device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void* src, unsigned long long policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ unsigned long long evict_first_policy() {
+  unsigned long long p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }

@@ -8,6 +8,8 @@
 
 namespace santa {
 
+constexpr int MAX_CTAS = 160;   // bound on the single-launch grid (aggregate slots per head)
+
 // Everything one decode call needs, already validated and carved out of the workspace.
 struct LaunchArgs {
   int dtype;       // 0 bf16, 1 fp16, 2 fp32
@@ -41,6 +43,11 @@ struct LaunchArgs {
   int32_t* jstart;         // [B, H, chunks_max + 1]
   float* head_max;         // [B, H]
   float* part_o;           // dense: [B, H, chunks_max, D] chunk partial outputs
+  // single-launch decode
+  float* agg_m;            // [B, H, MAX_CTAS] per-CTA max of s_n over the CTA's keys
+  float* agg_l;            // [B, H, MAX_CTAS] per-CTA sum of exp(s_n - agg_m)
+  uint32_t* ukeys;         // [B, H, S_max] sorted 24-bit uniform keys (i.i.d.)
+  unsigned long long* rcp_S;  // [B] ceil(2^64 / S_b)
   cudaStream_t stream;
 };
 
@@ -48,5 +55,7 @@ cudaError_t launch_score(const LaunchArgs& a);
 cudaError_t launch_combine(const LaunchArgs& a);
 cudaError_t launch_sample_gather(const LaunchArgs& a);
 cudaError_t launch_dense(const LaunchArgs& a);
+// The whole decode step in one cooperative launch (16-bit caches, Philox uniforms).
+cudaError_t launch_fused(const LaunchArgs& a, unsigned* bar_count, unsigned* bar_gen);
 
 }  // namespace santa

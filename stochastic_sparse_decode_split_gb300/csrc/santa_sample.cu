@@ -17,6 +17,7 @@
 
 #include "santa_common.cuh"
 #include "santa_launch.h"
+#include "santa_window.cuh"
 
 namespace santa {
 
@@ -43,24 +44,6 @@ __device__ __forceinline__ HeadCtx head_ctx(const LaunchArgs& a, int b) {
   return c;
 }
 
-// Probability masses are handled as fixed-point integers in units of 2^-40 of
-// the head-max key's mass (a key's mass relative to the max is <= 1).  Integer
-// sums are exact in any association, so every prefix is exactly monotone and
-// no FP64 arithmetic (slow on this part) is needed in any loop.  Conversion
-// truncates; masses below 2^-40 of the max key count as zero.
-constexpr int MASS_SHIFT = 40;
-
-// w * 2^40 rounded toward zero, for finite w in [0, 2^20], by integer operations.
-__device__ __forceinline__ long long mass_fixed(float w) {
-  const uint32_t bits = __float_as_uint(w);
-  const int e = (int)((bits >> 23) & 0xffu);
-  if (e == 0 || e == 0xff || (bits >> 31)) return 0;          // zero, subnormal, non-finite, negative
-  const long long m = (long long)((bits & 0x7fffffu) | 0x800000u);
-  const int sh = e - 127 - 23 + MASS_SHIFT;                  // w * 2^40 = m * 2^sh
-  if (sh >= 0) return m << min(sh, 39);
-  return sh > -64 ? (m >> -sh) : 0;
-}
-
 // Inclusive block-wide scan of one int64 per thread (NT threads).
 template <int NT>
 __device__ __forceinline__ long long block_inclusive_scan(long long v, long long* warp_tot) {
@@ -76,16 +59,6 @@ __device__ __forceinline__ long long block_inclusive_scan(long long v, long long
   for (int w = 0; w < warp; ++w) off += warp_tot[w];
   __syncthreads();
   return v + off;
-}
-
-// Inclusive warp scan of one int64 per lane.
-__device__ __forceinline__ long long warp_inclusive_scan(long long v, int lane) {
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const long long n = __shfl_up_sync(FULL, v, o);
-    if (lane >= o) v += n;
-  }
-  return v;
 }
 
 // ---------------------------------------------------------------------------
@@ -280,21 +253,6 @@ __host__ __device__ constexpr size_t sample_gather_smem(int G, int D) {
          (size_t)SG_WARPS * G * D * sizeof(float);
 }
 
-// lower_bound of v among the sorted values x held one per lane (lanes >= n hold +inf)
-__device__ __forceinline__ int lane_lower_bound(long long x, int n, long long v) {
-  int lo = 0, hi = n;
-#pragma unroll
-  for (int it = 0; it < 6; ++it) {
-    const int mid = (lo + hi) >> 1;
-    const long long xm = __shfl_sync(FULL, x, mid & 31);
-    if (lo < hi) {
-      if (xm < v) lo = mid + 1;
-      else hi = mid;
-    }
-  }
-  return lo;
-}
-
 template <typename T, int D, int GM>
 __global__ void __launch_bounds__(SG_THREADS)
 sample_gather_kernel(LaunchArgs a) {
@@ -358,34 +316,12 @@ sample_gather_kernel(LaunchArgs a) {
 #pragma unroll
     for (int g = 0; g < GM; ++g) {
       int cnt = 0;
-      const int nt = je[g][i] - js[g][i];
-      if (nt > 0) {  // warp-uniform
+      if (je[g][i] > js[g][i]) {  // warp-uniform
         const int64_t bh = bh0 + g;
-        const long long w = mass_fixed(expf(sv[g][i] - mst[g]));   // e^{-inf} = 0 past the sequence end
-        const long long F = warp_inclusive_scan(w, lane);
-        const long long total = __shfl_sync(FULL, F, 31);
-        const unsigned nz = __ballot_sync(FULL, w > 0);
-        const int last_nz = nz ? 31 - __clz(nz) : 0;             // rounding past the total goes here
-        int lb = 0, lb_total = 0;
-        for (int base = 0; base < nt; base += 32) {
-          const int n = min(32, nt - base);
-          long long x = (base == 0) ? th[g][i]
-                                    : ((lane < n) ? a.thresh[bh * a.S_max + js[g][i] + base + lane] : LLONG_MAX);
-          x = (lane < n) ? x - pb[g][i] : LLONG_MAX;
-          lb += lane_lower_bound(x, n, F);
-          lb_total += lane_lower_bound(x, n, total);
-        }
-        const int lb_up = __shfl_up_sync(FULL, lb, 1);
-        const int lb_prev = (lane == 0) ? 0 : lb_up;
-        cnt = lb - lb_prev;                                        // F_{lane-1} <= x < F_lane
-        if (lane == last_nz) cnt += nt - lb_total;                  // x >= the window's total
-        if (a.sample_idx) {
-          int32_t* dst = a.sample_idx + bh * a.S_max + js[g][i];
-          const int key = (w0 + i) * WIN + lane;
-          for (int j = lb_prev; j < lb; ++j) dst[j] = key;
-          if (lane == last_nz)
-            for (int j = lb_total; j < nt; ++j) dst[j] = key;
-        }
+        cnt = window_draws(sv[g][i], mst[g], th[g][i], je[g][i] - js[g][i], pb[g][i],
+                           a.thresh + bh * a.S_max + js[g][i],
+                           a.sample_idx ? a.sample_idx + bh * a.S_max + js[g][i] : nullptr, (w0 + i) * WIN + lane,
+                           lane);
       }
       cnt_s[(i * GM + g) * 32 + lane] = cnt;
       drawn[i] |= __ballot_sync(FULL, cnt > 0);
@@ -411,42 +347,8 @@ sample_gather_kernel(LaunchArgs a) {
 #pragma unroll
       for (int e = 0; e < TL::EPL; ++e) acc[g][e] = 0.f;
     const T* Vbase = reinterpret_cast<const T*>(a.V) + (hc.row0 * a.Hkv + kvh) * (int64_t)D + sub * TL::EPL;
-    constexpr int UNR = 8;
-    for (int i0 = slot; i0 < nrows; i0 += UNR * TL::KPI) {
-      uint4 vv[UNR][TL::NVEC];
-      int rk[UNR];
-#pragma unroll
-      for (int u = 0; u < UNR; ++u) {
-        const int i = i0 + u * TL::KPI;
-        rk[u] = (i < nrows) ? rows[i] : -1;
-        const int64_t key = (int64_t)(w0 + (rk[u] >> 5)) * WIN + (rk[u] & 31);
-#pragma unroll
-        for (int v = 0; v < TL::NVEC; ++v)
-          vv[u][v] = (rk[u] >= 0) ? ld_stream(Vbase + key * a.Hkv * D + v * (16 / TL::ES)) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int u = 0; u < UNR; ++u) {
-        if (rk[u] < 0) continue;
-        float vf[TL::EPL];
-#pragma unroll
-        for (int v = 0; v < TL::NVEC; ++v) Elem<T>::widen(vv[u][v], vf + v * (16 / TL::ES));
-        const int* cr = cnt_s + (rk[u] >> 5) * GM * 32 + (rk[u] & 31);
-#pragma unroll
-        for (int g = 0; g < GM; ++g) {
-          if (g < G) {
-            const float cg = (float)cr[g * 32];
-#pragma unroll
-            for (int e = 0; e < TL::EPL; ++e) acc[g][e] = fmaf(cg, vf[e], acc[g][e]);
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int o = TL::LPK; o < 32; o <<= 1)
-#pragma unroll
-      for (int g = 0; g < GM; ++g)
-#pragma unroll
-        for (int e = 0; e < TL::EPL; ++e) acc[g][e] += __shfl_xor_sync(FULL, acc[g][e], o);
+    gather_rows<T, D, GM>(acc, rows, nrows, cnt_s, Vbase, w0, a.Hkv, G, lane);
+    reduce_slots<T, D, GM>(acc);
     if (slot == 0) {
 #pragma unroll
       for (int g = 0; g < GM; ++g)

@@ -7,6 +7,7 @@
 
 #include "santa_common.cuh"
 #include "santa_launch.h"
+#include "santa_stream.cuh"
 
 namespace santa {
 
@@ -583,27 +584,67 @@ static cudaError_t allow_smem(KernelT kern, size_t bytes) {
   return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-// Width of a score-pass unit in KV heads: the largest power of two <= 8 dividing H_kv.
-static int unit_heads(int Hkv) {
-  int w = 8;
-  while (w > 1 && Hkv % w) w >>= 1;
-  return w;
+// Score pass for 16-bit caches: the per-warp streaming pipelines of
+// santa_stream.cuh; the CTA also clears `out` (the sampler accumulates into it).
+template <typename T, int D>
+__global__ void __launch_bounds__(SB_THREADS, 1)
+score_warp_kernel(StreamArgs a, float* __restrict__ out, int64_t out_n4) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ int start[4];
+  if (threadIdx.x < 32)
+    unit_range_start(a.kv_offsets, a.nk_max, a.B, a.Hkv / a.W, SB_UNIT_ROWS_X_W / a.W, blockIdx.x, gridDim.x, start);
+  __syncthreads();
+  allow_dependents();  // the next stage may launch now; it waits for this grid before reading
+  if (out)
+    for (int64_t i = (int64_t)blockIdx.x * SB_THREADS + threadIdx.x; i < out_n4; i += (int64_t)gridDim.x * SB_THREADS)
+      reinterpret_cast<float4*>(out)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  stream_scores<T, D>(a, smem_addr(smem), start);
+}
+
+template <typename T, int D>
+static cudaError_t launch_score_warp(const LaunchArgs& a) {
+  using Gm = StreamGeom<T, D>;
+  StreamArgs s;
+  s.q = a.q;
+  s.K = a.K;
+  s.kv_offsets = a.kv_offsets;
+  s.nk_max = a.nk_max;
+  s.B = a.B;
+  s.H = a.H;
+  s.Hkv = a.Hkv;
+  s.W = unit_heads(a.Hkv);
+  s.scale = a.scale;
+  s.stash = a.stash;
+  s.sub_max = a.tile_max;
+  s.sub_sum = a.tile_sum;
+  s.subs_max = a.chunks_max;
+  const int unit_rows = SB_UNIT_ROWS_X_W / s.W;
+  const long long units = (long long)a.B * ((a.nk_max + unit_rows - 1) / unit_rows) * (a.Hkv / s.W);
+  const unsigned grid = (unsigned)std::min<long long>(units, (long long)a.num_sms);
+  cudaError_t e = allow_smem(score_warp_kernel<T, D>, Gm::SMEM);
+  if (e != cudaSuccess) return e;
+  score_warp_kernel<T, D><<<grid, SB_THREADS, Gm::SMEM, a.stream>>>(s, a.out, a.out ? (int64_t)a.B * a.H * D / 4 : 0);
+  return cudaGetLastError();
 }
 
 template <typename T, int D>
 static cudaError_t launch_score_t(const LaunchArgs& a) {
-  const int W = unit_heads(a.Hkv);
-  const int unit_rows = 32 * (UNIT_TASKS / W);
-  const long long units = (long long)a.B * ((a.nk_max + unit_rows - 1) / unit_rows) * (a.Hkv / W);
-  const unsigned grid = (unsigned)std::min<long long>(units, (long long)a.num_sms);
-  auto kern = (sizeof(T) == 2 || a.H / a.Hkv <= HP) ? score_stream_kernel<T, D, 1> : score_stream_kernel<T, D, 2>;
-  const size_t smem = stream_smem_bytes<T, D>();
-  cudaError_t e = allow_smem(kern, smem);
-  if (e != cudaSuccess) return e;
-  kern<<<grid, ST_THREADS, smem, a.stream>>>((const T*)a.q, (const T*)a.K, a.kv_offsets, a.nk_max, a.B, a.H,
-                                             a.Hkv, W, a.scale, a.stash, a.tile_max, a.tile_sum, a.chunks_max,
-                                             a.out);
-  return cudaGetLastError();
+  if constexpr (sizeof(T) == 2) {
+    return launch_score_warp<T, D>(a);
+  } else {
+    const int W = unit_heads(a.Hkv);
+    const int unit_rows = 32 * (UNIT_TASKS / W);
+    const long long units = (long long)a.B * ((a.nk_max + unit_rows - 1) / unit_rows) * (a.Hkv / W);
+    const unsigned grid = (unsigned)std::min<long long>(units, (long long)a.num_sms);
+    auto kern = (a.H / a.Hkv <= HP) ? score_stream_kernel<T, D, 1> : score_stream_kernel<T, D, 2>;
+    const size_t smem = stream_smem_bytes<T, D>();
+    cudaError_t e = allow_smem(kern, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, ST_THREADS, smem, a.stream>>>((const T*)a.q, (const T*)a.K, a.kv_offsets, a.nk_max, a.B, a.H,
+                                               a.Hkv, W, a.scale, a.stash, a.tile_max, a.tile_sum, a.chunks_max,
+                                               a.out);
+    return cudaGetLastError();
+  }
 }
 
 template <typename T, int D>
