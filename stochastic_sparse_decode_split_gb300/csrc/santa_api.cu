@@ -20,7 +20,8 @@ constexpr size_t BAR_COUNT = 64, BAR_GEN = 128;  // header offsets of the grid-b
 size_t up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
 
 struct Layout {
-  size_t stash, tile_max, tile_sum, prefix, thresh, jstart, head_max, part_o, agg_m, agg_l, ukeys, rcp_S, total;
+  size_t stash, tile_max, tile_sum, prefix, thresh, jstart, head_max, part_o, agg_m, agg_l, ukeys, rcp_S;
+  size_t bnd_P, bnd_T, bnd_jlo, bnd_jhi, head_Z, total;
   int64_t chunks, groups;
 };
 
@@ -70,6 +71,11 @@ Layout santa_layout(const santa_params_t* p) {
   L.agg_l = off;    off += up(B * H * santa::MAX_CTAS * sizeof(float));
   L.ukeys = off;    off += up(B * H * S * sizeof(uint32_t));
   L.rcp_S = off;    off += up(B * sizeof(unsigned long long));
+  L.bnd_P = off;    off += up(B * H * santa::MAX_CTAS * sizeof(long long));
+  L.bnd_T = off;    off += up(B * H * santa::MAX_CTAS * sizeof(long long));
+  L.bnd_jlo = off;  off += up(B * H * santa::MAX_CTAS * sizeof(int32_t));
+  L.bnd_jhi = off;  off += up(B * H * santa::MAX_CTAS * sizeof(int32_t));
+  L.head_Z = off;   off += up(B * H * sizeof(long long));
   L.part_o = 0;
   L.total = off;
   return L;
@@ -156,6 +162,11 @@ santa_status_t decode_impl(const santa_params_t* p, int32_t variant, const void*
   a.agg_l = reinterpret_cast<float*>(w + L.agg_l);
   a.ukeys = reinterpret_cast<uint32_t*>(w + L.ukeys);
   a.rcp_S = reinterpret_cast<unsigned long long*>(w + L.rcp_S);
+  a.bnd_P = reinterpret_cast<long long*>(w + L.bnd_P);
+  a.bnd_T = reinterpret_cast<long long*>(w + L.bnd_T);
+  a.bnd_jlo = reinterpret_cast<int32_t*>(w + L.bnd_jlo);
+  a.bnd_jhi = reinterpret_cast<int32_t*>(w + L.bnd_jhi);
+  a.head_Z = reinterpret_cast<long long*>(w + L.head_Z);
 
   // 16-bit caches with Philox uniforms: the whole step in one cooperative
   // launch; otherwise (fp32, caller uniforms, per-stage events) three stages.

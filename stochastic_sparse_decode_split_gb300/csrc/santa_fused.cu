@@ -40,7 +40,6 @@
 namespace santa {
 
 constexpr int POOL_CAP = 4096;   // thresholds of one piece kept in shared memory
-constexpr int RCAP = 64;         // drawn rows listed per warp before a gather
 
 // ---------------------------------------------------------------------------
 // Exact thresholds.  A threshold is theta = floor(N * Z / (div * 2^24)) for an
@@ -176,29 +175,42 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ void grid_barrier(unsigned* count, unsigned* gen, int* err) {
-  __syncthreads();
+// Arrival half of the barrier (thread 0 acts; call after __syncthreads):
+// returns the generation seen before arriving, for grid_wait.
+__device__ __forceinline__ unsigned grid_arrive(unsigned* count, unsigned* gen) {
+  unsigned g = 0;
   if (threadIdx.x == 0) {
-    const unsigned g = ld_acquire(gen);
+    g = ld_acquire(gen);
     __threadfence();
     const unsigned arrived = atomicAdd(count, 1u);
     if (arrived == gridDim.x - 1) {
       atomicExch(count, 0u);
       __threadfence();
       atomicAdd(gen, 1u);
-    } else {
-      const unsigned long long t0 = global_ns();
-      while (ld_acquire(gen) == g) {
-        if (global_ns() - t0 > WAIT_LIMIT_NS) {
-          flag_error(err, ERR_TIMEOUT);
-          break;
-        }
-        __nanosleep(64);
+    }
+  }
+  return g;
+}
+// Waiting half: thread 0 spins until the generation moves past g (bounded),
+// then the CTA proceeds together.
+__device__ __forceinline__ void grid_wait(const unsigned* gen, unsigned g, int* err) {
+  if (threadIdx.x == 0) {
+    const unsigned long long t0 = global_ns();
+    while (ld_acquire(gen) == g) {
+      if (global_ns() - t0 > WAIT_LIMIT_NS) {
+        flag_error(err, ERR_TIMEOUT);
+        break;
       }
+      __nanosleep(64);
     }
     __threadfence();
   }
   __syncthreads();
+}
+__device__ __forceinline__ void grid_barrier(unsigned* count, unsigned* gen, int* err) {
+  __syncthreads();
+  const unsigned g = grid_arrive(count, gen);
+  grid_wait(gen, g, err);
 }
 
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
@@ -266,48 +278,11 @@ __device__ __forceinline__ int seq_error(const LaunchArgs& a, int b, int& S_b) {
 
 // Per-head state of phase B (shared memory).
 struct HeadInfo {
-  int jlo, jhi;   // this CTA's threshold range [jlo, jhi)
-  int off;        // offset of its thresholds in the shared pool, -1: in the global array
-  float mstar;    // the head's max score
+  long long pown;   // mass prefix of this CTA's key range
+  int jlo, jhi;     // this CTA's threshold range [jlo, jhi)
+  int off;          // offset of its thresholds in the shared pool, -1: in the global array
+  float mstar;      // the head's max score
 };
-
-// Count-weighted gather-and-add of the listed rows keys[0..n) (key indices of
-// one sequence and KV head) with counts cnt[r * GM + g] into acc (head g, the
-// lane's output columns; partial sums spread over the row slots).
-template <typename T, int D, int GM>
-__device__ __forceinline__ void gather_list(float (&acc)[GM][Tile<T, D>::EPL], const int* keys, const int* cnt,
-                                            int n, const T* __restrict__ Vbase, int Hkv, int G, int lane) {
-  using TL = Tile<T, D>;
-  const int slot = lane / TL::LPK;
-  constexpr int UNR = 4;
-  for (int r0 = 0; r0 < n; r0 += UNR * TL::KPI) {
-    uint4 vv[UNR][TL::NVEC];
-#pragma unroll
-    for (int u = 0; u < UNR; ++u) {
-      const int r = r0 + u * TL::KPI + slot;
-#pragma unroll
-      for (int v = 0; v < TL::NVEC; ++v)
-        vv[u][v] = r < n ? ld_stream(Vbase + (int64_t)keys[r] * Hkv * D + v * (16 / TL::ES)) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int u = 0; u < UNR; ++u) {
-      const int r = r0 + u * TL::KPI + slot;
-      if (r0 + u * TL::KPI < n) {   // warp-uniform
-        float vf[TL::EPL];
-#pragma unroll
-        for (int v = 0; v < TL::NVEC; ++v) Elem<T>::widen(vv[u][v], vf + v * (16 / TL::ES));
-#pragma unroll
-        for (int g = 0; g < GM; ++g) {
-          if (g < G) {
-            const float cg = r < n ? (float)cnt[r * GM + g] : 0.f;
-#pragma unroll
-            for (int e = 0; e < TL::EPL; ++e) acc[g][e] = fmaf(cg, vf[e], acc[g][e]);
-          }
-        }
-      }
-    }
-  }
-}
 
 template <typename T, int D, int GM>
 __global__ void __launch_bounds__(SB_THREADS, 1)
@@ -317,7 +292,6 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int start[4];
   __shared__ long long range[2];
-  __shared__ int pool_used;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int G = a.H / a.Hkv, W = unit_heads(a.Hkv), n_hg = a.Hkv / W;
   const int unit_rows = SB_UNIT_ROWS_X_W / W;
@@ -436,161 +410,294 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     }
   });
 
-  grid_barrier(bar_count, bar_gen, a.err);
-
-  // ======================= phase B =======================
+  // ---------------------------------------------------------------------------
+  // shared-memory plan of phase B (inside the ring, free by now)
+  // ---------------------------------------------------------------------------
   const long long n_units = range[0];
-  auto nonempty = [&](int i) {   // CTA i owns at least one unit
-    return n_units >= P || n_units * i / P < n_units * (i + 1) / P;
-  };
-  // fixed shared-memory regions (inside the ring, free by now)
   float* obuf = reinterpret_cast<float*>(smem);                                   // [GW][D] this CTA's sums
-  int* cnt_all = reinterpret_cast<int*>(obuf + GM * 8 * D);                      // [warps][RCAP][GM]
-  int* rows_all = cnt_all + SB_WARPS * RCAP * GM;                                 // [warps][RCAP]
-  HeadInfo* hinfo = reinterpret_cast<HeadInfo*>(rows_all + SB_WARPS * RCAP);      // [GW]
+  HeadInfo* hinfo = reinterpret_cast<HeadInfo*>(obuf + GM * 8 * D);              // [GW]
   long long* pool = reinterpret_cast<long long*>(hinfo + GM * 8);                // [POOL_CAP]
   unsigned char* var0 = reinterpret_cast<unsigned char*>(pool + POOL_CAP);       // per-piece staging
-  int* cnt_s = cnt_all + warp * RCAP * GM;
-  int* rows = rows_all + warp * RCAP;
   const size_t var_cap = Gm::SMEM - (size_t)(var0 - smem);
-
-  for_each_piece(a, n_hg, unit_rows, start, range[1], [&](const Piece& p) {
-    int S_b;
-    if (seq_error(a, p.b, S_b)) return;   // uniform over the CTA
-    const long long ufirst = p.ubase, ulast = p.ubase + p.units_b - 1;   // units of (b, hg)
-    const int i_first = (int)(((ufirst + 1) * P - 1) / n_units), i_last = (int)(((ulast + 1) * P - 1) / n_units);
-    const int ncov = i_last - i_first + 1;
-    const int c_lo = p.kb0 * C_of_unit;
-    const int c_hi = (int)min((int64_t)(p.kb0 + p.nkb) * C_of_unit, (p.nk + SUB - 1) / SUB);
-    const int nch = c_hi - c_lo;
-    const int64_t key_lo = (int64_t)c_lo * SUB, key_hi = min((int64_t)c_hi * SUB, p.nk);
-    const int nkeys = (int)(key_hi - key_lo);
-    const int64_t bh0 = (int64_t)p.b * a.H + (int64_t)p.hg * GW;   // first head of the group
-
-    // ---- staging plan: aggregates always; chunk statistics + chunk tables
-    //      and scores when they fit.  Rows are copied in 16-byte pieces from
-    //      the 16-byte boundary at or below their first element (reading up
-    //      to 12 bytes either side of a row stays inside the workspace).
+  __shared__ int pool_used, n_items, n_rows;
+  __shared__ float red_f[SB_WARPS];
+  __shared__ long long red_ll[SB_WARPS];
+  struct Stage {
+    int c_lo, c_hi, nch, nkeys, cap_ch, cap_st;
+    int64_t key_lo;
+    float *mx, *sm, *st;
+    long long* pref;
+    int *js, *items, *table, *rows;
+    bool ch, sto, tab;   // in shared memory: chunk statistics + tables + items / scores / count table
+  };
+  auto plan = [&](const Piece& p) {
+    Stage g;
+    g.c_lo = p.kb0 * C_of_unit;
+    g.c_hi = (int)min((int64_t)(p.kb0 + p.nkb) * C_of_unit, (p.nk + SUB - 1) / SUB);
+    g.nch = g.c_hi - g.c_lo;
+    g.key_lo = (int64_t)g.c_lo * SUB;
+    g.nkeys = (int)(min((int64_t)g.c_hi * SUB, p.nk) - g.key_lo);
+    g.cap_ch = (g.nch + 7) & ~3;   // floats per staged row (16-byte pieces from the boundary below)
+    g.cap_st = (g.nkeys + 7) & ~3;
     size_t off = 0;
     auto take = [&](size_t bytes) {
       const size_t o = (off + 15) & ~(size_t)15;
       off = o + bytes;
       return var0 + o;
     };
-    auto row_cap = [](int len) { return (len + 7) & ~3; };   // floats per staged row
-    const int cap_agg = row_cap(ncov), cap_ch = row_cap(nch), cap_st = row_cap(nkeys);
-    float* s_am = reinterpret_cast<float*>(take((size_t)GW * cap_agg * 4));
-    float* s_al = reinterpret_cast<float*>(take((size_t)GW * cap_agg * 4));
-    const size_t off_after_agg = off;
-    float* s_mx = reinterpret_cast<float*>(take((size_t)GW * cap_ch * 4));
-    float* s_sm = reinterpret_cast<float*>(take((size_t)GW * cap_ch * 4));
-    long long* s_pref = reinterpret_cast<long long*>(take((size_t)GW * nch * 8));
-    int* s_js = reinterpret_cast<int*>(take((size_t)GW * nch * 4));
-    const bool ch_smem = off <= var_cap;
-    if (!ch_smem) off = off_after_agg;
-    float* s_st = reinterpret_cast<float*>(take((size_t)GW * cap_st * 4));
-    const bool st_smem = off <= var_cap;
-    // row h of length len starting at global float index g0 -> s_row + h * cap (+ (g0 & 3))
-    auto stage_row = [&](float* s_row, const float* base, int64_t g0, int len) {
-      const int64_t a0 = g0 & ~(int64_t)3;
-      const int n16 = (int)((g0 + len - a0 + 3) >> 2);
-      for (int j = lane; j < n16; j += 32) cp_async16(smem_addr(s_row + 4 * j), base + a0 + 4 * j);
-    };
+    g.mx = reinterpret_cast<float*>(take((size_t)GW * g.cap_ch * 4));
+    g.sm = reinterpret_cast<float*>(take((size_t)GW * g.cap_ch * 4));
+    g.pref = reinterpret_cast<long long*>(take((size_t)GW * g.nch * 8));
+    g.js = reinterpret_cast<int*>(take((size_t)GW * g.nch * 4));
+    g.items = reinterpret_cast<int*>(take((size_t)GW * g.nch * 4));
+    g.ch = off <= var_cap;
+    if (!g.ch) off = 0;
+    size_t keep = off;
+    g.st = reinterpret_cast<float*>(take((size_t)GW * g.cap_st * 4));
+    g.sto = off <= var_cap;
+    if (!g.sto) off = keep;
+    keep = off;
+    g.table = reinterpret_cast<int*>(take((size_t)W * g.nkeys * GM * 4));
+    g.rows = reinterpret_cast<int*>(take((size_t)W * g.nkeys * 4));
+    g.tab = off <= var_cap;
+    return g;
+  };
+  // rows are copied in 16-byte pieces from the 16-byte boundary at or below
+  // their first element (reading up to 12 bytes either side of a row stays
+  // inside the workspace); row h lands at s_row + h * cap + (g0 & 3)
+  auto stage_row = [&](float* s_row, const float* base, int64_t g0, int len) {
+    const int64_t a0 = g0 & ~(int64_t)3;
+    const int n16 = (int)((g0 + len - a0 + 3) >> 2);
+    for (int j = lane; j < n16; j += 32) cp_async16(smem_addr(s_row + 4 * j), base + a0 + 4 * j);
+  };
+  auto stage = [&](const Piece& p, const Stage& g) {
+    const int64_t bh0 = (int64_t)p.b * a.H + (int64_t)p.hg * GW;
     for (int h = warp; h < GW; h += SB_WARPS) {
       const int64_t bh = bh0 + h;
-      stage_row(s_am + h * cap_agg, a.agg_m, bh * MAX_CTAS + i_first, ncov);
-      stage_row(s_al + h * cap_agg, a.agg_l, bh * MAX_CTAS + i_first, ncov);
-      if (ch_smem) {
-        stage_row(s_mx + h * cap_ch, a.tile_max, bh * a.chunks_max + c_lo, nch);
-        stage_row(s_sm + h * cap_ch, a.tile_sum, bh * a.chunks_max + c_lo, nch);
+      if (g.ch) {
+        stage_row(g.mx + h * g.cap_ch, a.tile_max, bh * a.chunks_max + g.c_lo, g.nch);
+        stage_row(g.sm + h * g.cap_ch, a.tile_sum, bh * a.chunks_max + g.c_lo, g.nch);
       }
-      if (st_smem) stage_row(s_st + h * cap_st, a.stash, bh * a.nk_max + key_lo, nkeys);
+      if (g.sto) stage_row(g.st + h * g.cap_st, a.stash, bh * a.nk_max + g.key_lo, g.nkeys);
     }
     cp_async_commit();
+  };
+
+  // first barrier; while waiting, this CTA stages its first piece's chunk
+  // statistics and scores (its own data, already written)
+  __syncthreads();
+  const unsigned gen1 = grid_arrive(bar_count, bar_gen);
+  bool prestaged = false;
+  if (start[3] > 0) {
+    UnitCursor c0;
+    c0.kv_offsets = a.kv_offsets;
+    c0.nk_max = a.nk_max;
+    c0.B = a.B;
+    c0.n_hg = n_hg;
+    c0.unit_rows = unit_rows;
+    c0.b = start[0];
+    c0.hg = start[1];
+    c0.kb = start[2];
+    c0.load_seq();
+    Piece p0;
+    p0.b = c0.b;
+    p0.hg = c0.hg;
+    p0.kb0 = c0.kb;
+    p0.nkb = min(start[3], c0.units_b - c0.kb);
+    p0.nk = c0.nk;
+    stage(p0, plan(p0));
+    prestaged = true;
+  }
+  grid_wait(bar_gen, gen1, a.err);
+
+  // ======================= phase B0: per-head globals =======================
+  // From the aggregates of the CTAs covering a head's (sequence, KV-head
+  // group): the head max m*, the total mass Z, and for each covering CTA i its
+  // mass prefix P_i, mass T_i and threshold range [count(P_i), count(P_i + T_i)).
+  // Heads covered by more than 32 CTAs take a whole CTA (one covering CTA per
+  // thread); the others a warp (one per lane).
+  auto nonempty = [&](int i) {   // CTA i owns at least one unit
+    return n_units >= P || n_units * i / P < n_units * (i + 1) / P;
+  };
+  struct HeadGeom {
+    int b, h, S_b, i_first, i_last;
+    bool ok;
+  };
+  auto geom = [&](long long bh) {   // the same in every lane of a warp
+    HeadGeom q;
+    q.b = (int)(bh / a.H);
+    q.h = (int)(bh % a.H);
+    q.ok = seq_error(a, q.b, q.S_b) == 0;
+    int64_t r0_, nk_;
+    const int units_b = UnitCursor::seq_units(a.kv_offsets, a.nk_max, unit_rows, q.b, r0_, nk_);
+    long long base = (long long)q.b * units_b;
+    if (a.kv_offsets) {
+      base = 0;
+      for (int b0 = 0; b0 < q.b; b0 += 32) {
+        int64_t r1, n1;
+        long long u = (b0 + lane < q.b) ? UnitCursor::seq_units(a.kv_offsets, a.nk_max, unit_rows, b0 + lane, r1, n1) : 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) u += __shfl_xor_sync(FULL, u, o);
+        base += u;
+      }
+    }
+    const long long U = base * n_hg + (long long)(q.h / GW) * units_b;   // unit (b, hg, kb = 0)
+    q.i_first = (int)(((U + 1) * P - 1) / n_units);
+    q.i_last = (int)(((U + units_b) * P - 1) / n_units);
+    q.ok = q.ok && units_b > 0;
+    return q;
+  };
+  auto make_draws = [&](const HeadGeom& q, long long bh, long long Z) {
+    Draws dr;
+    dr.variant = a.variant;
+    dr.S = q.S_b;
+    dr.h = q.h;
+    dr.b = q.b;
+    dr.step = a.step;
+    dr.k0 = k0;
+    dr.k1 = k1;
+    dr.ksys = a.variant == VAR_SYS ? philox4x32_10(make_uint4(0u, (uint32_t)q.h, (uint32_t)q.b, a.step), k0, k1).x >> 8
+                                   : 0u;
+    dr.sorted = a.ukeys + bh * a.S_max;
+    dr.tc = a.variant == VAR_IID ? theta_ctx(Z, 1u, 0ull) : theta_ctx(Z, (unsigned)q.S_b, a.rcp_S[q.b]);
+    return dr;
+  };
+  auto write_bnd = [&](const Draws& dr, long long bh, int i, long long Pi, long long Ti) {
+    const int64_t o = bh * MAX_CTAS + i;
+    a.bnd_P[o] = Pi;
+    a.bnd_T[o] = Ti;
+    // counts of the i.i.d. sorted thresholds are taken in the CTA that owns the range
+    a.bnd_jlo[o] = a.variant == VAR_IID ? -1 : dr.count_below(Pi, 0, 32, lane, 0);
+    a.bnd_jhi[o] = a.variant == VAR_IID ? -1 : dr.count_below(Pi + Ti, 0, 32, lane, 0);
+  };
+  // (1) wide heads: one CTA each
+  for (long long bh = cta; bh < (long long)a.B * a.H; bh += P) {
+    const HeadGeom q = geom(bh);
+    const int ncov = q.i_last - q.i_first + 1;
+    if (!q.ok || ncov <= 32) continue;   // uniform over the CTA
+    const int i = q.i_first + tid;
+    const bool ok = tid < ncov && nonempty(i);
+    const float mi = ok ? a.agg_m[bh * MAX_CTAS + i] : -INFINITY;
+    const float li = ok ? a.agg_l[bh * MAX_CTAS + i] : 0.f;
+    float m = warp_max(mi);
+    if (lane == 0) red_f[warp] = m;
+    __syncthreads();
+    m = red_f[0];
+#pragma unroll
+    for (int w = 1; w < SB_WARPS; ++w) m = fmaxf(m, red_f[w]);
+    const long long Ti = ok ? fixed40(fast_exp(mi - m) * li) : 0;
+    const long long incl = warp_inclusive_scan(Ti, lane);
+    if (lane == 31) red_ll[warp] = incl;
+    __syncthreads();
+    long long before = 0, Z = 0;
+#pragma unroll
+    for (int w = 0; w < SB_WARPS; ++w) {
+      before += w < warp ? red_ll[w] : 0;
+      Z += red_ll[w];
+    }
+    const Draws dr = make_draws(q, bh, Z);
+    if (tid < ncov) write_bnd(dr, bh, i, before + incl - Ti, Ti);
+    if (tid == 0) {
+      a.head_max[bh] = m;
+      a.head_Z[bh] = Z;
+    }
+    __syncthreads();
+  }
+  // (2) narrow heads: one warp each
+  for (long long bh = (long long)warp * P + cta; bh < (long long)a.B * a.H; bh += (long long)SB_WARPS * P) {
+    const HeadGeom q = geom(bh);
+    const int ncov = q.i_last - q.i_first + 1;
+    if (!q.ok || ncov > 32) continue;   // warp-uniform
+    const int i = q.i_first + lane;
+    const bool ok = lane < ncov && nonempty(i);
+    const float mi = ok ? a.agg_m[bh * MAX_CTAS + i] : -INFINITY;
+    const float li = ok ? a.agg_l[bh * MAX_CTAS + i] : 0.f;
+    const float m = warp_max(mi);
+    const long long Ti = ok ? fixed40(fast_exp(mi - m) * li) : 0;
+    const long long incl = warp_inclusive_scan(Ti, lane);
+    const long long Z = __shfl_sync(FULL, incl, 31);
+    const Draws dr = make_draws(q, bh, Z);
+    if (lane < ncov) write_bnd(dr, bh, i, incl - Ti, Ti);
+    if (lane == 0) {
+      a.head_max[bh] = m;
+      a.head_Z[bh] = Z;
+    }
+  }
+
+  grid_barrier(bar_count, bar_gen, a.err);
+
+  // ======================= phase B1: this CTA's draws =======================
+  int piece_no = 0;
+  for_each_piece(a, n_hg, unit_rows, start, range[1], [&](const Piece& p) {
+    int S_b;
+    const bool bad = seq_error(a, p.b, S_b) != 0;
+    const Stage g = plan(p);
+    if (!(piece_no == 0 && prestaged) && !bad) stage(p, g);
+    ++piece_no;
+    if (bad) return;   // uniform over the CTA
+    const int64_t bh0 = (int64_t)p.b * a.H + (int64_t)p.hg * GW;   // first head of the group
     for (int i = tid; i < GW * D; i += SB_THREADS) obuf[i] = 0.f;
-    if (tid == 0) pool_used = 0;
-    const unsigned long long rcp = a.rcp_S[p.b];
+    if (g.tab)
+      for (int i = tid; i < W * g.nkeys * GM; i += SB_THREADS) g.table[i] = 0;
+    if (tid == 0) {
+      pool_used = 0;
+      n_items = 0;
+      n_rows = 0;
+    }
     cp_async_wait_all();
     __syncthreads();
 
-    // ---- per head (a group of lph lanes each, all heads at once): m*, Z,
-    //      this CTA's interval, its thresholds, and the prefix / first
-    //      threshold of each of its chunks
+    // ---- per head (groups of lph lanes, all heads at once): interval,
+    //      thresholds, the prefix / first threshold of each chunk, and the
+    //      list of chunks that hold thresholds
     if (warp_on) {
       const int h = p.hg * GW + hl;
       const int64_t bh = bh0 + hl;
-      const int oa = (int)((bh * MAX_CTAS + i_first) & 3);
-      const float* am = s_am + hl * cap_agg + oa;
-      const float* al = s_al + hl * cap_agg + oa;
-      float m = -INFINITY;
-      for (int i = r; i < ncov; i += lph)
-        if (nonempty(i_first + i)) m = fmaxf(m, am[i]);
-      const float mstar = grp_max(m, lph);
-      const int kseg = (ncov + lph - 1) / lph;   // lane r sums the CTAs [r kseg, (r + 1) kseg)
-      long long seg = 0, before = 0, Tc = 0;
-      for (int t = 0; t < kseg; ++t) {
-        const int i = r * kseg + t;
-        if (i < ncov && nonempty(i_first + i)) {
-          const long long Ti = fixed40(fast_exp(am[i] - mstar) * al[i]);
-          seg += Ti;
-          if (i_first + i < cta) before += Ti;
-          if (i_first + i == cta) Tc = Ti;
-        }
-      }
-      const long long incl = grp_scan(seg, r, lph);
-      const int own = min((cta - i_first) / kseg, lph - 1);
-      const long long P_own = __shfl_sync(FULL, incl - seg + before, own, lph);
-      const long long T_own = __shfl_sync(FULL, Tc, own, lph);
-      const long long Z = __shfl_sync(FULL, incl, lph - 1, lph);
-      Draws dr;
-      dr.variant = a.variant;
-      dr.S = S_b;
-      dr.h = h;
-      dr.b = p.b;
-      dr.step = a.step;
-      dr.k0 = k0;
-      dr.k1 = k1;
-      dr.ksys = a.variant == VAR_SYS
-                    ? philox4x32_10(make_uint4(0u, (uint32_t)h, (uint32_t)p.b, a.step), k0, k1).x >> 8
-                    : 0u;
-      dr.sorted = a.ukeys + bh * a.S_max;
-      dr.tc = a.variant == VAR_IID ? theta_ctx(Z, 1u, 0ull) : theta_ctx(Z, (unsigned)S_b, rcp);
-      int rounds = 1;
-      if (a.variant == VAR_IID)
+      const int64_t o = bh * MAX_CTAS + cta;
+      const long long P_own = a.bnd_P[o], T_own = a.bnd_T[o], Z = a.head_Z[bh];
+      int jlo = a.bnd_jlo[o], jhi = a.bnd_jhi[o];
+      const float mstar = a.head_max[bh];
+      HeadGeom q;
+      q.b = p.b;
+      q.h = h;
+      q.S_b = S_b;
+      const Draws dr = make_draws(q, bh, Z);
+      if (a.variant == VAR_IID) {
+        int rounds = 1;
         for (int span = S_b; span > 1; span = (span + lph - 1) / lph) ++rounds;
-      const int jlo = dr.count_below(P_own, r, lph, lane, rounds);
-      const int jhi = dr.count_below(P_own + T_own, r, lph, lane, rounds);
+        jlo = dr.count_below(P_own, r, lph, lane, rounds);
+        jhi = dr.count_below(P_own + T_own, r, lph, lane, rounds);
+      }
       const int nt = jhi - jlo;
       int toff = -1;
       if (r == 0 && hv && nt > 0) {
-        const int o = atomicAdd(&pool_used, nt);
-        toff = (o + nt <= POOL_CAP) ? o : -1;
+        const int qq = atomicAdd(&pool_used, nt);
+        toff = (qq + nt <= POOL_CAP) ? qq : -1;
       }
       toff = __shfl_sync(FULL, toff, 0, lph);
       long long* thp = toff >= 0 ? pool + toff : a.thresh + bh * a.S_max + jlo;
       if (hv)
         for (int j = jlo + r; j < jhi; j += lph) thp[j - jlo] = dr.theta(j);
       if (r == 0 && hv) {
+        hinfo[hl].pown = P_own;
         hinfo[hl].jlo = jlo;
         hinfo[hl].jhi = jhi;
         hinfo[hl].off = toff;
         hinfo[hl].mstar = mstar;
-        a.head_max[bh] = mstar;
       }
       __syncwarp();
-      // chunk masses of this CTA's chunks, exclusive prefix from P_own
-      const int oc = (int)((bh * a.chunks_max + c_lo) & 3);
-      const float* mx = ch_smem ? s_mx + hl * cap_ch + oc : a.tile_max + bh * a.chunks_max + c_lo;
-      const float* sm = ch_smem ? s_sm + hl * cap_ch + oc : a.tile_sum + bh * a.chunks_max + c_lo;
-      long long* pr = ch_smem ? s_pref + hl * nch : a.prefix + bh * cm1 + c_lo;
-      int* jsr = ch_smem ? s_js + hl * nch : a.jstart + bh * cm1 + c_lo;
+      const int oc = (int)((bh * a.chunks_max + g.c_lo) & 3);
+      const float* mx = g.ch ? g.mx + hl * g.cap_ch + oc : a.tile_max + bh * a.chunks_max + g.c_lo;
+      const float* sm = g.ch ? g.sm + hl * g.cap_ch + oc : a.tile_sum + bh * a.chunks_max + g.c_lo;
+      long long* pr = g.ch ? g.pref + hl * g.nch : a.prefix + bh * cm1 + g.c_lo;
+      int* jsr = g.ch ? g.js + hl * g.nch : a.jstart + bh * cm1 + g.c_lo;
       long long run = P_own;
-      for (int c0 = 0; c0 < nch; c0 += lph) {
+      for (int c0 = 0; c0 < g.nch; c0 += lph) {
         const int c = c0 + r;
-        const long long Wc = c < nch ? fixed40(fast_exp(mx[c] - mstar) * sm[c]) : 0;
+        const long long Wc = c < g.nch ? fixed40(fast_exp(mx[c] - mstar) * sm[c]) : 0;
         const long long ci = grp_scan(Wc, r, lph);
         const long long pref = run + ci - Wc;
-        if (c < nch && hv) {
+        if (c < g.nch && hv) {
           int lo = 0, hi = nt;   // first threshold >= pref among [jlo, jhi)
           while (lo < hi) {
             const int mid = (lo + hi) >> 1;
@@ -602,153 +709,145 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
         }
         run += __shfl_sync(FULL, ci, lph - 1, lph);
       }
-    }
-    __syncthreads();   // per-head intervals, chunk tables and thresholds visible
-
-    // ---- per (KV head, 32-key window) with thresholds: draws, the union of
-    //      the drawn rows listed per warp, count-weighted gather into obuf.
-    //      Warp w takes a contiguous block of the (KV head, window) list, so
-    //      it gathers and flushes when the KV head changes or its list is full.
-    const int w_lo = c_lo / 2, nwin = (nch + 1) / 2;
-    const int ntask = W * nwin;
-    const int t_begin = (int)((long long)ntask * warp / SB_WARPS);
-    const int t_end = (int)((long long)ntask * (warp + 1) / SB_WARPS);
-    int nrows = 0, cur_wk = -1;
-    auto flush = [&]() {   // warp-uniform
-      if (nrows > 0) {
-        const int sub = lane % TL::LPK;
-        float acc[GM][TL::EPL];
-#pragma unroll
-        for (int g = 0; g < GM; ++g)
-#pragma unroll
-          for (int e = 0; e < TL::EPL; ++e) acc[g][e] = 0.f;
-        const T* Vb = reinterpret_cast<const T*>(a.V) + (p.row0 * a.Hkv + (int64_t)(p.hg * W + cur_wk)) * (int64_t)D +
-                      sub * TL::EPL;
-        gather_list<T, D, GM>(acc, rows, cnt_s, nrows, Vb, a.Hkv, G, lane);
-        reduce_slots<T, D, GM>(acc);
-        if (lane < TL::LPK) {
-#pragma unroll
-          for (int g = 0; g < GM; ++g)
-            if (g < G)
-#pragma unroll
-              for (int e = 0; e < TL::EPL; ++e) atomicAdd(&obuf[(cur_wk * G + g) * D + sub * TL::EPL + e], acc[g][e]);
-        }
-      }
-      nrows = 0;
       __syncwarp();
-    };
-    for (int task = t_begin; task < t_end; ++task) {
-      const int wk = task / nwin, wi = task % nwin;
-      if (wk != cur_wk) {
-        flush();
-        cur_wk = wk;
-      }
-      const int w = w_lo + wi;
-      int js[GM], nt[GM];
-      long long pb[GM];
-      bool any = false;
-#pragma unroll
-      for (int g = 0; g < GM; ++g) {
-        js[g] = 0;
-        nt[g] = 0;
-        pb[g] = 0;
-        if (g < G) {
-          const int h2 = wk * G + g;
-          const int64_t bh = bh0 + h2;
-          const int* jsr = ch_smem ? s_js + h2 * nch : a.jstart + bh * cm1 + c_lo;
-          js[g] = jsr[2 * wi];
-          const int je = (2 * wi + 2 < nch) ? jsr[2 * wi + 2] : hinfo[h2].jhi;
-          nt[g] = je - js[g];
-          if (nt[g] > 0) pb[g] = ch_smem ? s_pref[h2 * nch + 2 * wi] : a.prefix[bh * cm1 + c_lo + 2 * wi];
-          any |= nt[g] > 0;
+      if (g.ch && hv)
+        for (int c = r; c < g.nch; c += lph) {
+          const int je = c + 1 < g.nch ? jsr[c + 1] : jhi;
+          if (je > jsr[c]) g.items[atomicAdd(&n_items, 1)] = hl * 65536 + c;
+        }
+    }
+    __syncthreads();   // intervals, chunk tables, thresholds and items visible
+
+    // ---- per (head, 16-key chunk) holding thresholds, one half-warp each:
+    //      exact key-mass prefix over the chunk, one ballot per threshold
+    //      (the key is the first with F > x; a threshold at or beyond the
+    //      chunk's key total goes to its last nonzero key).  Counts go into
+    //      the (KV head, key) table (the union of the group's draws), or,
+    //      when the table does not fit, straight into a gather.
+    const int h16 = lane >> 4, l16 = lane & 15, hb = h16 * 16;
+    const int nwork = g.ch ? n_items : GW * g.nch;
+    for (int q0 = warp * 2; q0 < nwork; q0 += SB_WARPS * 2) {
+      const int q = q0 + h16;
+      const bool qv = q < nwork;
+      int qh = 0, qc = 0;
+      if (qv) {
+        if (g.ch) {
+          qh = g.items[q] >> 16;
+          qc = g.items[q] & 0xffff;
+        } else {
+          qh = q / g.nch;
+          qc = q % g.nch;
         }
       }
-      if (!any) continue;   // warp-uniform
-      const int64_t key = (int64_t)w * WIN + lane;
-      // all heads of the window at once: key masses, exact prefixes, thresholds
-      long long F[GM], th0[GM];
-      float mst[GM];
-      int lastnz[GM], cnt[GM];
+      const int* jsr = g.ch ? g.js + qh * g.nch : a.jstart + (bh0 + qh) * cm1 + g.c_lo;
+      const HeadInfo hi = hinfo[qh];
+      const int j0 = qv ? jsr[qc] : 0;
+      const int j1 = qv ? (qc + 1 < g.nch ? jsr[qc + 1] : hi.jhi) : 0;
+      const int nthr = j1 - j0;
+      const int tmax = max(nthr, __shfl_xor_sync(FULL, nthr, 16));
+      if (tmax == 0) continue;   // warp-uniform
+      const int64_t bh = bh0 + qh;
+      const int64_t key = (int64_t)(g.c_lo + qc) * SUB + l16;
+      float sv = -INFINITY;
+      if (nthr > 0 && key < p.nk)
+        sv = g.sto ? g.st[qh * g.cap_st + (int)((bh * a.nk_max + g.key_lo) & 3) + (int)(key - g.key_lo)]
+                   : a.stash[bh * a.nk_max + key];
+      long long F = fixed40(fast_exp(sv - hi.mstar));   // e^{-inf} = 0 past the sequence end
+      const unsigned nzb = (__ballot_sync(FULL, F > 0) >> hb) & 0xffffu;
+      const int lastnz = nzb ? 31 - __clz(nzb) : 0;
 #pragma unroll
-      for (int g = 0; g < GM; ++g) {
-        const int h2 = g < G ? wk * G + g : 0;
-        const int64_t bh = bh0 + h2;
-        const HeadInfo hi = hinfo[h2];
-        mst[g] = hi.mstar;
-        float sv = -INFINITY;
-        if (nt[g] > 0 && key < p.nk)
-          sv = st_smem ? s_st[h2 * cap_st + (int)((bh * a.nk_max + key_lo) & 3) + (int)(key - key_lo)]
-                       : a.stash[bh * a.nk_max + key];
-        F[g] = fixed40(fast_exp(sv - mst[g]));   // e^{-inf} = 0 past the sequence end
-        th0[g] = LLONG_MAX;
-        if (lane < nt[g])
-          th0[g] = hi.off >= 0 ? pool[hi.off + js[g] - hi.jlo + lane] : a.thresh[bh * a.S_max + js[g] + lane];
-        cnt[g] = 0;
+      for (int o = 1; o < 16; o <<= 1) {
+        const long long n = __shfl_up_sync(FULL, F, o, 16);
+        if (l16 >= o) F += n;
       }
-#pragma unroll
-      for (int g = 0; g < GM; ++g) lastnz[g] = __ballot_sync(FULL, F[g] > 0);
-#pragma unroll
-      for (int g = 0; g < GM; ++g) lastnz[g] = lastnz[g] ? 31 - __clz(lastnz[g]) : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-#pragma unroll
-        for (int g = 0; g < GM; ++g) {
-          const long long n = __shfl_up_sync(FULL, F[g], o);
-          if (lane >= o) F[g] += n;
+      const long long pref = nthr > 0 ? (g.ch ? g.pref[qh * g.nch + qc] : a.prefix[bh * cm1 + g.c_lo + qc]) : 0;
+      int cnt = 0;
+      for (int t = 0; t < tmax; ++t) {
+        const bool ok = t < nthr;
+        long long x = 0;
+        if (ok) x = (hi.off >= 0 ? pool[hi.off + (j0 - hi.jlo) + t] : a.thresh[bh * a.S_max + j0 + t]) - pref;
+        const unsigned above = (__ballot_sync(FULL, ok && F > x) >> hb) & 0xffffu;
+        const int k = above ? __ffs(above) - 1 : lastnz;
+        if (ok && l16 == k) {
+          ++cnt;
+          if (a.sample_idx) a.sample_idx[bh * a.S_max + j0 + t] = (int)key;
         }
       }
-      int ntmax = 0;
+      if (g.tab) {
+        if (cnt > 0) atomicAdd(&g.table[((qh / G) * g.nkeys + (int)(key - g.key_lo)) * GM + qh % G], cnt);
+        continue;
+      }
+      // no table: gather the drawn keys' rows here, four at a time per half-warp
+      const unsigned drawn = (__ballot_sync(FULL, cnt > 0) >> hb) & 0xffffu;
+      const int nd = __popc(drawn), ndmax = max(nd, __shfl_xor_sync(FULL, nd, 16));
+      const int kvh = p.hg * W + qh / G;
+      const T* Vb = reinterpret_cast<const T*>(a.V) + (p.row0 * a.Hkv + kvh) * (int64_t)D + l16 * TL::EPL;
+      for (int d0 = 0; d0 < ndmax; d0 += 4) {
+        uint4 vv[4];
+        float cw[4];
 #pragma unroll
-      for (int g = 0; g < GM; ++g) ntmax = max(ntmax, nt[g]);
-      if (ntmax <= 8) {
-        // one ballot per threshold: the key is the first lane with F > x (the
-        // last nonzero key for x beyond the window's total)
-        for (int t = 0; t < ntmax; ++t) {
+        for (int u = 0; u < 4; ++u) {
+          const bool have = d0 + u < nd;
+          const int kl = have ? (int)__fns(drawn, 0, d0 + u + 1) : 0;
+          cw[u] = (float)__shfl_sync(FULL, cnt, hb + kl);
+          const int64_t kk = (int64_t)(g.c_lo + qc) * SUB + kl;
+          vv[u] = (have && l16 < TL::LPK) ? ld_stream(Vb + kk * a.Hkv * D) : make_uint4(0, 0, 0, 0);
+          if (!have) cw[u] = 0.f;
+        }
 #pragma unroll
-          for (int g = 0; g < GM; ++g) {
-            if (t < nt[g]) {   // warp-uniform
-              const long long x = __shfl_sync(FULL, th0[g], t) - pb[g];
-              const unsigned above = __ballot_sync(FULL, F[g] > x);
-              const int k = above ? __ffs(above) - 1 : lastnz[g];
-              if (lane == k) {
-                ++cnt[g];
-                if (a.sample_idx) a.sample_idx[(bh0 + wk * G + g) * a.S_max + js[g] + t] = (int)key;
-              }
+        for (int u = 0; u < 4; ++u) {
+          if (cw[u] != 0.f && l16 < TL::LPK) {
+            float vf[TL::EPL];
+            Elem<T>::widen(vv[u], vf);
+#pragma unroll
+            for (int e = 0; e < TL::EPL; ++e) atomicAdd(&obuf[qh * D + l16 * TL::EPL + e], cw[u] * vf[e]);
+          }
+        }
+      }
+    }
+    if (g.tab) {
+      __syncthreads();   // the count table is complete
+      // rows drawn by any head of their KV head, each read once for all of them
+      for (int e = tid; e < W * g.nkeys; e += SB_THREADS) {
+        bool any = false;
+#pragma unroll
+        for (int gg = 0; gg < GM; ++gg) any |= g.table[e * GM + gg] != 0;
+        if (any) g.rows[atomicAdd(&n_rows, 1)] = e;
+      }
+      __syncthreads();
+      const int nr = n_rows;
+      for (int r0 = (warp * 2 + h16) * 2; r0 < nr; r0 += SB_WARPS * 4) {   // two rows per half-warp and pass
+        uint4 vv[2];
+        int er[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int ri = r0 + u;
+          er[u] = ri < nr ? g.rows[ri] : -1;
+          vv[u] = make_uint4(0, 0, 0, 0);
+          if (er[u] >= 0 && l16 < TL::LPK) {
+            const int wk = er[u] / g.nkeys;
+            const int64_t key = g.key_lo + er[u] % g.nkeys;
+            vv[u] = ld_stream(reinterpret_cast<const T*>(a.V) + ((p.row0 + key) * a.Hkv + p.hg * W + wk) * (int64_t)D +
+                              l16 * TL::EPL);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          if (er[u] >= 0 && l16 < TL::LPK) {
+            const int wk = er[u] / g.nkeys;
+            float vf[TL::EPL];
+            Elem<T>::widen(vv[u], vf);
+            for (int gg = 0; gg < G; ++gg) {
+              const int c = g.table[er[u] * GM + gg];
+              if (c)
+#pragma unroll
+                for (int e = 0; e < TL::EPL; ++e)
+                  atomicAdd(&obuf[(wk * G + gg) * D + l16 * TL::EPL + e], (float)c * vf[e]);
             }
           }
         }
-      } else {
-#pragma unroll
-        for (int g = 0; g < GM; ++g) {
-          if (nt[g] > 0) {   // warp-uniform
-            const int h2 = wk * G + g;
-            const int64_t bh = bh0 + h2;
-            const HeadInfo hi = hinfo[h2];
-            const long long* th = hi.off >= 0 ? pool + hi.off + (js[g] - hi.jlo) : a.thresh + bh * a.S_max + js[g];
-            float sv = -INFINITY;
-            if (key < p.nk)
-              sv = st_smem ? s_st[h2 * cap_st + (int)((bh * a.nk_max + key_lo) & 3) + (int)(key - key_lo)]
-                           : a.stash[bh * a.nk_max + key];
-            cnt[g] = window_draws(sv, hi.mstar, th0[g], nt[g], pb[g], th,
-                                  a.sample_idx ? a.sample_idx + bh * a.S_max + js[g] : nullptr, (int)key, lane);
-          }
-        }
       }
-      bool mine = false;
-#pragma unroll
-      for (int g = 0; g < GM; ++g) mine |= cnt[g] > 0;
-      const unsigned drawn = __ballot_sync(FULL, mine);
-      if (nrows + __popc(drawn) > RCAP) flush();   // warp-uniform
-      if (mine) {
-        const int rr = nrows + __popc(drawn & ((1u << lane) - 1u));
-        rows[rr] = (int)key;
-#pragma unroll
-        for (int g = 0; g < GM; ++g) cnt_s[rr * GM + g] = cnt[g];
-      }
-      nrows += __popc(drawn);
-      __syncwarp();
     }
-    flush();
     __syncthreads();
     // this CTA's sums, times 1/S_b, into out (vectorised fp32 reductions;
     // the order of the additions across CTAs is not fixed)
@@ -761,6 +860,7 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     }
     __syncthreads();
   });
+  cp_async_wait_all();   // no copy outlives the CTA (a staged piece that was skipped)
 }
 
 // ---------------------------------------------------------------------------
@@ -769,10 +869,8 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
 template <typename T, int D, int GM>
 static cudaError_t launch_fused_g(const LaunchArgs& a, unsigned* bar_count, unsigned* bar_gen) {
   using Gm = StreamGeom<T, D>;
-  static_assert((size_t)GM * 8 * D * 4 + (size_t)SB_WARPS * RCAP * (GM + 1) * 4 + (size_t)GM * 8 * sizeof(HeadInfo) +
-                        (size_t)POOL_CAP * 8 + (size_t)64 * MAX_CTAS * 8 + 64 <=
-                    Gm::SMEM,
-                "phase B fixed regions and the aggregates fit the ring");
+  static_assert((size_t)GM * 8 * D * 4 + (size_t)GM * 8 * sizeof(HeadInfo) + (size_t)POOL_CAP * 8 + 4096 <= Gm::SMEM,
+                "phase B fixed regions fit the ring");
   const int W = unit_heads(a.Hkv);
   const int unit_rows = SB_UNIT_ROWS_X_W / W;
   const long long units = (long long)a.B * ((a.nk_max + unit_rows - 1) / unit_rows) * (a.Hkv / W);

@@ -48,6 +48,11 @@ struct LaunchArgs {
   float* agg_l;            // [B, H, MAX_CTAS] per-CTA sum of exp(s_n - agg_m)
   uint32_t* ukeys;         // [B, H, S_max] sorted 24-bit uniform keys (i.i.d.)
   unsigned long long* rcp_S;  // [B] ceil(2^64 / S_b)
+  long long* bnd_P;        // [B, H, MAX_CTAS] mass prefix of each CTA's key range
+  long long* bnd_T;        // [B, H, MAX_CTAS] mass of each CTA's key range
+  int32_t* bnd_jlo;        // [B, H, MAX_CTAS] first threshold of each CTA's range
+  int32_t* bnd_jhi;        // [B, H, MAX_CTAS] end of each CTA's threshold range
+  long long* head_Z;       // [B, H] total mass
   cudaStream_t stream;
 };
 
