@@ -311,6 +311,10 @@ __device__ __forceinline__ void flag_error(int* err, int bits) { atomicOr(err, b
 __device__ __forceinline__ void wait_for_predecessor() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// out[i..i+1] += v with one vectorised fp32 reduction (no return value).
+__device__ __forceinline__ void red_add_v2(float* out, float2 v) {
+  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(out), "f"(v.x), "f"(v.y) : "memory");
+}
 // out[i..i+3] += v with one vectorised fp32 reduction (no return value).
 __device__ __forceinline__ void red_add_v4(float* out, float4 v) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(out), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)

@@ -419,7 +419,7 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
   long long* pool = reinterpret_cast<long long*>(hinfo + GM * 8);                // [POOL_CAP]
   unsigned char* var0 = reinterpret_cast<unsigned char*>(pool + POOL_CAP);       // per-piece staging
   const size_t var_cap = Gm::SMEM - (size_t)(var0 - smem);
-  __shared__ int pool_used, n_items, n_rows;
+  __shared__ int pool_used, n_items;
   __shared__ float red_f[SB_WARPS];
   __shared__ long long red_ll[SB_WARPS];
   struct Stage {
@@ -427,7 +427,7 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     int64_t key_lo;
     float *mx, *sm, *st;
     long long* pref;
-    int *js, *items, *table, *rows;
+    int *js, *items, *table;
     bool ch, sto, tab;   // in shared memory: chunk statistics + tables + items / scores / count table
   };
   auto plan = [&](const Piece& p) {
@@ -458,7 +458,6 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     if (!g.sto) off = keep;
     keep = off;
     g.table = reinterpret_cast<int*>(take((size_t)W * g.nkeys * GM * 4));
-    g.rows = reinterpret_cast<int*>(take((size_t)W * g.nkeys * 4));
     g.tab = off <= var_cap;
     return g;
   };
@@ -483,6 +482,59 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     cp_async_commit();
   };
 
+  auto nonempty = [&](int i) {   // CTA i owns at least one unit
+    return n_units >= P || n_units * i / P < n_units * (i + 1) / P;
+  };
+  struct HeadGeom {
+    int b, h, S_b, i_first, i_last;
+    unsigned long long rcp;   // ceil(2^64 / S_b)
+    uint32_t ksys;            // systematic: the head's uniform key
+    bool ok;
+  };
+  auto geom = [&](long long bh) {   // the same in every lane of a warp
+    HeadGeom q;
+    q.b = (int)(bh / a.H);
+    q.h = (int)(bh % a.H);
+    q.ok = seq_error(a, q.b, q.S_b) == 0;
+    int64_t r0_, nk_;
+    const int units_b = UnitCursor::seq_units(a.kv_offsets, a.nk_max, unit_rows, q.b, r0_, nk_);
+    long long base = (long long)q.b * units_b;
+    if (a.kv_offsets) {
+      base = 0;
+      for (int b0 = 0; b0 < q.b; b0 += 32) {
+        int64_t r1, n1;
+        long long u = (b0 + lane < q.b) ? UnitCursor::seq_units(a.kv_offsets, a.nk_max, unit_rows, b0 + lane, r1, n1) : 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) u += __shfl_xor_sync(FULL, u, o);
+        base += u;
+      }
+    }
+    const long long U = base * n_hg + (long long)(q.h / GW) * units_b;   // unit (b, hg, kb = 0)
+    q.i_first = (int)(((U + 1) * P - 1) / n_units);
+    q.i_last = (int)(((U + units_b) * P - 1) / n_units);
+    q.ok = q.ok && units_b > 0;
+    q.rcp = (q.ok && q.S_b > 1) ? ~0ull / (unsigned)q.S_b + 1ull : 0ull;
+    q.ksys = a.variant == VAR_SYS ? philox4x32_10(make_uint4(0u, (uint32_t)q.h, (uint32_t)q.b, a.step), k0, k1).x >> 8
+                                  : 0u;
+    return q;
+  };
+  auto make_draws = [&](const HeadGeom& q, long long bh, long long Z) {
+    Draws dr;
+    dr.variant = a.variant;
+    dr.S = q.S_b;
+    dr.h = q.h;
+    dr.b = q.b;
+    dr.step = a.step;
+    dr.k0 = k0;
+    dr.k1 = k1;
+    dr.ksys = q.ksys;
+    dr.sorted = a.ukeys + bh * a.S_max;
+    dr.tc = a.variant == VAR_IID ? theta_ctx(Z, 1u, 0ull) : theta_ctx(Z, (unsigned)q.S_b, q.rcp);
+    return dr;
+  };
+  // boundary i of a head: prefix, mass and the first threshold of the range
+  // (counts of the i.i.d. sorted thresholds are taken in the CTA that owns the
+  // range); the range ends where the next one starts
   // first barrier; while waiting, this CTA stages its first piece's chunk
   // statistics and scores (its own data, already written)
   __syncthreads();
@@ -508,7 +560,23 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     stage(p0, plan(p0));
     prestaged = true;
   }
-  grid_wait(bar_gen, gen1, a.err);
+  // ... and the geometry of the heads it will own in the next step (metadata
+  // loads, budget reciprocal, systematic uniform), one warp per head
+  constexpr int PRE_MAX = SB_WARPS;
+  __shared__ HeadGeom pre_geom[PRE_MAX];
+  {
+    const long long bh = cta + (long long)warp * P;
+    if (bh < (long long)a.B * a.H) {
+      const HeadGeom q = geom(bh);
+      if (lane == 0) pre_geom[warp] = q;
+    }
+  }
+  grid_wait(bar_gen, gen1, a.err);   // its __syncthreads also publishes pre_geom
+  // the k-th head owned by this CTA
+  auto owned_geom = [&](long long bh) {
+    const long long k = (bh - cta) / P;
+    return k < PRE_MAX ? pre_geom[k] : geom(bh);
+  };
 
   // ======================= phase B0: per-head globals =======================
   // From the aggregates of the CTAs covering a head's (sequence, KV-head
@@ -516,69 +584,25 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
   // mass prefix P_i, mass T_i and threshold range [count(P_i), count(P_i + T_i)).
   // Heads covered by more than 32 CTAs take a whole CTA (one covering CTA per
   // thread); the others a warp (one per lane).
-  auto nonempty = [&](int i) {   // CTA i owns at least one unit
-    return n_units >= P || n_units * i / P < n_units * (i + 1) / P;
-  };
-  struct HeadGeom {
-    int b, h, S_b, i_first, i_last;
-    bool ok;
-  };
-  auto geom = [&](long long bh) {   // the same in every lane of a warp
-    HeadGeom q;
-    q.b = (int)(bh / a.H);
-    q.h = (int)(bh % a.H);
-    q.ok = seq_error(a, q.b, q.S_b) == 0;
-    int64_t r0_, nk_;
-    const int units_b = UnitCursor::seq_units(a.kv_offsets, a.nk_max, unit_rows, q.b, r0_, nk_);
-    long long base = (long long)q.b * units_b;
-    if (a.kv_offsets) {
-      base = 0;
-      for (int b0 = 0; b0 < q.b; b0 += 32) {
-        int64_t r1, n1;
-        long long u = (b0 + lane < q.b) ? UnitCursor::seq_units(a.kv_offsets, a.nk_max, unit_rows, b0 + lane, r1, n1) : 0;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) u += __shfl_xor_sync(FULL, u, o);
-        base += u;
-      }
-    }
-    const long long U = base * n_hg + (long long)(q.h / GW) * units_b;   // unit (b, hg, kb = 0)
-    q.i_first = (int)(((U + 1) * P - 1) / n_units);
-    q.i_last = (int)(((U + units_b) * P - 1) / n_units);
-    q.ok = q.ok && units_b > 0;
-    return q;
-  };
-  auto make_draws = [&](const HeadGeom& q, long long bh, long long Z) {
-    Draws dr;
-    dr.variant = a.variant;
-    dr.S = q.S_b;
-    dr.h = q.h;
-    dr.b = q.b;
-    dr.step = a.step;
-    dr.k0 = k0;
-    dr.k1 = k1;
-    dr.ksys = a.variant == VAR_SYS ? philox4x32_10(make_uint4(0u, (uint32_t)q.h, (uint32_t)q.b, a.step), k0, k1).x >> 8
-                                   : 0u;
-    dr.sorted = a.ukeys + bh * a.S_max;
-    dr.tc = a.variant == VAR_IID ? theta_ctx(Z, 1u, 0ull) : theta_ctx(Z, (unsigned)q.S_b, a.rcp_S[q.b]);
-    return dr;
-  };
   auto write_bnd = [&](const Draws& dr, long long bh, int i, long long Pi, long long Ti) {
     const int64_t o = bh * MAX_CTAS + i;
     a.bnd_P[o] = Pi;
     a.bnd_T[o] = Ti;
-    // counts of the i.i.d. sorted thresholds are taken in the CTA that owns the range
-    a.bnd_jlo[o] = a.variant == VAR_IID ? -1 : dr.count_below(Pi, 0, 32, lane, 0);
-    a.bnd_jhi[o] = a.variant == VAR_IID ? -1 : dr.count_below(Pi + Ti, 0, 32, lane, 0);
+    const int jlo = a.variant == VAR_IID ? -1 : dr.count_below(Pi, 0, 32, lane, 0);
+    a.bnd_jlo[o] = jlo;
+    return jlo;
   };
+  __shared__ int s_jlo[MAX_CTAS + 1];
   // (1) wide heads: one CTA each
   for (long long bh = cta; bh < (long long)a.B * a.H; bh += P) {
-    const HeadGeom q = geom(bh);
+    const HeadGeom q = owned_geom(bh);
     const int ncov = q.i_last - q.i_first + 1;
-    if (!q.ok || ncov <= 32) continue;   // uniform over the CTA
     const int i = q.i_first + tid;
-    const bool ok = tid < ncov && nonempty(i);
+    // loaded before the validity test so that these loads overlap the metadata loads
+    const bool ok = tid < ncov && i < MAX_CTAS && nonempty(i);
     const float mi = ok ? a.agg_m[bh * MAX_CTAS + i] : -INFINITY;
     const float li = ok ? a.agg_l[bh * MAX_CTAS + i] : 0.f;
+    if (!q.ok || ncov <= 32) continue;   // uniform over the CTA
     float m = warp_max(mi);
     if (lane == 0) red_f[warp] = m;
     __syncthreads();
@@ -596,28 +620,34 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
       Z += red_ll[w];
     }
     const Draws dr = make_draws(q, bh, Z);
-    if (tid < ncov) write_bnd(dr, bh, i, before + incl - Ti, Ti);
+    if (tid < ncov) s_jlo[tid] = write_bnd(dr, bh, i, before + incl - Ti, Ti);
     if (tid == 0) {
       a.head_max[bh] = m;
       a.head_Z[bh] = Z;
     }
     __syncthreads();
+    if (tid < ncov)
+      a.bnd_jhi[bh * MAX_CTAS + i] = a.variant == VAR_IID ? -1 : (tid + 1 < ncov ? s_jlo[tid + 1] : q.S_b);
+    __syncthreads();
   }
   // (2) narrow heads: one warp each
   for (long long bh = (long long)warp * P + cta; bh < (long long)a.B * a.H; bh += (long long)SB_WARPS * P) {
-    const HeadGeom q = geom(bh);
+    const HeadGeom q = owned_geom(bh);
     const int ncov = q.i_last - q.i_first + 1;
-    if (!q.ok || ncov > 32) continue;   // warp-uniform
     const int i = q.i_first + lane;
-    const bool ok = lane < ncov && nonempty(i);
+    const bool ok = lane < ncov && i < MAX_CTAS && nonempty(i);
     const float mi = ok ? a.agg_m[bh * MAX_CTAS + i] : -INFINITY;
     const float li = ok ? a.agg_l[bh * MAX_CTAS + i] : 0.f;
+    if (!q.ok || ncov > 32) continue;   // warp-uniform
     const float m = warp_max(mi);
     const long long Ti = ok ? fixed40(fast_exp(mi - m) * li) : 0;
     const long long incl = warp_inclusive_scan(Ti, lane);
     const long long Z = __shfl_sync(FULL, incl, 31);
     const Draws dr = make_draws(q, bh, Z);
-    if (lane < ncov) write_bnd(dr, bh, i, incl - Ti, Ti);
+    const int jlo = lane < ncov ? write_bnd(dr, bh, i, incl - Ti, Ti) : 0;
+    const int jnext = __shfl_down_sync(FULL, jlo, 1);
+    if (lane < ncov)
+      a.bnd_jhi[bh * MAX_CTAS + i] = a.variant == VAR_IID ? -1 : (lane + 1 < ncov ? jnext : q.S_b);
     if (lane == 0) {
       a.head_max[bh] = m;
       a.head_Z[bh] = Z;
@@ -636,13 +666,13 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     ++piece_no;
     if (bad) return;   // uniform over the CTA
     const int64_t bh0 = (int64_t)p.b * a.H + (int64_t)p.hg * GW;   // first head of the group
-    for (int i = tid; i < GW * D; i += SB_THREADS) obuf[i] = 0.f;
     if (g.tab)
       for (int i = tid; i < W * g.nkeys * GM; i += SB_THREADS) g.table[i] = 0;
+    else
+      for (int i = tid; i < GW * D; i += SB_THREADS) obuf[i] = 0.f;
     if (tid == 0) {
       pool_used = 0;
       n_items = 0;
-      n_rows = 0;
     }
     cp_async_wait_all();
     __syncthreads();
@@ -661,6 +691,9 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
       q.b = p.b;
       q.h = h;
       q.S_b = S_b;
+      q.rcp = a.rcp_S[p.b];
+      q.ksys = a.variant == VAR_SYS ? philox4x32_10(make_uint4(0u, (uint32_t)h, (uint32_t)p.b, a.step), k0, k1).x >> 8
+                                    : 0u;
       const Draws dr = make_draws(q, bh, Z);
       if (a.variant == VAR_IID) {
         int rounds = 1;
@@ -807,50 +840,122 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     }
     if (g.tab) {
       __syncthreads();   // the count table is complete
-      // rows drawn by any head of their KV head, each read once for all of them
-      for (int e = tid; e < W * g.nkeys; e += SB_THREADS) {
-        bool any = false;
+      // ---- gather by KV head: warp w takes KV head w % W and every
+      //      (16 / W)-th of its drawn rows; each drawn V row is read once for
+      //      all heads of its group, lane l owns output columns [4l, 4l + 4)
+      //      (D = 128) or [2l, 2l + 2) (D = 64) of every head, and the warp's
+      //      sums, times 1/S_b, go into out with vectorised fp32 reductions
+      //      (their order across warps and CTAs is not fixed).
+      const int wk = warp % W, part = warp / W, nparts = SB_WARPS / W;
+      constexpr int CPL = D / 32;                 // output columns per lane
+      float acc[GM][CPL];
 #pragma unroll
-        for (int gg = 0; gg < GM; ++gg) any |= g.table[e * GM + gg] != 0;
-        if (any) g.rows[atomicAdd(&n_rows, 1)] = e;
-      }
-      __syncthreads();
-      const int nr = n_rows;
-      for (int r0 = (warp * 2 + h16) * 2; r0 < nr; r0 += SB_WARPS * 4) {   // two rows per half-warp and pass
-        uint4 vv[2];
-        int er[2];
+      for (int gg = 0; gg < GM; ++gg)
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int ri = r0 + u;
-          er[u] = ri < nr ? g.rows[ri] : -1;
-          vv[u] = make_uint4(0, 0, 0, 0);
-          if (er[u] >= 0 && l16 < TL::LPK) {
-            const int wk = er[u] / g.nkeys;
-            const int64_t key = g.key_lo + er[u] % g.nkeys;
-            vv[u] = ld_stream(reinterpret_cast<const T*>(a.V) + ((p.row0 + key) * a.Hkv + p.hg * W + wk) * (int64_t)D +
-                              l16 * TL::EPL);
+        for (int c = 0; c < CPL; ++c) acc[gg][c] = 0.f;
+      const int* tab = g.table + (size_t)wk * g.nkeys * GM;
+      const T* Vk = reinterpret_cast<const T*>(a.V) + (p.row0 * a.Hkv + p.hg * W + wk) * (int64_t)D + lane * CPL;
+      // this warp's drawn rows (key within the piece, counts), then their
+      // loads all in flight together, eight at a time
+      bool any_rows = false;
+      int seen = 0;   // drawn rows of this KV head met so far (for the part split)
+      int nmine = 0;
+      int rk_l = -1;            // lane l holds the l-th row of this warp (32 at most per batch)
+      int rc_l[GM];
+#pragma unroll
+      for (int gg = 0; gg < GM; ++gg) rc_l[gg] = 0;
+      auto gather_batch = [&](int n) {   // rows held by lanes 0..n-1
+        for (int r0 = 0; r0 < n; r0 += 8) {
+          uint2 raw[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int kr = __shfl_sync(FULL, rk_l, (r0 + u) & 31);
+            raw[u] = make_uint2(0u, 0u);
+            if (r0 + u < n) {
+              const T* src = Vk + (g.key_lo + kr) * a.Hkv * D;
+              if constexpr (CPL == 4) raw[u] = *reinterpret_cast<const uint2*>(src);
+              else raw[u].x = *reinterpret_cast<const uint32_t*>(src);
+            }
           }
-        }
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          if (er[u] >= 0 && l16 < TL::LPK) {
-            const int wk = er[u] / g.nkeys;
-            float vf[TL::EPL];
-            Elem<T>::widen(vv[u], vf);
-            for (int gg = 0; gg < G; ++gg) {
-              const int c = g.table[er[u] * GM + gg];
-              if (c)
+          for (int u = 0; u < 8; ++u) {
+            if (r0 + u < n) {   // warp-uniform
+              float vf[4];
+              f2x pr[4];
+              Pairs<T>::get(make_uint4(raw[u].x, raw[u].y, 0u, 0u), pr);
+              const float2 p0 = unpack2(pr[0]), p1 = unpack2(pr[1]);
+              vf[0] = p0.x; vf[1] = p0.y; vf[2] = p1.x; vf[3] = p1.y;
 #pragma unroll
-                for (int e = 0; e < TL::EPL; ++e)
-                  atomicAdd(&obuf[(wk * G + gg) * D + l16 * TL::EPL + e], (float)c * vf[e]);
+              for (int gg = 0; gg < GM; ++gg) {
+                const float cw = (float)__shfl_sync(FULL, rc_l[gg], (r0 + u) & 31);
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) acc[gg][c] = fmaf(cw, vf[c], acc[gg][c]);
+              }
             }
           }
         }
+      };
+      for (int k0 = 0; k0 < g.nkeys; k0 += 32) {
+        const int kr = k0 + lane;
+        int cg[GM];
+        bool drawn_here = false;
+#pragma unroll
+        for (int gg = 0; gg < GM; ++gg) {
+          cg[gg] = (kr < g.nkeys && gg < G) ? tab[kr * GM + gg] : 0;
+          drawn_here |= cg[gg] != 0;
+        }
+        const unsigned m = __ballot_sync(FULL, drawn_here);
+        // rows of this part: every nparts-th drawn row of the KV head
+        unsigned mine = 0u;
+        const int nm = __popc(m);
+        for (int t = 0, mm = (int)m; t < nm; ++t, mm &= mm - 1)
+          if (((seen + t) % nparts) == part) mine |= 1u << (__ffs(mm) - 1);
+        seen += nm;
+        // append to the lane-held list; gather when it would overflow
+        const int add = __popc(mine);
+        if (nmine + add > 32) {
+          gather_batch(nmine);
+          any_rows = any_rows || nmine > 0;
+          nmine = 0;
+        }
+        // lane nmine + t receives the t-th row of this block
+        for (int t = 0; t < add; ++t) {
+          const int src_lane = (int)__fns(mine, 0, t + 1);
+          const int krow = __shfl_sync(FULL, kr, src_lane);
+          int cgs[GM];
+#pragma unroll
+          for (int gg = 0; gg < GM; ++gg) cgs[gg] = __shfl_sync(FULL, cg[gg], src_lane);
+          if (lane == nmine + t) {
+            rk_l = krow;
+#pragma unroll
+            for (int gg = 0; gg < GM; ++gg) rc_l[gg] = cgs[gg];
+          }
+        }
+        nmine += add;
       }
+      if (nmine > 0) {
+        gather_batch(nmine);
+        any_rows = true;
+      }
+      if (any_rows) {   // warp-uniform
+        const float inv_S = 1.0f / (float)S_b;
+        float* outp = a.out + (bh0 + (int64_t)wk * G) * D + lane * CPL;
+#pragma unroll
+        for (int gg = 0; gg < GM; ++gg) {
+          if (gg < G) {
+            if constexpr (CPL == 4)
+              red_add_v4(outp + (int64_t)gg * D,
+                         make_float4(acc[gg][0] * inv_S, acc[gg][1] * inv_S, acc[gg][2] * inv_S, acc[gg][3] * inv_S));
+            else
+              red_add_v2(outp + (int64_t)gg * D, make_float2(acc[gg][0] * inv_S, acc[gg][1] * inv_S));
+          }
+        }
+      }
+      __syncthreads();
+      return;   // uniform over the CTA (g.tab)
     }
     __syncthreads();
-    // this CTA's sums, times 1/S_b, into out (vectorised fp32 reductions;
-    // the order of the additions across CTAs is not fixed)
+    // no table (a piece too large for it): this CTA's sums, times 1/S_b, into out
     const float inv_S = 1.0f / (float)S_b;
     float* outp = a.out + bh0 * D;
     for (int i4 = tid; i4 < GW * D / 4; i4 += SB_THREADS) {
