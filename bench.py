@@ -76,6 +76,18 @@ def dist_env():
     return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest of every rank's value (the whole job ends when its slowest
+    replica does); the value itself on one rank.  Any process-group backend."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ---------------------------------------------------------------------------
 # peaks, clocks, traffic record
 # ---------------------------------------------------------------------------
@@ -378,11 +390,7 @@ def run_ours(args):
     ms = timed_loop(lambda i: decs[i % R](step=0), args.steps, args.warmup)
     clocks = sampler.stop()
 
-    total_ms = sum(ms)
-    if world > 1:
-        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(sum(ms), dev)
     mean_ms = total_ms / args.steps
     med_ms = statistics.median(ms)
 
