@@ -332,6 +332,7 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     }
   }
   __syncthreads();
+  __shared__ float run_m[SB_WARPS * 8], run_l[SB_WARPS * 8];   // per-warp running statistics
   {
     StreamArgs sa;
     sa.q = a.q;
@@ -347,7 +348,7 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     sa.sub_max = a.tile_max;
     sa.sub_sum = a.tile_sum;
     sa.subs_max = a.chunks_max;
-    stream_scores<T, D>(sa, smem_addr(smem), start);
+    stream_scores<T, D>(sa, smem_addr(smem), start, run_m, run_l);
   }
   __syncthreads();   // statistics of the whole range written; the ring is free
 
@@ -390,7 +391,29 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     }
   }
 
-  // aggregates (max, sum exp(s - max)) of every head over this CTA's keys
+  // aggregates (max, sum exp(s - max)) of every head over this CTA's keys:
+  // from the warps' running statistics when the range is one (sequence,
+  // KV-head group), else from the range's chunk statistics
+  bool one_piece = false;
+  if (start[3] > 0) {
+    int64_t r0_, nk_;
+    const int ub = UnitCursor::seq_units(a.kv_offsets, a.nk_max, unit_rows, start[0], r0_, nk_);
+    one_piece = start[2] + start[3] <= ub;
+  }
+  if (one_piece) {
+    if (tid < GW) {
+      const int wl = tid / G, g = tid % G;   // KV head within the group, head within its query group
+      float m = -INFINITY;
+      for (int w = 0; w < SB_WARPS; ++w)
+        if (((w >> 1) % W) == wl) m = fmaxf(m, run_m[w * 8 + g]);
+      float l = 0.f;
+      for (int w = 0; w < SB_WARPS; ++w)
+        if (((w >> 1) % W) == wl && run_m[w * 8 + g] > -INFINITY) l += run_l[w * 8 + g] * expf(run_m[w * 8 + g] - m);
+      const int64_t bh = (int64_t)start[0] * a.H + (int64_t)start[1] * GW + tid;
+      a.agg_m[bh * MAX_CTAS + cta] = m;
+      a.agg_l[bh * MAX_CTAS + cta] = l;
+    }
+  } else
   for_each_piece(a, n_hg, unit_rows, start, range[1], [&](const Piece& p) {
     if (!warp_on) return;
     const int c_lo = p.kb0 * C_of_unit;
@@ -540,6 +563,8 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
   __syncthreads();
   const unsigned gen1 = grid_arrive(bar_count, bar_gen);
   bool prestaged = false;
+  __shared__ int pre_S0;
+  __shared__ bool pre_bad0;
   if (start[3] > 0) {
     UnitCursor c0;
     c0.kv_offsets = a.kv_offsets;
@@ -557,8 +582,12 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     p0.kb0 = c0.kb;
     p0.nkb = min(start[3], c0.units_b - c0.kb);
     p0.nk = c0.nk;
-    stage(p0, plan(p0));
+    const Stage g0 = plan(p0);
+    stage(p0, g0);
+    if (g0.tab)
+      for (int i = tid; i < W * g0.nkeys * GM; i += SB_THREADS) g0.table[i] = 0;
     prestaged = true;
+    if (tid == 0) pre_bad0 = seq_error(a, p0.b, pre_S0) != 0;
   }
   // ... and the geometry of the heads it will own in the next step (metadata
   // loads, budget reciprocal, systematic uniform), one warp per head
@@ -660,16 +689,24 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
   int piece_no = 0;
   for_each_piece(a, n_hg, unit_rows, start, range[1], [&](const Piece& p) {
     int S_b;
-    const bool bad = seq_error(a, p.b, S_b) != 0;
+    bool bad;
+    if (piece_no == 0 && prestaged) {   // checked while waiting at the first barrier
+      bad = pre_bad0;
+      S_b = pre_S0;
+    } else {
+      bad = seq_error(a, p.b, S_b) != 0;
+    }
     const Stage g = plan(p);
     if (!(piece_no == 0 && prestaged) && !bad) stage(p, g);
     ++piece_no;
     if (bad) return;   // uniform over the CTA
     const int64_t bh0 = (int64_t)p.b * a.H + (int64_t)p.hg * GW;   // first head of the group
-    if (g.tab)
-      for (int i = tid; i < W * g.nkeys * GM; i += SB_THREADS) g.table[i] = 0;
-    else
+    if (g.tab) {
+      if (!(piece_no == 1 && prestaged))   // the first piece's table was cleared at the first barrier
+        for (int i = tid; i < W * g.nkeys * GM; i += SB_THREADS) g.table[i] = 0;
+    } else {
       for (int i = tid; i < GW * D; i += SB_THREADS) obuf[i] = 0.f;
+    }
     if (tid == 0) {
       pool_used = 0;
       n_items = 0;
@@ -807,7 +844,14 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
         }
       }
       if (g.tab) {
-        if (cnt > 0) atomicAdd(&g.table[((qh / G) * g.nkeys + (int)(key - g.key_lo)) * GM + qh % G], cnt);
+        if (cnt > 0) {
+          atomicAdd(&g.table[((qh / G) * g.nkeys + (int)(key - g.key_lo)) * GM + qh % G], cnt);
+          // the gather reads this row after the table is complete: start it towards L2 now
+          const T* vrow = reinterpret_cast<const T*>(a.V) + ((p.row0 + key) * a.Hkv + p.hg * W + qh / G) * (int64_t)D;
+#pragma unroll
+          for (int ln = 0; ln < (D * 2 + 127) / 128; ++ln)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(vrow + ln * 64));
+        }
         continue;
       }
       // no table: gather the drawn keys' rows here, four at a time per half-warp
@@ -858,7 +902,6 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
       // this warp's drawn rows (key within the piece, counts), then their
       // loads all in flight together, eight at a time
       bool any_rows = false;
-      int seen = 0;   // drawn rows of this KV head met so far (for the part split)
       int nmine = 0;
       int rk_l = -1;            // lane l holds the l-th row of this warp (32 at most per batch)
       int rc_l[GM];
@@ -904,13 +947,8 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
           cg[gg] = (kr < g.nkeys && gg < G) ? tab[kr * GM + gg] : 0;
           drawn_here |= cg[gg] != 0;
         }
-        const unsigned m = __ballot_sync(FULL, drawn_here);
-        // rows of this part: every nparts-th drawn row of the KV head
-        unsigned mine = 0u;
-        const int nm = __popc(m);
-        for (int t = 0, mm = (int)m; t < nm; ++t, mm &= mm - 1)
-          if (((seen + t) % nparts) == part) mine |= 1u << (__ffs(mm) - 1);
-        seen += nm;
+        // rows of this part: the drawn rows of every nparts-th 32-key block
+        const unsigned mine = ((k0 / 32) % nparts == part) ? __ballot_sync(FULL, drawn_here) : 0u;
         // append to the lane-held list; gather when it would overflow
         const int add = __popc(mine);
         if (nmine + add > 32) {

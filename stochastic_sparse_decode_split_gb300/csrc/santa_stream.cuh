@@ -187,8 +187,14 @@ struct StreamArgs {
 // The streaming loop of one CTA over its unit range.  `ring` is the dynamic
 // shared memory (SMEM bytes, 16-byte aligned), `start` the range start
 // broadcast by unit_range_start.  Called by all SB_THREADS threads.
+//
+// run_m / run_l (shared memory, [16 warps][8 heads], may be NULL): each warp's
+// running (max, sum exp(s - max)) over every key it scored, per head of its
+// KV head's query group; meaningful when the range is one (sequence, KV-head
+// group), which the caller checks.
 template <typename T, int D>
-__device__ __forceinline__ void stream_scores(const StreamArgs& a, uint32_t ring, const int* start) {
+__device__ __forceinline__ void stream_scores(const StreamArgs& a, uint32_t ring, const int* start,
+                                              float* run_m = nullptr, float* run_l = nullptr) {
   using Gm = StreamGeom<T, D>;
   constexpr int NS = Gm::NS;
   constexpr int CPL = 16 * Gm::NCH / 32;      // 16-byte copies per lane per unit
@@ -237,6 +243,7 @@ __device__ __forceinline__ void stream_scores(const StreamArgs& a, uint32_t ring
   }
 
   const int g8 = lane >> 2, t4 = lane & 3;
+  float rm[2] = {-INFINITY, -INFINITY}, rl[2] = {0.f, 0.f};   // running statistics, heads 2*t4 + hh
   const T* q = static_cast<const T*>(a.q);
   uint32_t bq[D / 16][2];
   int bq_b = -1, bq_kvh = -1;
@@ -300,11 +307,20 @@ __device__ __forceinline__ void stream_scores(const StreamArgs& a, uint32_t ring
           a.sub_max[(bh0 + head) * a.subs_max + sc] = m;
           a.sub_sum[(bh0 + head) * a.subs_max + sc] = l;
         }
+        const float nm = fmaxf(rm[hh], m);
+        rl[hh] = rl[hh] * fast_exp(rm[hh] - nm) + l * fast_exp(m - nm);
+        rm[hh] = nm;
       }
     }
     cur.advance();
   }
   cp_async_wait<0>();
+  if (run_m && (lane & ~3) == 0) {   // lanes 0..3: this warp's running statistics of heads 2*lane, 2*lane + 1
+    run_m[warp * 8 + 2 * lane] = rm[0];
+    run_m[warp * 8 + 2 * lane + 1] = rm[1];
+    run_l[warp * 8 + 2 * lane] = rl[0];
+    run_l[warp * 8 + 2 * lane + 1] = rl[1];
+  }
 }
 
 }  // namespace santa
