@@ -55,6 +55,9 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample length")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--l2", choices=["auto", "replicas", "flush"], default="auto",
+                    help="inputs larger than L2 (rotating K/V copies) or an L2 flush between steps; "
+                         "auto: copies when the cache is at least 128 MiB")
     return ap.parse_args()
 
 
@@ -336,7 +339,7 @@ def run_ours(args):
     # flush instead: write 512 MiB, then read 512 MiB so that no dirty line of
     # the flush is written back inside the timed step.
     kv_bytes = t["K"].numel() * t["K"].element_size() * 2
-    if kv_bytes * 4 >= FLUSH_BYTES:
+    if args.l2 == "replicas" or (args.l2 == "auto" and kv_bytes * 4 >= FLUSH_BYTES):
         R = max(2, -(-FLUSH_BYTES // kv_bytes))
         reps = [(t["K"], t["V"])] + [(t["K"].clone(), t["V"].clone()) for _ in range(R - 1)]
         l2_note = f"inputs larger than L2: {R} replicas of the K/V cache used in turn ({R * kv_bytes >> 20} MiB)"

@@ -276,6 +276,45 @@ __device__ __forceinline__ int seq_error(const LaunchArgs& a, int b, int& S_b) {
   return err;
 }
 
+// Geometry of head bh (global index b * H + h) for the owner step: its
+// sequence's validity and budget, the covering CTAs [i_first, i_last] of its
+// (sequence, KV-head group), the budget reciprocal and the systematic uniform.
+// Warp-uniform (the ragged unit count is a warp reduction).
+struct HeadGeom {
+  int b, h, S_b, i_first, i_last;
+  unsigned long long rcp;   // ceil(2^64 / S_b)
+  uint32_t ksys;            // systematic: the head's uniform key
+  bool ok;
+};
+__device__ __forceinline__ HeadGeom head_geom(const LaunchArgs& a, long long bh, int unit_rows, int n_hg, int GW, int P,
+                                           long long n_units, uint32_t k0, uint32_t k1) {
+  const int lane = threadIdx.x % 32;
+  HeadGeom q;
+  q.b = (int)(bh / a.H);
+  q.h = (int)(bh % a.H);
+  q.ok = seq_error(a, q.b, q.S_b) == 0;
+  int64_t r0_, nk_;
+  const int units_b = UnitCursor::seq_units(a.kv_offsets, a.nk_max, unit_rows, q.b, r0_, nk_);
+  long long base = (long long)q.b * units_b;
+  if (a.kv_offsets) {
+    base = 0;
+    for (int b0 = 0; b0 < q.b; b0 += 32) {
+      int64_t r1, n1;
+      long long u = (b0 + lane < q.b) ? UnitCursor::seq_units(a.kv_offsets, a.nk_max, unit_rows, b0 + lane, r1, n1) : 0;
+      for (int o = 16; o > 0; o >>= 1) u += __shfl_xor_sync(FULL, u, o);
+      base += u;
+    }
+  }
+  const long long U = base * n_hg + (long long)(q.h / GW) * units_b;   // unit (b, hg, kb = 0)
+  q.i_first = (int)(((U + 1) * P - 1) / n_units);
+  q.i_last = (int)(((U + units_b) * P - 1) / n_units);
+  q.ok = q.ok && units_b > 0;
+  q.rcp = (q.ok && q.S_b > 1) ? ~0ull / (unsigned)q.S_b + 1ull : 0ull;
+  q.ksys = a.variant == VAR_SYS ? philox4x32_10(make_uint4(0u, (uint32_t)q.h, (uint32_t)q.b, a.step), k0, k1).x >> 8
+                                : 0u;
+  return q;
+}
+
 // Per-head state of phase B (shared memory).
 struct HeadInfo {
   long long pown;   // mass prefix of this CTA's key range
@@ -298,7 +337,6 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
   const int GW = G * W;                       // query heads of one KV-head group
   const int lph = GW > 32 ? 8 : (GW > 16 ? 16 : 32);   // lanes per head in the per-head steps
   const int P = gridDim.x, cta = blockIdx.x;
-  const int cm1 = a.chunks_max + 1;
   const int C_of_unit = unit_rows / SUB;      // statistics chunks per unit
   const uint32_t k0 = (uint32_t)a.seed, k1 = (uint32_t)(a.seed >> 32);
   // head group of this thread in the per-head steps (groups fill whole warps)
@@ -437,29 +475,38 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
   // shared-memory plan of phase B (inside the ring, free by now)
   // ---------------------------------------------------------------------------
   const long long n_units = range[0];
-  float* obuf = reinterpret_cast<float*>(smem);                                   // [GW][D] this CTA's sums
-  HeadInfo* hinfo = reinterpret_cast<HeadInfo*>(obuf + GM * 8 * D);              // [GW]
+  HeadInfo* hinfo = reinterpret_cast<HeadInfo*>(smem);                           // [GW]
   long long* pool = reinterpret_cast<long long*>(hinfo + GM * 8);                // [POOL_CAP]
-  unsigned char* var0 = reinterpret_cast<unsigned char*>(pool + POOL_CAP);       // per-piece staging
+  unsigned char* var0 = reinterpret_cast<unsigned char*>(pool + POOL_CAP);       // per-segment staging
   const size_t var_cap = Gm::SMEM - (size_t)(var0 - smem);
   __shared__ int pool_used, n_items;
   __shared__ float red_f[SB_WARPS];
   __shared__ long long red_ll[SB_WARPS];
-  struct Stage {
-    int c_lo, c_hi, nch, nkeys, cap_ch, cap_st;
+  // A piece's key range is processed in segments of SEG statistics chunks, so
+  // that a segment's chunk statistics, scores, chunk tables, item list and
+  // (KV head, key) count table all fit in shared memory.
+  const int SEG = [&] {
+    const size_t per_chunk = (size_t)GW * (8 + 16 + 4 * SUB) + (size_t)W * SUB * GM * 4;
+    const size_t fixed = (size_t)GW * (2 * 7 * 4 + 7 * 4) + 8 * 16;   // row caps and alignment of 7 buffers
+    const int n = (int)((var_cap - fixed) / per_chunk);
+    return max(2, n & ~1);
+  }();
+  struct Seg {
+    int c_lo, nch, nkeys, cap_ch, cap_st;   // first statistics chunk (in the sequence), chunks, keys
     int64_t key_lo;
     float *mx, *sm, *st;
     long long* pref;
     int *js, *items, *table;
-    bool ch, sto, tab;   // in shared memory: chunk statistics + tables + items / scores / count table
   };
-  auto plan = [&](const Piece& p) {
-    Stage g;
-    g.c_lo = p.kb0 * C_of_unit;
-    g.c_hi = (int)min((int64_t)(p.kb0 + p.nkb) * C_of_unit, (p.nk + SUB - 1) / SUB);
-    g.nch = g.c_hi - g.c_lo;
+  // segment k of piece p: chunks [c_lo + k SEG, ...) of the piece's range
+  auto seg_of = [&](const Piece& p, int k) {
+    Seg g;
+    const int pc_lo = p.kb0 * C_of_unit;
+    const int pc_hi = (int)min((int64_t)(p.kb0 + p.nkb) * C_of_unit, (p.nk + SUB - 1) / SUB);
+    g.c_lo = pc_lo + k * SEG;
+    g.nch = max(0, min(SEG, pc_hi - g.c_lo));
     g.key_lo = (int64_t)g.c_lo * SUB;
-    g.nkeys = (int)(min((int64_t)g.c_hi * SUB, p.nk) - g.key_lo);
+    g.nkeys = (int)max((int64_t)0, min((int64_t)(g.c_lo + g.nch) * SUB, p.nk) - g.key_lo);
     g.cap_ch = (g.nch + 7) & ~3;   // floats per staged row (16-byte pieces from the boundary below)
     g.cap_st = (g.nkeys + 7) & ~3;
     size_t off = 0;
@@ -473,16 +520,14 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     g.pref = reinterpret_cast<long long*>(take((size_t)GW * g.nch * 8));
     g.js = reinterpret_cast<int*>(take((size_t)GW * g.nch * 4));
     g.items = reinterpret_cast<int*>(take((size_t)GW * g.nch * 4));
-    g.ch = off <= var_cap;
-    if (!g.ch) off = 0;
-    size_t keep = off;
     g.st = reinterpret_cast<float*>(take((size_t)GW * g.cap_st * 4));
-    g.sto = off <= var_cap;
-    if (!g.sto) off = keep;
-    keep = off;
     g.table = reinterpret_cast<int*>(take((size_t)W * g.nkeys * GM * 4));
-    g.tab = off <= var_cap;
     return g;
+  };
+  auto seg_count = [&](const Piece& p) {
+    const int pc_lo = p.kb0 * C_of_unit;
+    const int pc_hi = (int)min((int64_t)(p.kb0 + p.nkb) * C_of_unit, (p.nk + SUB - 1) / SUB);
+    return (pc_hi - pc_lo + SEG - 1) / SEG;
   };
   // rows are copied in 16-byte pieces from the 16-byte boundary at or below
   // their first element (reading up to 12 bytes either side of a row stays
@@ -492,54 +537,24 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     const int n16 = (int)((g0 + len - a0 + 3) >> 2);
     for (int j = lane; j < n16; j += 32) cp_async16(smem_addr(s_row + 4 * j), base + a0 + 4 * j);
   };
-  auto stage = [&](const Piece& p, const Stage& g) {
+  // copies of a segment's statistics and scores (one commit group), count table cleared
+  auto stage = [&](const Piece& p, const Seg& g) {
     const int64_t bh0 = (int64_t)p.b * a.H + (int64_t)p.hg * GW;
     for (int h = warp; h < GW; h += SB_WARPS) {
       const int64_t bh = bh0 + h;
-      if (g.ch) {
-        stage_row(g.mx + h * g.cap_ch, a.tile_max, bh * a.chunks_max + g.c_lo, g.nch);
-        stage_row(g.sm + h * g.cap_ch, a.tile_sum, bh * a.chunks_max + g.c_lo, g.nch);
-      }
-      if (g.sto) stage_row(g.st + h * g.cap_st, a.stash, bh * a.nk_max + g.key_lo, g.nkeys);
+      stage_row(g.mx + h * g.cap_ch, a.tile_max, bh * a.chunks_max + g.c_lo, g.nch);
+      stage_row(g.sm + h * g.cap_ch, a.tile_sum, bh * a.chunks_max + g.c_lo, g.nch);
+      stage_row(g.st + h * g.cap_st, a.stash, bh * a.nk_max + g.key_lo, g.nkeys);
     }
     cp_async_commit();
+    for (int i = tid; i < W * g.nkeys * GM; i += SB_THREADS) g.table[i] = 0;
   };
 
   auto nonempty = [&](int i) {   // CTA i owns at least one unit
     return n_units >= P || n_units * i / P < n_units * (i + 1) / P;
   };
-  struct HeadGeom {
-    int b, h, S_b, i_first, i_last;
-    unsigned long long rcp;   // ceil(2^64 / S_b)
-    uint32_t ksys;            // systematic: the head's uniform key
-    bool ok;
-  };
   auto geom = [&](long long bh) {   // the same in every lane of a warp
-    HeadGeom q;
-    q.b = (int)(bh / a.H);
-    q.h = (int)(bh % a.H);
-    q.ok = seq_error(a, q.b, q.S_b) == 0;
-    int64_t r0_, nk_;
-    const int units_b = UnitCursor::seq_units(a.kv_offsets, a.nk_max, unit_rows, q.b, r0_, nk_);
-    long long base = (long long)q.b * units_b;
-    if (a.kv_offsets) {
-      base = 0;
-      for (int b0 = 0; b0 < q.b; b0 += 32) {
-        int64_t r1, n1;
-        long long u = (b0 + lane < q.b) ? UnitCursor::seq_units(a.kv_offsets, a.nk_max, unit_rows, b0 + lane, r1, n1) : 0;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) u += __shfl_xor_sync(FULL, u, o);
-        base += u;
-      }
-    }
-    const long long U = base * n_hg + (long long)(q.h / GW) * units_b;   // unit (b, hg, kb = 0)
-    q.i_first = (int)(((U + 1) * P - 1) / n_units);
-    q.i_last = (int)(((U + units_b) * P - 1) / n_units);
-    q.ok = q.ok && units_b > 0;
-    q.rcp = (q.ok && q.S_b > 1) ? ~0ull / (unsigned)q.S_b + 1ull : 0ull;
-    q.ksys = a.variant == VAR_SYS ? philox4x32_10(make_uint4(0u, (uint32_t)q.h, (uint32_t)q.b, a.step), k0, k1).x >> 8
-                                  : 0u;
-    return q;
+    return head_geom(a, bh, unit_rows, n_hg, GW, P, n_units, k0, k1);
   };
   auto make_draws = [&](const HeadGeom& q, long long bh, long long Z) {
     Draws dr;
@@ -582,10 +597,7 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     p0.kb0 = c0.kb;
     p0.nkb = min(start[3], c0.units_b - c0.kb);
     p0.nk = c0.nk;
-    const Stage g0 = plan(p0);
-    stage(p0, g0);
-    if (g0.tab)
-      for (int i = tid; i < W * g0.nkeys * GM; i += SB_THREADS) g0.table[i] = 0;
+    stage(p0, seg_of(p0, 0));
     prestaged = true;
     if (tid == 0) pre_bad0 = seq_error(a, p0.b, pre_S0) != 0;
   }
@@ -686,6 +698,8 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
   grid_barrier(bar_count, bar_gen, a.err);
 
   // ======================= phase B1: this CTA's draws =======================
+  __shared__ long long carry_s[GM * 8];   // per head: mass prefix at the current segment's start
+  __shared__ int jend_s[GM * 8];          // per head: end of the current segment's thresholds
   int piece_no = 0;
   for_each_piece(a, n_hg, unit_rows, start, range[1], [&](const Piece& p) {
     int S_b;
@@ -696,27 +710,15 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     } else {
       bad = seq_error(a, p.b, S_b) != 0;
     }
-    const Stage g = plan(p);
-    if (!(piece_no == 0 && prestaged) && !bad) stage(p, g);
+    const bool first = piece_no == 0 && prestaged;
     ++piece_no;
     if (bad) return;   // uniform over the CTA
     const int64_t bh0 = (int64_t)p.b * a.H + (int64_t)p.hg * GW;   // first head of the group
-    if (g.tab) {
-      if (!(piece_no == 1 && prestaged))   // the first piece's table was cleared at the first barrier
-        for (int i = tid; i < W * g.nkeys * GM; i += SB_THREADS) g.table[i] = 0;
-    } else {
-      for (int i = tid; i < GW * D; i += SB_THREADS) obuf[i] = 0.f;
-    }
-    if (tid == 0) {
-      pool_used = 0;
-      n_items = 0;
-    }
-    cp_async_wait_all();
+    if (tid == 0) pool_used = 0;
     __syncthreads();
 
-    // ---- per head (groups of lph lanes, all heads at once): interval,
-    //      thresholds, the prefix / first threshold of each chunk, and the
-    //      list of chunks that hold thresholds
+    // ---- per head (groups of lph lanes, all heads at once): this CTA's
+    //      interval and its thresholds
     if (warp_on) {
       const int h = p.hg * GW + hl;
       const int64_t bh = bh0 + hl;
@@ -754,254 +756,225 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
         hinfo[hl].jhi = jhi;
         hinfo[hl].off = toff;
         hinfo[hl].mstar = mstar;
+        carry_s[hl] = P_own;
       }
-      __syncwarp();
-      const int oc = (int)((bh * a.chunks_max + g.c_lo) & 3);
-      const float* mx = g.ch ? g.mx + hl * g.cap_ch + oc : a.tile_max + bh * a.chunks_max + g.c_lo;
-      const float* sm = g.ch ? g.sm + hl * g.cap_ch + oc : a.tile_sum + bh * a.chunks_max + g.c_lo;
-      long long* pr = g.ch ? g.pref + hl * g.nch : a.prefix + bh * cm1 + g.c_lo;
-      int* jsr = g.ch ? g.js + hl * g.nch : a.jstart + bh * cm1 + g.c_lo;
-      long long run = P_own;
-      for (int c0 = 0; c0 < g.nch; c0 += lph) {
-        const int c = c0 + r;
-        const long long Wc = c < g.nch ? fixed40(fast_exp(mx[c] - mstar) * sm[c]) : 0;
-        const long long ci = grp_scan(Wc, r, lph);
-        const long long pref = run + ci - Wc;
-        if (c < g.nch && hv) {
-          int lo = 0, hi = nt;   // first threshold >= pref among [jlo, jhi)
-          while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (thp[mid] < pref) lo = mid + 1;
-            else hi = mid;
-          }
-          pr[c] = pref;
-          jsr[c] = jlo + lo;
-        }
-        run += __shfl_sync(FULL, ci, lph - 1, lph);
-      }
-      __syncwarp();
-      if (g.ch && hv)
-        for (int c = r; c < g.nch; c += lph) {
-          const int je = c + 1 < g.nch ? jsr[c + 1] : jhi;
-          if (je > jsr[c]) g.items[atomicAdd(&n_items, 1)] = hl * 65536 + c;
-        }
     }
-    __syncthreads();   // intervals, chunk tables, thresholds and items visible
+    const int nseg = seg_count(p);
+    for (int sg_i = 0; sg_i < nseg; ++sg_i) {
+      const Seg g = seg_of(p, sg_i);
+      if (!(first && sg_i == 0)) stage(p, g);   // the first piece's first segment was staged at the first barrier
+      if (tid == 0) n_items = 0;
+      cp_async_wait_all();
+      __syncthreads();   // staged data, cleared table, thresholds and head state visible
 
-    // ---- per (head, 16-key chunk) holding thresholds, one half-warp each:
-    //      exact key-mass prefix over the chunk, one ballot per threshold
-    //      (the key is the first with F > x; a threshold at or beyond the
-    //      chunk's key total goes to its last nonzero key).  Counts go into
-    //      the (KV head, key) table (the union of the group's draws), or,
-    //      when the table does not fit, straight into a gather.
-    const int h16 = lane >> 4, l16 = lane & 15, hb = h16 * 16;
-    const int nwork = g.ch ? n_items : GW * g.nch;
-    for (int q0 = warp * 2; q0 < nwork; q0 += SB_WARPS * 2) {
-      const int q = q0 + h16;
-      const bool qv = q < nwork;
-      int qh = 0, qc = 0;
-      if (qv) {
-        if (g.ch) {
-          qh = g.items[q] >> 16;
-          qc = g.items[q] & 0xffff;
-        } else {
-          qh = q / g.nch;
-          qc = q % g.nch;
+      // ---- per head: the segment's chunk prefixes (from the running carry),
+      //      first threshold of each chunk, and the chunks that hold thresholds
+      if (warp_on) {
+        const int64_t bh = bh0 + hl;
+        const HeadInfo hi = hinfo[hl];
+        const int nt = hi.jhi - hi.jlo;
+        const long long* thp = hi.off >= 0 ? pool + hi.off : a.thresh + bh * a.S_max + hi.jlo;
+        const int oc = (int)((bh * a.chunks_max + g.c_lo) & 3);
+        const float* mx = g.mx + hl * g.cap_ch + oc;
+        const float* sm = g.sm + hl * g.cap_ch + oc;
+        long long* pr = g.pref + hl * g.nch;
+        int* jsr = g.js + hl * g.nch;
+        auto first_at_or_above = [&](long long v) {   // index of the first threshold >= v among [jlo, jhi)
+          int lo = 0, hi2 = nt;
+          while (lo < hi2) {
+            const int mid = (lo + hi2) >> 1;
+            if (thp[mid] < v) lo = mid + 1;
+            else hi2 = mid;
+          }
+          return hi.jlo + lo;
+        };
+        long long run = carry_s[hl];
+        for (int c0 = 0; c0 < g.nch; c0 += lph) {
+          const int c = c0 + r;
+          const long long Wc = c < g.nch ? fixed40(fast_exp(mx[c] - hi.mstar) * sm[c]) : 0;
+          const long long ci = grp_scan(Wc, r, lph);
+          const long long pref = run + ci - Wc;
+          if (c < g.nch && hv) {
+            pr[c] = pref;
+            jsr[c] = first_at_or_above(pref);
+          }
+          run += __shfl_sync(FULL, ci, lph - 1, lph);
+        }
+        // end of this segment's thresholds: the next segment's first, or the
+        // range's end for the last segment (thresholds in the rounding gap
+        // between the chunk sums and the range mass go to its last chunk)
+        const int jend = sg_i + 1 < nseg ? first_at_or_above(run) : hi.jhi;
+        __syncwarp();
+        if (hv) {
+          for (int c = r; c < g.nch; c += lph) {
+            const int je = c + 1 < g.nch ? jsr[c + 1] : jend;
+            if (je > jsr[c]) g.items[atomicAdd(&n_items, 1)] = hl * 65536 + c;
+          }
+          if (r == 0) {
+            jend_s[hl] = jend;
+            carry_s[hl] = run;
+          }
         }
       }
-      const int* jsr = g.ch ? g.js + qh * g.nch : a.jstart + (bh0 + qh) * cm1 + g.c_lo;
-      const HeadInfo hi = hinfo[qh];
-      const int j0 = qv ? jsr[qc] : 0;
-      const int j1 = qv ? (qc + 1 < g.nch ? jsr[qc + 1] : hi.jhi) : 0;
-      const int nthr = j1 - j0;
-      const int tmax = max(nthr, __shfl_xor_sync(FULL, nthr, 16));
-      if (tmax == 0) continue;   // warp-uniform
-      const int64_t bh = bh0 + qh;
-      const int64_t key = (int64_t)(g.c_lo + qc) * SUB + l16;
-      float sv = -INFINITY;
-      if (nthr > 0 && key < p.nk)
-        sv = g.sto ? g.st[qh * g.cap_st + (int)((bh * a.nk_max + g.key_lo) & 3) + (int)(key - g.key_lo)]
-                   : a.stash[bh * a.nk_max + key];
-      long long F = fixed40(fast_exp(sv - hi.mstar));   // e^{-inf} = 0 past the sequence end
-      const unsigned nzb = (__ballot_sync(FULL, F > 0) >> hb) & 0xffffu;
-      const int lastnz = nzb ? 31 - __clz(nzb) : 0;
+      __syncthreads();   // chunk tables and items visible
+
+      // ---- per (head, 16-key chunk) holding thresholds, one half-warp each:
+      //      exact key-mass prefix over the chunk, one ballot per threshold
+      //      (the key is the first with F > x; a threshold at or beyond the
+      //      chunk's key total goes to its last nonzero key); counts into the
+      //      (KV head, key) table, the union of the group's draws.
+      const int h16 = lane >> 4, l16 = lane & 15, hb = h16 * 16;
+      const int nwork = n_items;
+      for (int q0 = warp * 2; q0 < nwork; q0 += SB_WARPS * 2) {
+        const int q = q0 + h16;
+        const bool qv = q < nwork;
+        const int qh = qv ? g.items[q] >> 16 : 0, qc = qv ? g.items[q] & 0xffff : 0;
+        const int* jsr = g.js + qh * g.nch;
+        const HeadInfo hi = hinfo[qh];
+        const int j0 = qv ? jsr[qc] : 0;
+        const int j1 = qv ? (qc + 1 < g.nch ? jsr[qc + 1] : jend_s[qh]) : 0;
+        const int nthr = j1 - j0;
+        const int tmax = max(nthr, __shfl_xor_sync(FULL, nthr, 16));
+        const int64_t bh = bh0 + qh;
+        const int64_t key = (int64_t)(g.c_lo + qc) * SUB + l16;
+        float sv = -INFINITY;
+        if (nthr > 0 && key < p.nk)
+          sv = g.st[qh * g.cap_st + (int)((bh * a.nk_max + g.key_lo) & 3) + (int)(key - g.key_lo)];
+        long long F = fixed40(fast_exp(sv - hi.mstar));   // e^{-inf} = 0 past the sequence end
+        const unsigned nzb = (__ballot_sync(FULL, F > 0) >> hb) & 0xffffu;
+        const int lastnz = nzb ? 31 - __clz(nzb) : 0;
 #pragma unroll
-      for (int o = 1; o < 16; o <<= 1) {
-        const long long n = __shfl_up_sync(FULL, F, o, 16);
-        if (l16 >= o) F += n;
-      }
-      const long long pref = nthr > 0 ? (g.ch ? g.pref[qh * g.nch + qc] : a.prefix[bh * cm1 + g.c_lo + qc]) : 0;
-      int cnt = 0;
-      for (int t = 0; t < tmax; ++t) {
-        const bool ok = t < nthr;
-        long long x = 0;
-        if (ok) x = (hi.off >= 0 ? pool[hi.off + (j0 - hi.jlo) + t] : a.thresh[bh * a.S_max + j0 + t]) - pref;
-        const unsigned above = (__ballot_sync(FULL, ok && F > x) >> hb) & 0xffffu;
-        const int k = above ? __ffs(above) - 1 : lastnz;
-        if (ok && l16 == k) {
-          ++cnt;
-          if (a.sample_idx) a.sample_idx[bh * a.S_max + j0 + t] = (int)key;
+        for (int o = 1; o < 16; o <<= 1) {
+          const long long n = __shfl_up_sync(FULL, F, o, 16);
+          if (l16 >= o) F += n;
         }
-      }
-      if (g.tab) {
+        const long long pref = nthr > 0 ? g.pref[qh * g.nch + qc] : 0;
+        int cnt = 0;
+        for (int t = 0; t < tmax; ++t) {
+          const bool ok = t < nthr;
+          long long x = 0;
+          if (ok) x = (hi.off >= 0 ? pool[hi.off + (j0 - hi.jlo) + t] : a.thresh[bh * a.S_max + j0 + t]) - pref;
+          const unsigned above = (__ballot_sync(FULL, ok && F > x) >> hb) & 0xffffu;
+          const int k = above ? __ffs(above) - 1 : lastnz;
+          if (ok && l16 == k) {
+            ++cnt;
+            if (a.sample_idx) a.sample_idx[bh * a.S_max + j0 + t] = (int)key;
+          }
+        }
         if (cnt > 0) {
           atomicAdd(&g.table[((qh / G) * g.nkeys + (int)(key - g.key_lo)) * GM + qh % G], cnt);
-          // the gather reads this row after the table is complete: start it towards L2 now
+          // the gather reads this row once the table is complete: start it towards L2 now
           const T* vrow = reinterpret_cast<const T*>(a.V) + ((p.row0 + key) * a.Hkv + p.hg * W + qh / G) * (int64_t)D;
 #pragma unroll
           for (int ln = 0; ln < (D * 2 + 127) / 128; ++ln)
             asm volatile("prefetch.global.L2 [%0];" ::"l"(vrow + ln * 64));
         }
-        continue;
       }
-      // no table: gather the drawn keys' rows here, four at a time per half-warp
-      const unsigned drawn = (__ballot_sync(FULL, cnt > 0) >> hb) & 0xffffu;
-      const int nd = __popc(drawn), ndmax = max(nd, __shfl_xor_sync(FULL, nd, 16));
-      const int kvh = p.hg * W + qh / G;
-      const T* Vb = reinterpret_cast<const T*>(a.V) + (p.row0 * a.Hkv + kvh) * (int64_t)D + l16 * TL::EPL;
-      for (int d0 = 0; d0 < ndmax; d0 += 4) {
-        uint4 vv[4];
-        float cw[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const bool have = d0 + u < nd;
-          const int kl = have ? (int)__fns(drawn, 0, d0 + u + 1) : 0;
-          cw[u] = (float)__shfl_sync(FULL, cnt, hb + kl);
-          const int64_t kk = (int64_t)(g.c_lo + qc) * SUB + kl;
-          vv[u] = (have && l16 < TL::LPK) ? ld_stream(Vb + kk * a.Hkv * D) : make_uint4(0, 0, 0, 0);
-          if (!have) cw[u] = 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (cw[u] != 0.f && l16 < TL::LPK) {
-            float vf[TL::EPL];
-            Elem<T>::widen(vv[u], vf);
-#pragma unroll
-            for (int e = 0; e < TL::EPL; ++e) atomicAdd(&obuf[qh * D + l16 * TL::EPL + e], cw[u] * vf[e]);
-          }
-        }
-      }
-    }
-    if (g.tab) {
       __syncthreads();   // the count table is complete
+
       // ---- gather by KV head: warp w takes KV head w % W and every
-      //      (16 / W)-th of its drawn rows; each drawn V row is read once for
-      //      all heads of its group, lane l owns output columns [4l, 4l + 4)
-      //      (D = 128) or [2l, 2l + 2) (D = 64) of every head, and the warp's
-      //      sums, times 1/S_b, go into out with vectorised fp32 reductions
-      //      (their order across warps and CTAs is not fixed).
-      const int wk = warp % W, part = warp / W, nparts = SB_WARPS / W;
-      constexpr int CPL = D / 32;                 // output columns per lane
-      float acc[GM][CPL];
+      //      (16 / W)-th 32-key block of the segment; each drawn V row is read
+      //      once for all heads of its group, lane l owns output columns
+      //      [l CPL, (l + 1) CPL) of every head, and the warp's sums, times
+      //      1/S_b, go into out with vectorised fp32 reductions (their order
+      //      across warps and CTAs is not fixed).
+      {
+        const int wk = warp % W, part = warp / W, nparts = SB_WARPS / W;
+        constexpr int CPL = D / 32;   // output columns per lane
+        float acc[GM][CPL];
 #pragma unroll
-      for (int gg = 0; gg < GM; ++gg)
+        for (int gg = 0; gg < GM; ++gg)
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) acc[gg][c] = 0.f;
-      const int* tab = g.table + (size_t)wk * g.nkeys * GM;
-      const T* Vk = reinterpret_cast<const T*>(a.V) + (p.row0 * a.Hkv + p.hg * W + wk) * (int64_t)D + lane * CPL;
-      // this warp's drawn rows (key within the piece, counts), then their
-      // loads all in flight together, eight at a time
-      bool any_rows = false;
-      int nmine = 0;
-      int rk_l = -1;            // lane l holds the l-th row of this warp (32 at most per batch)
-      int rc_l[GM];
+          for (int c = 0; c < CPL; ++c) acc[gg][c] = 0.f;
+        const int* tab = g.table + (size_t)wk * g.nkeys * GM;
+        const T* Vk = reinterpret_cast<const T*>(a.V) + (p.row0 * a.Hkv + p.hg * W + wk) * (int64_t)D + lane * CPL;
+        bool any_rows = false;
+        int nmine = 0;
+        int rk_l = -1;   // lane l holds the l-th listed row of this warp
+        int rc_l[GM];
 #pragma unroll
-      for (int gg = 0; gg < GM; ++gg) rc_l[gg] = 0;
-      auto gather_batch = [&](int n) {   // rows held by lanes 0..n-1
-        for (int r0 = 0; r0 < n; r0 += 8) {
-          uint2 raw[8];
+        for (int gg = 0; gg < GM; ++gg) rc_l[gg] = 0;
+        auto gather_batch = [&](int n) {   // rows held by lanes 0..n-1, four loads in flight
+          for (int r0 = 0; r0 < n; r0 += 4) {
+            uint2 raw[4];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int kr = __shfl_sync(FULL, rk_l, (r0 + u) & 31);
-            raw[u] = make_uint2(0u, 0u);
-            if (r0 + u < n) {
-              const T* src = Vk + (g.key_lo + kr) * a.Hkv * D;
-              if constexpr (CPL == 4) raw[u] = *reinterpret_cast<const uint2*>(src);
-              else raw[u].x = *reinterpret_cast<const uint32_t*>(src);
+            for (int u = 0; u < 4; ++u) {
+              const int kr = __shfl_sync(FULL, rk_l, (r0 + u) & 31);
+              raw[u] = make_uint2(0u, 0u);
+              if (r0 + u < n) {
+                const T* src = Vk + (g.key_lo + kr) * a.Hkv * D;
+                if constexpr (CPL == 4) raw[u] = *reinterpret_cast<const uint2*>(src);
+                else raw[u].x = *reinterpret_cast<const uint32_t*>(src);
+              }
             }
-          }
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            if (r0 + u < n) {   // warp-uniform
-              float vf[4];
-              f2x pr[4];
-              Pairs<T>::get(make_uint4(raw[u].x, raw[u].y, 0u, 0u), pr);
-              const float2 p0 = unpack2(pr[0]), p1 = unpack2(pr[1]);
-              vf[0] = p0.x; vf[1] = p0.y; vf[2] = p1.x; vf[3] = p1.y;
+            for (int u = 0; u < 4; ++u) {
+              if (r0 + u < n) {   // warp-uniform
+                f2x pr[4];
+                Pairs<T>::get(make_uint4(raw[u].x, raw[u].y, 0u, 0u), pr);
+                const float2 p0 = unpack2(pr[0]), p1 = unpack2(pr[1]);
+                const float vf[4] = {p0.x, p0.y, p1.x, p1.y};
 #pragma unroll
-              for (int gg = 0; gg < GM; ++gg) {
-                const float cw = (float)__shfl_sync(FULL, rc_l[gg], (r0 + u) & 31);
+                for (int gg = 0; gg < GM; ++gg) {
+                  const float cw = (float)__shfl_sync(FULL, rc_l[gg], (r0 + u) & 31);
 #pragma unroll
-                for (int c = 0; c < CPL; ++c) acc[gg][c] = fmaf(cw, vf[c], acc[gg][c]);
+                  for (int c = 0; c < CPL; ++c) acc[gg][c] = fmaf(cw, vf[c], acc[gg][c]);
+                }
               }
             }
           }
-        }
-      };
-      for (int k0 = 0; k0 < g.nkeys; k0 += 32) {
-        const int kr = k0 + lane;
-        int cg[GM];
-        bool drawn_here = false;
+        };
+        for (int k0b = part * 32; k0b < g.nkeys; k0b += 32 * nparts) {
+          const int kr = k0b + lane;
+          int cg[GM];
+          bool drawn_here = false;
 #pragma unroll
-        for (int gg = 0; gg < GM; ++gg) {
-          cg[gg] = (kr < g.nkeys && gg < G) ? tab[kr * GM + gg] : 0;
-          drawn_here |= cg[gg] != 0;
+          for (int gg = 0; gg < GM; ++gg) {
+            cg[gg] = (kr < g.nkeys && gg < G) ? tab[kr * GM + gg] : 0;
+            drawn_here |= cg[gg] != 0;
+          }
+          const unsigned mine = __ballot_sync(FULL, drawn_here);
+          const int add = __popc(mine);
+          if (nmine + add > 32) {
+            gather_batch(nmine);
+            any_rows = any_rows || nmine > 0;
+            nmine = 0;
+          }
+          for (int t = 0; t < add; ++t) {   // lane nmine + t receives the t-th row of this block
+            const int src_lane = (int)__fns(mine, 0, t + 1);
+            const int krow = __shfl_sync(FULL, kr, src_lane);
+            int cgs[GM];
+#pragma unroll
+            for (int gg = 0; gg < GM; ++gg) cgs[gg] = __shfl_sync(FULL, cg[gg], src_lane);
+            if (lane == nmine + t) {
+              rk_l = krow;
+#pragma unroll
+              for (int gg = 0; gg < GM; ++gg) rc_l[gg] = cgs[gg];
+            }
+          }
+          nmine += add;
         }
-        // rows of this part: the drawn rows of every nparts-th 32-key block
-        const unsigned mine = ((k0 / 32) % nparts == part) ? __ballot_sync(FULL, drawn_here) : 0u;
-        // append to the lane-held list; gather when it would overflow
-        const int add = __popc(mine);
-        if (nmine + add > 32) {
+        if (nmine > 0) {
           gather_batch(nmine);
-          any_rows = any_rows || nmine > 0;
-          nmine = 0;
+          any_rows = true;
         }
-        // lane nmine + t receives the t-th row of this block
-        for (int t = 0; t < add; ++t) {
-          const int src_lane = (int)__fns(mine, 0, t + 1);
-          const int krow = __shfl_sync(FULL, kr, src_lane);
-          int cgs[GM];
+        if (any_rows) {   // warp-uniform
+          const float inv_S = 1.0f / (float)S_b;
+          float* outp = a.out + (bh0 + (int64_t)wk * G) * D + lane * CPL;
 #pragma unroll
-          for (int gg = 0; gg < GM; ++gg) cgs[gg] = __shfl_sync(FULL, cg[gg], src_lane);
-          if (lane == nmine + t) {
-            rk_l = krow;
-#pragma unroll
-            for (int gg = 0; gg < GM; ++gg) rc_l[gg] = cgs[gg];
-          }
-        }
-        nmine += add;
-      }
-      if (nmine > 0) {
-        gather_batch(nmine);
-        any_rows = true;
-      }
-      if (any_rows) {   // warp-uniform
-        const float inv_S = 1.0f / (float)S_b;
-        float* outp = a.out + (bh0 + (int64_t)wk * G) * D + lane * CPL;
-#pragma unroll
-        for (int gg = 0; gg < GM; ++gg) {
-          if (gg < G) {
-            if constexpr (CPL == 4)
-              red_add_v4(outp + (int64_t)gg * D,
-                         make_float4(acc[gg][0] * inv_S, acc[gg][1] * inv_S, acc[gg][2] * inv_S, acc[gg][3] * inv_S));
-            else
-              red_add_v2(outp + (int64_t)gg * D, make_float2(acc[gg][0] * inv_S, acc[gg][1] * inv_S));
+          for (int gg = 0; gg < GM; ++gg) {
+            if (gg < G) {
+              if constexpr (CPL == 4)
+                red_add_v4(outp + (int64_t)gg * D,
+                           make_float4(acc[gg][0] * inv_S, acc[gg][1] * inv_S, acc[gg][2] * inv_S, acc[gg][3] * inv_S));
+              else
+                red_add_v2(outp + (int64_t)gg * D, make_float2(acc[gg][0] * inv_S, acc[gg][1] * inv_S));
+            }
           }
         }
       }
-      __syncthreads();
-      return;   // uniform over the CTA (g.tab)
+      __syncthreads();   // the segment's buffers are free for the next one
     }
-    __syncthreads();
-    // no table (a piece too large for it): this CTA's sums, times 1/S_b, into out
-    const float inv_S = 1.0f / (float)S_b;
-    float* outp = a.out + bh0 * D;
-    for (int i4 = tid; i4 < GW * D / 4; i4 += SB_THREADS) {
-      const float4 v = reinterpret_cast<const float4*>(obuf)[i4];
-      if (v.x != 0.f || v.y != 0.f || v.z != 0.f || v.w != 0.f)
-        red_add_v4(outp + 4 * i4, make_float4(v.x * inv_S, v.y * inv_S, v.z * inv_S, v.w * inv_S));
-    }
-    __syncthreads();
   });
   cp_async_wait_all();   // no copy outlives the CTA (a staged piece that was skipped)
 }
@@ -1012,8 +985,10 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
 template <typename T, int D, int GM>
 static cudaError_t launch_fused_g(const LaunchArgs& a, unsigned* bar_count, unsigned* bar_gen) {
   using Gm = StreamGeom<T, D>;
-  static_assert((size_t)GM * 8 * D * 4 + (size_t)GM * 8 * sizeof(HeadInfo) + (size_t)POOL_CAP * 8 + 4096 <= Gm::SMEM,
-                "phase B fixed regions fit the ring");
+  static_assert((size_t)GM * 8 * sizeof(HeadInfo) + (size_t)POOL_CAP * 8 +
+                        (size_t)64 * (8 + 16 + 4 * SUB) * 2 + (size_t)8 * SUB * GM * 4 * 2 + 64 * 84 + 96 <=
+                    Gm::SMEM,
+                "phase B fixed regions and a two-chunk segment fit the ring");
   const int W = unit_heads(a.Hkv);
   const int unit_rows = SB_UNIT_ROWS_X_W / W;
   const long long units = (long long)a.B * ((a.nk_max + unit_rows - 1) / unit_rows) * (a.Hkv / W);

@@ -64,7 +64,8 @@ __device__ __forceinline__ int lane_lower_bound(long long x, int n, long long v)
 // A key n is drawn by threshold x with F(n-1) <= x < F(n) (window-relative
 // exact prefixes); thresholds at or beyond the window's total (rounding of the
 // chunk masses against the key masses) go to the window's last nonzero key.
-__device__ __forceinline__ int window_draws(float sv, float mst, long long th0, int nt, long long pb,
+// Not inlined (the staged sampler calls it from many unrolled sites).
+static __device__ __noinline__ int window_draws(float sv, float mst, long long th0, int nt, long long pb,
                                             const long long* th, int32_t* idx, int key, int lane) {
   const long long w = mass_fixed(expf(sv - mst));   // e^{-inf} = 0 past the sequence end
   const long long F = warp_inclusive_scan(w, lane);
