@@ -20,8 +20,7 @@ constexpr size_t BAR_COUNT = 64, BAR_GEN = 128;  // header offsets of the grid-b
 size_t up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
 
 struct Layout {
-  size_t stash, tile_max, tile_sum, prefix, thresh, jstart, head_max, part_o, agg_m, agg_l, ukeys, rcp_S;
-  size_t bnd_P, bnd_T, bnd_jlo, bnd_jhi, head_Z, total;
+  size_t stash, tile_max, tile_sum, prefix, thresh, jstart, head_max, part_o, agg, ukeys, rcp_S, total;
   int64_t chunks, groups;
 };
 
@@ -67,15 +66,9 @@ Layout santa_layout(const santa_params_t* p) {
   L.thresh = off;   off += up(B * H * S * sizeof(long long));
   L.jstart = off;   off += up(B * H * ((size_t)L.chunks + 1) * sizeof(int32_t));
   L.head_max = off; off += up(B * H * sizeof(float));
-  L.agg_m = off;    off += up(B * H * santa::MAX_CTAS * sizeof(float));
-  L.agg_l = off;    off += up(B * H * santa::MAX_CTAS * sizeof(float));
+  L.agg = off;      off += up(B * H * santa::MAX_CTAS * 16);
   L.ukeys = off;    off += up(B * H * S * sizeof(uint32_t));
   L.rcp_S = off;    off += up(B * sizeof(unsigned long long));
-  L.bnd_P = off;    off += up(B * H * santa::MAX_CTAS * sizeof(long long));
-  L.bnd_T = off;    off += up(B * H * santa::MAX_CTAS * sizeof(long long));
-  L.bnd_jlo = off;  off += up(B * H * santa::MAX_CTAS * sizeof(int32_t));
-  L.bnd_jhi = off;  off += up(B * H * santa::MAX_CTAS * sizeof(int32_t));
-  L.head_Z = off;   off += up(B * H * sizeof(long long));
   L.part_o = 0;
   L.total = off;
   return L;
@@ -158,15 +151,9 @@ santa_status_t decode_impl(const santa_params_t* p, int32_t variant, const void*
   a.thresh = reinterpret_cast<long long*>(w + L.thresh);
   a.jstart = reinterpret_cast<int32_t*>(w + L.jstart);
   a.head_max = reinterpret_cast<float*>(w + L.head_max);
-  a.agg_m = reinterpret_cast<float*>(w + L.agg_m);
-  a.agg_l = reinterpret_cast<float*>(w + L.agg_l);
+  a.agg = w + L.agg;
   a.ukeys = reinterpret_cast<uint32_t*>(w + L.ukeys);
   a.rcp_S = reinterpret_cast<unsigned long long*>(w + L.rcp_S);
-  a.bnd_P = reinterpret_cast<long long*>(w + L.bnd_P);
-  a.bnd_T = reinterpret_cast<long long*>(w + L.bnd_T);
-  a.bnd_jlo = reinterpret_cast<int32_t*>(w + L.bnd_jlo);
-  a.bnd_jhi = reinterpret_cast<int32_t*>(w + L.bnd_jhi);
-  a.head_Z = reinterpret_cast<long long*>(w + L.head_Z);
 
   // 16-bit caches with Philox uniforms: the whole step in one cooperative
   // launch; otherwise (fp32, caller uniforms, per-stage events) three stages.

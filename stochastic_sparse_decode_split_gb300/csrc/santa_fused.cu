@@ -11,18 +11,21 @@
 // Grid: one 512-thread CTA per SM, launched cooperatively (all CTAs
 // resident).  Phase A streams the CTA's contiguous range of score-pass units
 // (santa_stream.cuh) and reduces, for every head it touched, the range's
-// (max, exp-sum) aggregate.  One grid-wide barrier.  Phase B: every CTA reads
-// the aggregates of the CTAs that cover the same (sequence, KV-head group),
-// which gives the head max m*, the total mass Z and the mass prefix P_i of its
-// own key range exactly (fixed-point int64, computed identically in every
-// CTA), places the thresholds that fall in [P_i, P_i + T_i), resolves them in
-// its own chunks and 32-key windows, and gathers and adds the drawn V rows.
+// aggregate (max, and the mass relative to a power of two).  One grid-wide
+// barrier.  Phase B: every CTA reads the aggregates of the CTAs that cover the
+// same (sequence, KV-head group), which gives the head's reference 2^E*, the
+// total mass Z and the mass prefix P_i of its own key range exactly
+// (fixed-point int64, the same integers in every CTA), places the thresholds
+// that fall in [P_i, P_i + T_i), resolves them in its own chunks, and gathers
+// and adds the drawn V rows.
 //
 // Phase B is latency-bound (little data, dependent steps), so it is laid out
-// for parallelism: one round of asynchronous copies stages everything a CTA
-// reads (aggregates, its chunk statistics, its scores) in shared memory; the
+// for parallelism and few waits: the first segment of chunk statistics and
+// scores is staged in shared memory while the CTA waits at the barrier; the
 // per-head work runs in groups of 8-32 lanes, all heads of a KV-head group at
-// once; windows go to warps in contiguous blocks.
+// once; each (head, chunk) holding draws takes a half-warp; drawn (head, key)
+// pairs go to a list, and warp w sums the V rows of its heads (w, w + 16, ...)
+// in registers until the end of the piece.
 //
 // Difference from the pages' kernels: Alg. 4 rounds per-tile budgets by
 // largest remainder and samples each tile on its own; here the S thresholds of
@@ -102,10 +105,36 @@ __device__ __forceinline__ long long grp_scan(long long v, int r, int lph) {   /
   return v;
 }
 
-// Mass w (relative to the head max, in [0, 2^22)) in units of 2^-40, rounded
-// toward zero: one exact scaling and one conversion (the same value as
-// mass_fixed for these w).
-__device__ __forceinline__ long long fixed40(float w) { return __float2ll_rz(w * 1099511627776.0f); }
+// Mass w (relative to the head's reference, in [0, 2^22)) in units of 2^-40,
+// rounded toward zero, by integer operations (mass_fixed).
+__device__ __forceinline__ long long fixed40(float w) { return mass_fixed(w); }
+
+// Aggregate of one head over one CTA's keys.  Masses are taken relative to a
+// power of two so that every reader rescales them exactly by a shift:
+//   m  max score over the keys
+//   e  ceil(m log2(e)), an integer
+//   F  sum_n 2^(s_n log2(e) - e) in units of 2^-40 (rounded toward zero)
+// With E* the largest e over the CTAs of a head, CTA k's mass relative to
+// 2^E* is F_k >> (E* - e_k): the same integer in every CTA that computes it.
+constexpr int AGG_EMPTY = -(1 << 30);   // e of a range with no finite score
+struct __align__(16) Agg {
+  float m;
+  int e;
+  long long F;
+};
+// from the max m and the natural-base sum l = sum_n exp(s_n - m)
+__device__ __forceinline__ Agg make_agg(float m, float l) {
+  Agg x;
+  x.m = m;
+  x.e = AGG_EMPTY;
+  x.F = 0;
+  if (m > -INFINITY) {
+    const float t = m * LOG2E;
+    x.e = (int)ceilf(t);
+    x.F = fixed40(l * fast_exp2(t - (float)x.e));
+  }
+  return x;
+}
 
 struct Draws {
   int variant, S, h, b;
@@ -133,11 +162,13 @@ struct Draws {
       if (X <= 0) return 0;
       if (X >= tc.Z) return S;
       // theta_j lies in [floor(j Z / S), floor((j + 1) Z / S)): start next to X S / Z
-      long long e = (long long)(__fdividef((float)X, (float)tc.Z) * (float)S);
+      // (24 leading bits of X and Z: 32-bit conversions, not the FP64-pipe int64 ones)
+      const int sh = max(0, 40 - __clzll(tc.Z));
+      int e = (int)(__fdividef((float)(uint32_t)(X >> sh), (float)(uint32_t)(tc.Z >> sh)) * (float)S);
       e = e < 0 ? 0 : (e > S ? S : e);
-      while (e > 0 && theta((int)e - 1) >= X) --e;
-      while (e < S && theta((int)e) < X) ++e;
-      return (int)e;
+      while (e > 0 && theta(e - 1) >= X) --e;
+      while (e < S && theta(e) < X) ++e;
+      return e;
     }
     // sorted keys: lph-way search, one probe per lane and round
     int lo = 0, hi = S;
@@ -207,11 +238,6 @@ __device__ __forceinline__ void grid_wait(const unsigned* gen, unsigned g, int* 
   }
   __syncthreads();
 }
-__device__ __forceinline__ void grid_barrier(unsigned* count, unsigned* gen, int* err) {
-  __syncthreads();
-  const unsigned g = grid_arrive(count, gen);
-  grid_wait(gen, g, err);
-}
 
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
@@ -276,51 +302,19 @@ __device__ __forceinline__ int seq_error(const LaunchArgs& a, int b, int& S_b) {
   return err;
 }
 
-// Geometry of head bh (global index b * H + h) for the owner step: its
-// sequence's validity and budget, the covering CTAs [i_first, i_last] of its
-// (sequence, KV-head group), the budget reciprocal and the systematic uniform.
-// Warp-uniform (the ragged unit count is a warp reduction).
+// Per-head constants of the thresholds.
 struct HeadGeom {
-  int b, h, S_b, i_first, i_last;
+  int b, h, S_b;
   unsigned long long rcp;   // ceil(2^64 / S_b)
   uint32_t ksys;            // systematic: the head's uniform key
-  bool ok;
 };
-__device__ __forceinline__ HeadGeom head_geom(const LaunchArgs& a, long long bh, int unit_rows, int n_hg, int GW, int P,
-                                           long long n_units, uint32_t k0, uint32_t k1) {
-  const int lane = threadIdx.x % 32;
-  HeadGeom q;
-  q.b = (int)(bh / a.H);
-  q.h = (int)(bh % a.H);
-  q.ok = seq_error(a, q.b, q.S_b) == 0;
-  int64_t r0_, nk_;
-  const int units_b = UnitCursor::seq_units(a.kv_offsets, a.nk_max, unit_rows, q.b, r0_, nk_);
-  long long base = (long long)q.b * units_b;
-  if (a.kv_offsets) {
-    base = 0;
-    for (int b0 = 0; b0 < q.b; b0 += 32) {
-      int64_t r1, n1;
-      long long u = (b0 + lane < q.b) ? UnitCursor::seq_units(a.kv_offsets, a.nk_max, unit_rows, b0 + lane, r1, n1) : 0;
-      for (int o = 16; o > 0; o >>= 1) u += __shfl_xor_sync(FULL, u, o);
-      base += u;
-    }
-  }
-  const long long U = base * n_hg + (long long)(q.h / GW) * units_b;   // unit (b, hg, kb = 0)
-  q.i_first = (int)(((U + 1) * P - 1) / n_units);
-  q.i_last = (int)(((U + units_b) * P - 1) / n_units);
-  q.ok = q.ok && units_b > 0;
-  q.rcp = (q.ok && q.S_b > 1) ? ~0ull / (unsigned)q.S_b + 1ull : 0ull;
-  q.ksys = a.variant == VAR_SYS ? philox4x32_10(make_uint4(0u, (uint32_t)q.h, (uint32_t)q.b, a.step), k0, k1).x >> 8
-                                : 0u;
-  return q;
-}
 
 // Per-head state of phase B (shared memory).
 struct HeadInfo {
   long long pown;   // mass prefix of this CTA's key range
   int jlo, jhi;     // this CTA's threshold range [jlo, jhi)
   int off;          // offset of its thresholds in the shared pool, -1: in the global array
-  float mstar;      // the head's max score
+  float ref;        // masses are 2^(s log2(e) - ref): ref = E*, the head's largest aggregate exponent
 };
 
 template <typename T, int D, int GM>
@@ -332,7 +326,7 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
   __shared__ int start[4];
   __shared__ long long range[2];
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const int G = a.H / a.Hkv, W = unit_heads(a.Hkv), n_hg = a.Hkv / W;
+  const int G = a.H / a.Hkv, W = a.W, n_hg = a.Hkv / W;
   const int unit_rows = SB_UNIT_ROWS_X_W / W;
   const int GW = G * W;                       // query heads of one KV-head group
   const int lph = GW > 32 ? 8 : (GW > 16 ? 16 : 32);   // lanes per head in the per-head steps
@@ -438,18 +432,19 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     const int ub = UnitCursor::seq_units(a.kv_offsets, a.nk_max, unit_rows, start[0], r0_, nk_);
     one_piece = start[2] + start[3] <= ub;
   }
+  Agg* const agg = reinterpret_cast<Agg*>(a.agg);
   if (one_piece) {
     if (tid < GW) {
+      // warps 2x and 2x + 1 stream KV head x mod W of the group
       const int wl = tid / G, g = tid % G;   // KV head within the group, head within its query group
       float m = -INFINITY;
-      for (int w = 0; w < SB_WARPS; ++w)
-        if (((w >> 1) % W) == wl) m = fmaxf(m, run_m[w * 8 + g]);
+      for (int x = wl; x < SB_WARPS / 2; x += W) m = fmaxf(m, fmaxf(run_m[2 * x * 8 + g], run_m[(2 * x + 1) * 8 + g]));
       float l = 0.f;
-      for (int w = 0; w < SB_WARPS; ++w)
-        if (((w >> 1) % W) == wl && run_m[w * 8 + g] > -INFINITY) l += run_l[w * 8 + g] * expf(run_m[w * 8 + g] - m);
+      for (int x = wl; x < SB_WARPS / 2; x += W)
+        for (int w = 2 * x; w < 2 * x + 2; ++w)
+          if (run_m[w * 8 + g] > -INFINITY) l += run_l[w * 8 + g] * expf(run_m[w * 8 + g] - m);
       const int64_t bh = (int64_t)start[0] * a.H + (int64_t)start[1] * GW + tid;
-      a.agg_m[bh * MAX_CTAS + cta] = m;
-      a.agg_l[bh * MAX_CTAS + cta] = l;
+      agg[bh * MAX_CTAS + cta] = make_agg(m, l);
     }
   } else
   for_each_piece(a, n_hg, unit_rows, start, range[1], [&](const Piece& p) {
@@ -465,10 +460,7 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     float l = 0.f;
     for (int c = c_lo + r; c < c_hi; c += lph) l += expf(mx[c] - m) * sm[c];
     l = grp_sum(l, lph);
-    if (hv && r == 0) {
-      a.agg_m[bh * MAX_CTAS + cta] = m;
-      a.agg_l[bh * MAX_CTAS + cta] = l;
-    }
+    if (hv && r == 0) agg[bh * MAX_CTAS + cta] = make_agg(m, l);
   });
 
   // ---------------------------------------------------------------------------
@@ -479,24 +471,25 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
   long long* pool = reinterpret_cast<long long*>(hinfo + GM * 8);                // [POOL_CAP]
   unsigned char* var0 = reinterpret_cast<unsigned char*>(pool + POOL_CAP);       // per-segment staging
   const size_t var_cap = Gm::SMEM - (size_t)(var0 - smem);
-  __shared__ int pool_used, n_items;
-  __shared__ float red_f[SB_WARPS];
-  __shared__ long long red_ll[SB_WARPS];
+  __shared__ int pool_used, n_items, n_ent;
+  constexpr int HPW = GM / 2;    // heads per warp in the gather: head h goes to warp h mod 16 (GW <= 8 GM)
+  constexpr int CPL = D / 32;    // output columns per lane
   // A piece's key range is processed in segments of SEG statistics chunks, so
   // that a segment's chunk statistics, scores, chunk tables, item list and
-  // (KV head, key) count table all fit in shared memory.
+  // list of drawn (head, key) pairs all fit in shared memory.
   const int SEG = [&] {
-    const size_t per_chunk = (size_t)GW * (8 + 16 + 4 * SUB) + (size_t)W * SUB * GM * 4;
+    const size_t per_chunk = (size_t)GW * (8 + 16 + 4 * SUB) + (size_t)GW * SUB * 4;
     const size_t fixed = (size_t)GW * (2 * 7 * 4 + 7 * 4) + 8 * 16;   // row caps and alignment of 7 buffers
     const int n = (int)((var_cap - fixed) / per_chunk);
-    return max(2, n & ~1);
+    return min(512, max(2, n & ~1));   // keys of a segment fit the 13-bit key field of a list entry
   }();
   struct Seg {
     int c_lo, nch, nkeys, cap_ch, cap_st;   // first statistics chunk (in the sequence), chunks, keys
     int64_t key_lo;
     float *mx, *sm, *st;
     long long* pref;
-    int *js, *items, *table;
+    int *js, *items;
+    uint32_t* ent;   // drawn (head, key) pairs: key << 19 | head << 13 | count
   };
   // segment k of piece p: chunks [c_lo + k SEG, ...) of the piece's range
   auto seg_of = [&](const Piece& p, int k) {
@@ -521,7 +514,7 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     g.js = reinterpret_cast<int*>(take((size_t)GW * g.nch * 4));
     g.items = reinterpret_cast<int*>(take((size_t)GW * g.nch * 4));
     g.st = reinterpret_cast<float*>(take((size_t)GW * g.cap_st * 4));
-    g.table = reinterpret_cast<int*>(take((size_t)W * g.nkeys * GM * 4));
+    g.ent = reinterpret_cast<uint32_t*>(take((size_t)GW * g.nkeys * 4));
     return g;
   };
   auto seg_count = [&](const Piece& p) {
@@ -537,7 +530,7 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     const int n16 = (int)((g0 + len - a0 + 3) >> 2);
     for (int j = lane; j < n16; j += 32) cp_async16(smem_addr(s_row + 4 * j), base + a0 + 4 * j);
   };
-  // copies of a segment's statistics and scores (one commit group), count table cleared
+  // copies of a segment's statistics and scores (one commit group)
   auto stage = [&](const Piece& p, const Seg& g) {
     const int64_t bh0 = (int64_t)p.b * a.H + (int64_t)p.hg * GW;
     for (int h = warp; h < GW; h += SB_WARPS) {
@@ -547,14 +540,10 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
       stage_row(g.st + h * g.cap_st, a.stash, bh * a.nk_max + g.key_lo, g.nkeys);
     }
     cp_async_commit();
-    for (int i = tid; i < W * g.nkeys * GM; i += SB_THREADS) g.table[i] = 0;
   };
 
   auto nonempty = [&](int i) {   // CTA i owns at least one unit
     return n_units >= P || n_units * i / P < n_units * (i + 1) / P;
-  };
-  auto geom = [&](long long bh) {   // the same in every lane of a warp
-    return head_geom(a, bh, unit_rows, n_hg, GW, P, n_units, k0, k1);
   };
   auto make_draws = [&](const HeadGeom& q, long long bh, long long Z) {
     Draws dr;
@@ -570,9 +559,6 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     dr.tc = a.variant == VAR_IID ? theta_ctx(Z, 1u, 0ull) : theta_ctx(Z, (unsigned)q.S_b, q.rcp);
     return dr;
   };
-  // boundary i of a head: prefix, mass and the first threshold of the range
-  // (counts of the i.i.d. sorted thresholds are taken in the CTA that owns the
-  // range); the range ends where the next one starts
   // first barrier; while waiting, this CTA stages its first piece's chunk
   // statistics and scores (its own data, already written)
   __syncthreads();
@@ -601,101 +587,7 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     prestaged = true;
     if (tid == 0) pre_bad0 = seq_error(a, p0.b, pre_S0) != 0;
   }
-  // ... and the geometry of the heads it will own in the next step (metadata
-  // loads, budget reciprocal, systematic uniform), one warp per head
-  constexpr int PRE_MAX = SB_WARPS;
-  __shared__ HeadGeom pre_geom[PRE_MAX];
-  {
-    const long long bh = cta + (long long)warp * P;
-    if (bh < (long long)a.B * a.H) {
-      const HeadGeom q = geom(bh);
-      if (lane == 0) pre_geom[warp] = q;
-    }
-  }
-  grid_wait(bar_gen, gen1, a.err);   // its __syncthreads also publishes pre_geom
-  // the k-th head owned by this CTA
-  auto owned_geom = [&](long long bh) {
-    const long long k = (bh - cta) / P;
-    return k < PRE_MAX ? pre_geom[k] : geom(bh);
-  };
-
-  // ======================= phase B0: per-head globals =======================
-  // From the aggregates of the CTAs covering a head's (sequence, KV-head
-  // group): the head max m*, the total mass Z, and for each covering CTA i its
-  // mass prefix P_i, mass T_i and threshold range [count(P_i), count(P_i + T_i)).
-  // Heads covered by more than 32 CTAs take a whole CTA (one covering CTA per
-  // thread); the others a warp (one per lane).
-  auto write_bnd = [&](const Draws& dr, long long bh, int i, long long Pi, long long Ti) {
-    const int64_t o = bh * MAX_CTAS + i;
-    a.bnd_P[o] = Pi;
-    a.bnd_T[o] = Ti;
-    const int jlo = a.variant == VAR_IID ? -1 : dr.count_below(Pi, 0, 32, lane, 0);
-    a.bnd_jlo[o] = jlo;
-    return jlo;
-  };
-  __shared__ int s_jlo[MAX_CTAS + 1];
-  // (1) wide heads: one CTA each
-  for (long long bh = cta; bh < (long long)a.B * a.H; bh += P) {
-    const HeadGeom q = owned_geom(bh);
-    const int ncov = q.i_last - q.i_first + 1;
-    const int i = q.i_first + tid;
-    // loaded before the validity test so that these loads overlap the metadata loads
-    const bool ok = tid < ncov && i < MAX_CTAS && nonempty(i);
-    const float mi = ok ? a.agg_m[bh * MAX_CTAS + i] : -INFINITY;
-    const float li = ok ? a.agg_l[bh * MAX_CTAS + i] : 0.f;
-    if (!q.ok || ncov <= 32) continue;   // uniform over the CTA
-    float m = warp_max(mi);
-    if (lane == 0) red_f[warp] = m;
-    __syncthreads();
-    m = red_f[0];
-#pragma unroll
-    for (int w = 1; w < SB_WARPS; ++w) m = fmaxf(m, red_f[w]);
-    const long long Ti = ok ? fixed40(fast_exp(mi - m) * li) : 0;
-    const long long incl = warp_inclusive_scan(Ti, lane);
-    if (lane == 31) red_ll[warp] = incl;
-    __syncthreads();
-    long long before = 0, Z = 0;
-#pragma unroll
-    for (int w = 0; w < SB_WARPS; ++w) {
-      before += w < warp ? red_ll[w] : 0;
-      Z += red_ll[w];
-    }
-    const Draws dr = make_draws(q, bh, Z);
-    if (tid < ncov) s_jlo[tid] = write_bnd(dr, bh, i, before + incl - Ti, Ti);
-    if (tid == 0) {
-      a.head_max[bh] = m;
-      a.head_Z[bh] = Z;
-    }
-    __syncthreads();
-    if (tid < ncov)
-      a.bnd_jhi[bh * MAX_CTAS + i] = a.variant == VAR_IID ? -1 : (tid + 1 < ncov ? s_jlo[tid + 1] : q.S_b);
-    __syncthreads();
-  }
-  // (2) narrow heads: one warp each
-  for (long long bh = (long long)warp * P + cta; bh < (long long)a.B * a.H; bh += (long long)SB_WARPS * P) {
-    const HeadGeom q = owned_geom(bh);
-    const int ncov = q.i_last - q.i_first + 1;
-    const int i = q.i_first + lane;
-    const bool ok = lane < ncov && i < MAX_CTAS && nonempty(i);
-    const float mi = ok ? a.agg_m[bh * MAX_CTAS + i] : -INFINITY;
-    const float li = ok ? a.agg_l[bh * MAX_CTAS + i] : 0.f;
-    if (!q.ok || ncov > 32) continue;   // warp-uniform
-    const float m = warp_max(mi);
-    const long long Ti = ok ? fixed40(fast_exp(mi - m) * li) : 0;
-    const long long incl = warp_inclusive_scan(Ti, lane);
-    const long long Z = __shfl_sync(FULL, incl, 31);
-    const Draws dr = make_draws(q, bh, Z);
-    const int jlo = lane < ncov ? write_bnd(dr, bh, i, incl - Ti, Ti) : 0;
-    const int jnext = __shfl_down_sync(FULL, jlo, 1);
-    if (lane < ncov)
-      a.bnd_jhi[bh * MAX_CTAS + i] = a.variant == VAR_IID ? -1 : (lane + 1 < ncov ? jnext : q.S_b);
-    if (lane == 0) {
-      a.head_max[bh] = m;
-      a.head_Z[bh] = Z;
-    }
-  }
-
-  grid_barrier(bar_count, bar_gen, a.err);
+  grid_wait(bar_gen, gen1, a.err);
 
   // ======================= phase B1: this CTA's draws =======================
   __shared__ long long carry_s[GM * 8];   // per head: mass prefix at the current segment's start
@@ -714,31 +606,87 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     ++piece_no;
     if (bad) return;   // uniform over the CTA
     const int64_t bh0 = (int64_t)p.b * a.H + (int64_t)p.hg * GW;   // first head of the group
-    if (tid == 0) pool_used = 0;
+    __shared__ int cov_s[2];   // the CTAs covering the piece's (sequence, KV-head group)
+    if (tid == 0) {
+      pool_used = 0;
+      cov_s[0] = (int)(((p.ubase + 1) * P - 1) / n_units);
+      cov_s[1] = (int)(((p.ubase + p.units_b) * P - 1) / n_units);
+    }
     __syncthreads();
 
-    // ---- per head (groups of lph lanes, all heads at once): this CTA's
-    //      interval and its thresholds
+    // ---- per head (groups of lph lanes, all heads at once): from the
+    //      aggregates of the CTAs covering the piece's (sequence, KV-head
+    //      group), the reference exponent E*, the head max m*, the total mass Z, this CTA's mass prefix
+    //      P_own and mass T_own, and its threshold range [count(P_own),
+    //      count(P_own + T_own)).  Every covering CTA computes the same
+    //      integers in the same way, so the intervals tile [0, Z) exactly.
     if (warp_on) {
       const int h = p.hg * GW + hl;
       const int64_t bh = bh0 + hl;
-      const int64_t o = bh * MAX_CTAS + cta;
-      const long long P_own = a.bnd_P[o], T_own = a.bnd_T[o], Z = a.head_Z[bh];
-      int jlo = a.bnd_jlo[o], jhi = a.bnd_jhi[o];
-      const float mstar = a.head_max[bh];
-      HeadGeom q;
+      HeadGeom q;   // first: independent of the aggregates, overlaps their loads
       q.b = p.b;
       q.h = h;
       q.S_b = S_b;
       q.rcp = a.rcp_S[p.b];
       q.ksys = a.variant == VAR_SYS ? philox4x32_10(make_uint4(0u, (uint32_t)h, (uint32_t)p.b, a.step), k0, k1).x >> 8
                                     : 0u;
+      const int i_first = cov_s[0], i_last = cov_s[1];
+      const Agg* ag = agg + bh * MAX_CTAS;
+      constexpr int KR = 10;   // aggregates a lane keeps in registers (10 x 16 lanes covers every grid)
+      int ek[KR];
+      long long Fk[KR];
+      int emax = AGG_EMPTY;
+      float mloc = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < KR; ++k) {
+        const int i = i_first + r + k * lph;
+        Agg x;
+        x.m = -INFINITY;
+        x.e = AGG_EMPTY;
+        x.F = 0;
+        if (i <= i_last && nonempty(i)) x = ag[i];
+        ek[k] = x.e;
+        Fk[k] = x.F;
+        emax = max(emax, x.e);
+        mloc = fmaxf(mloc, x.m);
+      }
+      for (int i = i_first + r + KR * lph; i <= i_last; i += lph)
+        if (nonempty(i)) {
+          emax = max(emax, ag[i].e);
+          mloc = fmaxf(mloc, ag[i].m);
+        }
+      for (int o = lph >> 1; o > 0; o >>= 1) emax = max(emax, __shfl_xor_sync(FULL, emax, o, lph));
+      const float mstar = grp_max(mloc, lph);
+      long long before = 0, Z = 0, T_own = 0;
+      auto add = [&](int i, int e, long long F) {
+        const int d = emax - e;
+        const long long Ti = d < 63 ? (F >> d) : 0;
+        Z += Ti;
+        before += i < cta ? Ti : 0;
+        T_own += i == cta ? Ti : 0;
+      };
+#pragma unroll
+      for (int k = 0; k < KR; ++k) add(i_first + r + k * lph, ek[k], Fk[k]);
+      for (int i = i_first + r + KR * lph; i <= i_last; i += lph)
+        if (nonempty(i)) add(i, ag[i].e, ag[i].F);
+      for (int o = lph >> 1; o > 0; o >>= 1) {
+        Z += __shfl_xor_sync(FULL, Z, o, lph);
+        before += __shfl_xor_sync(FULL, before, o, lph);
+        T_own += __shfl_xor_sync(FULL, T_own, o, lph);
+      }
+      const long long P_own = before;
+      if (cta == i_first && r == 0 && hv) a.head_max[bh] = mstar;
       const Draws dr = make_draws(q, bh, Z);
+      int jlo, jhi;
       if (a.variant == VAR_IID) {
         int rounds = 1;
         for (int span = S_b; span > 1; span = (span + lph - 1) / lph) ++rounds;
         jlo = dr.count_below(P_own, r, lph, lane, rounds);
         jhi = dr.count_below(P_own + T_own, r, lph, lane, rounds);
+      } else {   // lane 0 of the group counts below P_own, lane 1 below P_own + T_own
+        const int c = dr.count_below((r & 1) ? P_own + T_own : P_own, 0, lph, lane, 0);
+        jlo = __shfl_sync(FULL, c, 0, lph);
+        jhi = __shfl_sync(FULL, c, 1, lph);
       }
       const int nt = jhi - jlo;
       int toff = -1;
@@ -755,17 +703,25 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
         hinfo[hl].jlo = jlo;
         hinfo[hl].jhi = jhi;
         hinfo[hl].off = toff;
-        hinfo[hl].mstar = mstar;
+        hinfo[hl].ref = (float)emax;
         carry_s[hl] = P_own;
       }
     }
+    float acc[HPW][CPL];   // this warp's heads' sums of count x V (output columns of the lane)
+#pragma unroll
+    for (int j = 0; j < HPW; ++j)
+#pragma unroll
+      for (int k = 0; k < CPL; ++k) acc[j][k] = 0.f;
     const int nseg = seg_count(p);
     for (int sg_i = 0; sg_i < nseg; ++sg_i) {
       const Seg g = seg_of(p, sg_i);
       if (!(first && sg_i == 0)) stage(p, g);   // the first piece's first segment was staged at the first barrier
-      if (tid == 0) n_items = 0;
+      if (tid == 0) {
+        n_items = 0;
+        n_ent = 0;
+      }
       cp_async_wait_all();
-      __syncthreads();   // staged data, cleared table, thresholds and head state visible
+      __syncthreads();   // staged data, thresholds and head state visible
 
       // ---- per head: the segment's chunk prefixes (from the running carry),
       //      first threshold of each chunk, and the chunks that hold thresholds
@@ -791,7 +747,7 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
         long long run = carry_s[hl];
         for (int c0 = 0; c0 < g.nch; c0 += lph) {
           const int c = c0 + r;
-          const long long Wc = c < g.nch ? fixed40(fast_exp(mx[c] - hi.mstar) * sm[c]) : 0;
+          const long long Wc = c < g.nch ? fixed40(fast_exp2(fmaf(mx[c], LOG2E, -hi.ref)) * sm[c]) : 0;
           const long long ci = grp_scan(Wc, r, lph);
           const long long pref = run + ci - Wc;
           if (c < g.nch && hv) {
@@ -821,8 +777,9 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
       // ---- per (head, 16-key chunk) holding thresholds, one half-warp each:
       //      exact key-mass prefix over the chunk, one ballot per threshold
       //      (the key is the first with F > x; a threshold at or beyond the
-      //      chunk's key total goes to its last nonzero key); counts into the
-      //      (KV head, key) table, the union of the group's draws.
+      //      chunk's key total goes to its last nonzero key); each drawn
+      //      (head, key) pair and its count go to the segment's list, and its
+      //      V row is started towards L2.
       const int h16 = lane >> 4, l16 = lane & 15, hb = h16 * 16;
       const int nwork = n_items;
       for (int q0 = warp * 2; q0 < nwork; q0 += SB_WARPS * 2) {
@@ -840,7 +797,7 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
         float sv = -INFINITY;
         if (nthr > 0 && key < p.nk)
           sv = g.st[qh * g.cap_st + (int)((bh * a.nk_max + g.key_lo) & 3) + (int)(key - g.key_lo)];
-        long long F = fixed40(fast_exp(sv - hi.mstar));   // e^{-inf} = 0 past the sequence end
+        long long F = fixed40(fast_exp2(fmaf(sv, LOG2E, -hi.ref)));   // 2^-inf = 0 past the sequence end
         const unsigned nzb = (__ballot_sync(FULL, F > 0) >> hb) & 0xffffu;
         const int lastnz = nzb ? 31 - __clz(nzb) : 0;
 #pragma unroll
@@ -861,119 +818,88 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
             if (a.sample_idx) a.sample_idx[bh * a.S_max + j0 + t] = (int)key;
           }
         }
-        if (cnt > 0) {
-          atomicAdd(&g.table[((qh / G) * g.nkeys + (int)(key - g.key_lo)) * GM + qh % G], cnt);
-          // the gather reads this row once the table is complete: start it towards L2 now
-          const T* vrow = reinterpret_cast<const T*>(a.V) + ((p.row0 + key) * a.Hkv + p.hg * W + qh / G) * (int64_t)D;
+        const unsigned dm = __ballot_sync(FULL, cnt > 0);
+        if (dm) {   // warp-uniform: one list slot per drawn (head, key)
+          int base = 0;
+          if (lane == __ffs(dm) - 1) base = atomicAdd(&n_ent, __popc(dm));
+          base = __shfl_sync(FULL, base, __ffs(dm) - 1);
+          if (cnt > 0) {
+            g.ent[base + __popc(dm & ((1u << lane) - 1u))] =
+                ((uint32_t)(key - g.key_lo) << 19) | ((uint32_t)qh << 13) | (uint32_t)cnt;
+            const T* vrow = reinterpret_cast<const T*>(a.V) + ((p.row0 + key) * a.Hkv + p.hg * W + qh / G) * (int64_t)D;
 #pragma unroll
-          for (int ln = 0; ln < (D * 2 + 127) / 128; ++ln)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(vrow + ln * 64));
+            for (int ln = 0; ln < (D * 2 + 127) / 128; ++ln)
+              asm volatile("prefetch.global.L2 [%0];" ::"l"(vrow + ln * 64));
+          }
         }
       }
-      __syncthreads();   // the count table is complete
+      __syncthreads();   // the list is complete
 
-      // ---- gather by KV head: warp w takes KV head w % W and every
-      //      (16 / W)-th 32-key block of the segment; each drawn V row is read
-      //      once for all heads of its group, lane l owns output columns
-      //      [l CPL, (l + 1) CPL) of every head, and the warp's sums, times
-      //      1/S_b, go into out with vectorised fp32 reductions (their order
-      //      across warps and CTAs is not fixed).
+      // ---- gather: warp w sums the listed pairs of its heads (w, w + 16,
+      //      ...), four V rows in flight; lane l owns output columns
+      //      [l CPL, (l + 1) CPL), the sums stay in registers for the piece
       {
-        const int wk = warp % W, part = warp / W, nparts = SB_WARPS / W;
-        constexpr int CPL = D / 32;   // output columns per lane
-        float acc[GM][CPL];
-#pragma unroll
-        for (int gg = 0; gg < GM; ++gg)
-#pragma unroll
-          for (int c = 0; c < CPL; ++c) acc[gg][c] = 0.f;
-        const int* tab = g.table + (size_t)wk * g.nkeys * GM;
-        const T* Vk = reinterpret_cast<const T*>(a.V) + (p.row0 * a.Hkv + p.hg * W + wk) * (int64_t)D + lane * CPL;
-        bool any_rows = false;
-        int nmine = 0;
-        int rk_l = -1;   // lane l holds the l-th listed row of this warp
-        int rc_l[GM];
-#pragma unroll
-        for (int gg = 0; gg < GM; ++gg) rc_l[gg] = 0;
-        auto gather_batch = [&](int n) {   // rows held by lanes 0..n-1, four loads in flight
-          for (int r0 = 0; r0 < n; r0 += 4) {
+        const int ne = n_ent;
+        const T* Vb = reinterpret_cast<const T*>(a.V) + (p.row0 + g.key_lo) * a.Hkv * D + (int64_t)p.hg * W * D +
+                      lane * CPL;
+        for (int e0 = 0; e0 < ne; e0 += 32) {
+          const uint32_t ev = e0 + lane < ne ? g.ent[e0 + lane] : 0u;
+          unsigned mine = __ballot_sync(FULL, e0 + lane < ne && (int)((ev >> 13) & 63u) % SB_WARPS == warp);
+          while (mine) {   // warp-uniform
+            uint32_t eu[4];
             uint2 raw[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const int kr = __shfl_sync(FULL, rk_l, (r0 + u) & 31);
+              const int src = mine ? __ffs(mine) - 1 : 0;
+              eu[u] = mine ? __shfl_sync(FULL, ev, src) : 0u;
+              mine &= mine - 1;
               raw[u] = make_uint2(0u, 0u);
-              if (r0 + u < n) {
-                const T* src = Vk + (g.key_lo + kr) * a.Hkv * D;
-                if constexpr (CPL == 4) raw[u] = *reinterpret_cast<const uint2*>(src);
-                else raw[u].x = *reinterpret_cast<const uint32_t*>(src);
+              if (eu[u] & 8191u) {   // a count of zero marks an empty slot
+                const T* srow = Vb + ((int64_t)(eu[u] >> 19) * a.Hkv + (int)((eu[u] >> 13) & 63u) / G) * D;
+                if constexpr (CPL == 4) raw[u] = *reinterpret_cast<const uint2*>(srow);
+                else raw[u].x = *reinterpret_cast<const uint32_t*>(srow);
               }
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              if (r0 + u < n) {   // warp-uniform
+              if (eu[u] & 8191u) {   // warp-uniform
+                const int jj = (int)((eu[u] >> 13) & 63u) / SB_WARPS;
+                const float c = (float)(eu[u] & 8191u);
                 f2x pr[4];
                 Pairs<T>::get(make_uint4(raw[u].x, raw[u].y, 0u, 0u), pr);
                 const float2 p0 = unpack2(pr[0]), p1 = unpack2(pr[1]);
                 const float vf[4] = {p0.x, p0.y, p1.x, p1.y};
 #pragma unroll
-                for (int gg = 0; gg < GM; ++gg) {
-                  const float cw = (float)__shfl_sync(FULL, rc_l[gg], (r0 + u) & 31);
+                for (int j = 0; j < HPW; ++j)
+                  if (j == jj)
 #pragma unroll
-                  for (int c = 0; c < CPL; ++c) acc[gg][c] = fmaf(cw, vf[c], acc[gg][c]);
-                }
+                    for (int k = 0; k < CPL; ++k) acc[j][k] = fmaf(c, vf[k], acc[j][k]);
               }
-            }
-          }
-        };
-        for (int k0b = part * 32; k0b < g.nkeys; k0b += 32 * nparts) {
-          const int kr = k0b + lane;
-          int cg[GM];
-          bool drawn_here = false;
-#pragma unroll
-          for (int gg = 0; gg < GM; ++gg) {
-            cg[gg] = (kr < g.nkeys && gg < G) ? tab[kr * GM + gg] : 0;
-            drawn_here |= cg[gg] != 0;
-          }
-          const unsigned mine = __ballot_sync(FULL, drawn_here);
-          const int add = __popc(mine);
-          if (nmine + add > 32) {
-            gather_batch(nmine);
-            any_rows = any_rows || nmine > 0;
-            nmine = 0;
-          }
-          for (int t = 0; t < add; ++t) {   // lane nmine + t receives the t-th row of this block
-            const int src_lane = (int)__fns(mine, 0, t + 1);
-            const int krow = __shfl_sync(FULL, kr, src_lane);
-            int cgs[GM];
-#pragma unroll
-            for (int gg = 0; gg < GM; ++gg) cgs[gg] = __shfl_sync(FULL, cg[gg], src_lane);
-            if (lane == nmine + t) {
-              rk_l = krow;
-#pragma unroll
-              for (int gg = 0; gg < GM; ++gg) rc_l[gg] = cgs[gg];
-            }
-          }
-          nmine += add;
-        }
-        if (nmine > 0) {
-          gather_batch(nmine);
-          any_rows = true;
-        }
-        if (any_rows) {   // warp-uniform
-          const float inv_S = 1.0f / (float)S_b;
-          float* outp = a.out + (bh0 + (int64_t)wk * G) * D + lane * CPL;
-#pragma unroll
-          for (int gg = 0; gg < GM; ++gg) {
-            if (gg < G) {
-              if constexpr (CPL == 4)
-                red_add_v4(outp + (int64_t)gg * D,
-                           make_float4(acc[gg][0] * inv_S, acc[gg][1] * inv_S, acc[gg][2] * inv_S, acc[gg][3] * inv_S));
-              else
-                red_add_v2(outp + (int64_t)gg * D, make_float2(acc[gg][0] * inv_S, acc[gg][1] * inv_S));
             }
           }
         }
       }
       __syncthreads();   // the segment's buffers are free for the next one
+    }
+
+    // ---- the piece's sums, times 1/S_b, into out (vectorised fp32
+    //      reductions, their order across CTAs not fixed)
+    {
+      const float inv_S = 1.0f / (float)S_b;
+#pragma unroll
+      for (int j = 0; j < HPW; ++j) {
+        const int hl2 = warp + j * SB_WARPS;
+        bool nz = false;
+#pragma unroll
+        for (int k = 0; k < CPL; ++k) nz |= acc[j][k] != 0.f;
+        if (hl2 < GW && nz) {
+          float* o = a.out + (bh0 + hl2) * D + lane * CPL;
+          if constexpr (CPL == 4)
+            red_add_v4(o, make_float4(acc[j][0] * inv_S, acc[j][1] * inv_S, acc[j][2] * inv_S, acc[j][3] * inv_S));
+          else
+            red_add_v2(o, make_float2(acc[j][0] * inv_S, acc[j][1] * inv_S));
+        }
+      }
     }
   });
   cp_async_wait_all();   // no copy outlives the CTA (a staged piece that was skipped)
@@ -986,10 +912,10 @@ template <typename T, int D, int GM>
 static cudaError_t launch_fused_g(const LaunchArgs& a, unsigned* bar_count, unsigned* bar_gen) {
   using Gm = StreamGeom<T, D>;
   static_assert((size_t)GM * 8 * sizeof(HeadInfo) + (size_t)POOL_CAP * 8 +
-                        (size_t)64 * (8 + 16 + 4 * SUB) * 2 + (size_t)8 * SUB * GM * 4 * 2 + 64 * 84 + 96 <=
+                        (size_t)64 * (8 + 16 + 4 * SUB) * 2 + (size_t)64 * SUB * 4 * 2 + 64 * 84 + 128 <=
                     Gm::SMEM,
                 "phase B fixed regions and a two-chunk segment fit the ring");
-  const int W = unit_heads(a.Hkv);
+  const int W = a.W;
   const int unit_rows = SB_UNIT_ROWS_X_W / W;
   const long long units = (long long)a.B * ((a.nk_max + unit_rows - 1) / unit_rows) * (a.Hkv / W);
   const int grid = (int)std::min<long long>(std::min<long long>(units, (long long)a.num_sms), (long long)MAX_CTAS);
@@ -1015,7 +941,12 @@ static cudaError_t launch_fused_t(const LaunchArgs& a, unsigned* bar_count, unsi
                             : launch_fused_g<T, D, 8>(a, bar_count, bar_gen);
 }
 
-cudaError_t launch_fused(const LaunchArgs& a, unsigned* bar_count, unsigned* bar_gen) {
+cudaError_t launch_fused(const LaunchArgs& a_in, unsigned* bar_count, unsigned* bar_gen) {
+  LaunchArgs a = a_in;
+  // W = the largest power of two <= 8 dividing H_kv: units of 32 keys x W KV
+  // heads (measured against W = 1, 2, 4 on 8K-128K contexts and batched
+  // workloads, this was the fastest or within 1% except at 8K)
+  a.W = unit_heads(a.Hkv);
   switch (a.dtype * 2 + (a.D == 128)) {
     case 0: return launch_fused_t<bf16_t, 64>(a, bar_count, bar_gen);
     case 1: return launch_fused_t<bf16_t, 128>(a, bar_count, bar_gen);

@@ -15,6 +15,7 @@ struct LaunchArgs {
   int dtype;       // 0 bf16, 1 fp16, 2 fp32
   int D;           // head_dim (64 or 128)
   int B, H, Hkv;
+  int W;           // single-launch decode: KV heads per work unit (chosen by launch_fused)
   int64_t nk_max;
   int chunks_max;  // santa: ceil(nk_max / SUB) statistics chunks; dense: ceil(nk_max / DCHUNK)
   int groups_max;  // santa: ceil(ceil(nk_max / WIN) / SPC) sampler CTAs per (b, kv head)
@@ -44,15 +45,9 @@ struct LaunchArgs {
   float* head_max;         // [B, H]
   float* part_o;           // dense: [B, H, chunks_max, D] chunk partial outputs
   // single-launch decode
-  float* agg_m;            // [B, H, MAX_CTAS] per-CTA max of s_n over the CTA's keys
-  float* agg_l;            // [B, H, MAX_CTAS] per-CTA sum of exp(s_n - agg_m)
+  void* agg;               // [B, H, MAX_CTAS] per-CTA aggregates (16 bytes each, see santa_fused.cu)
   uint32_t* ukeys;         // [B, H, S_max] sorted 24-bit uniform keys (i.i.d.)
   unsigned long long* rcp_S;  // [B] ceil(2^64 / S_b)
-  long long* bnd_P;        // [B, H, MAX_CTAS] mass prefix of each CTA's key range
-  long long* bnd_T;        // [B, H, MAX_CTAS] mass of each CTA's key range
-  int32_t* bnd_jlo;        // [B, H, MAX_CTAS] first threshold of each CTA's range
-  int32_t* bnd_jhi;        // [B, H, MAX_CTAS] end of each CTA's threshold range
-  long long* head_Z;       // [B, H] total mass
   cudaStream_t stream;
 };
 
