@@ -560,12 +560,16 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     return dr;
   };
   // first barrier; while waiting, this CTA stages its first piece's chunk
-  // statistics and scores (its own data, already written)
+  // statistics and scores (its own data, already written) and sets up what
+  // its first piece needs that does not depend on other CTAs
   __syncthreads();
   const unsigned gen1 = grid_arrive(bar_count, bar_gen);
   bool prestaged = false;
   __shared__ int pre_S0;
   __shared__ bool pre_bad0;
+  __shared__ int cov_s[2];                    // the CTAs covering the piece's (sequence, KV-head group)
+  __shared__ unsigned long long pre_rcp;     // first piece: ceil(2^64 / S_b)
+  __shared__ uint32_t pre_ksys[GM * 8];      // first piece, systematic: each head's uniform key
   if (start[3] > 0) {
     UnitCursor c0;
     c0.kv_offsets = a.kv_offsets;
@@ -585,7 +589,17 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     p0.nk = c0.nk;
     stage(p0, seg_of(p0, 0));
     prestaged = true;
-    if (tid == 0) pre_bad0 = seq_error(a, p0.b, pre_S0) != 0;
+    if (tid == 0) {
+      int S0;
+      pre_bad0 = seq_error(a, p0.b, S0) != 0;
+      pre_S0 = S0;
+      pre_rcp = (!pre_bad0 && S0 > 1) ? ~0ull / (unsigned)S0 + 1ull : 0ull;
+      const long long ubase = range[1] - c0.kb;   // unit (b, hg, kb = 0)
+      cov_s[0] = (int)(((ubase + 1) * P - 1) / range[0]);
+      cov_s[1] = (int)(((ubase + c0.units_b) * P - 1) / range[0]);
+    }
+    if (a.variant == VAR_SYS && tid < GW)
+      pre_ksys[tid] = philox4x32_10(make_uint4(0u, (uint32_t)(p0.hg * GW + tid), (uint32_t)p0.b, a.step), k0, k1).x >> 8;
   }
   grid_wait(bar_gen, gen1, a.err);
 
@@ -606,11 +620,12 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     ++piece_no;
     if (bad) return;   // uniform over the CTA
     const int64_t bh0 = (int64_t)p.b * a.H + (int64_t)p.hg * GW;   // first head of the group
-    __shared__ int cov_s[2];   // the CTAs covering the piece's (sequence, KV-head group)
     if (tid == 0) {
       pool_used = 0;
-      cov_s[0] = (int)(((p.ubase + 1) * P - 1) / n_units);
-      cov_s[1] = (int)(((p.ubase + p.units_b) * P - 1) / n_units);
+      if (!first) {
+        cov_s[0] = (int)(((p.ubase + 1) * P - 1) / n_units);
+        cov_s[1] = (int)(((p.ubase + p.units_b) * P - 1) / n_units);
+      }
     }
     __syncthreads();
 
@@ -627,9 +642,10 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
       q.b = p.b;
       q.h = h;
       q.S_b = S_b;
-      q.rcp = a.rcp_S[p.b];
-      q.ksys = a.variant == VAR_SYS ? philox4x32_10(make_uint4(0u, (uint32_t)h, (uint32_t)p.b, a.step), k0, k1).x >> 8
-                                    : 0u;
+      q.rcp = first ? pre_rcp : a.rcp_S[p.b];
+      q.ksys = a.variant != VAR_SYS ? 0u
+               : first ? pre_ksys[hl]
+                       : philox4x32_10(make_uint4(0u, (uint32_t)h, (uint32_t)p.b, a.step), k0, k1).x >> 8;
       const int i_first = cov_s[0], i_last = cov_s[1];
       const Agg* ag = agg + bh * MAX_CTAS;
       constexpr int KR = 10;   // aggregates a lane keeps in registers (10 x 16 lanes covers every grid)
@@ -683,8 +699,30 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
         for (int span = S_b; span > 1; span = (span + lph - 1) / lph) ++rounds;
         jlo = dr.count_below(P_own, r, lph, lane, rounds);
         jhi = dr.count_below(P_own + T_own, r, lph, lane, rounds);
-      } else {   // lane 0 of the group counts below P_own, lane 1 below P_own + T_own
-        const int c = dr.count_below((r & 1) ? P_own + T_own : P_own, 0, lph, lane, 0);
+      } else {
+        // even lanes of the group count the thresholds below P_own, odd
+        // lanes those below P_own + T_own.  theta_j lies in
+        // [floor(j Z / S), floor((j + 1) Z / S)], so the count is within 2 of
+        // e = trunc(X S / Z): the lanes test the window [e - w, e + w) at once
+        // (w = lph / 4 >= 2); the serial search covers a missed window.
+        const long long X = (r & 1) ? P_own + T_own : P_own;
+        const int w = lph >> 2;
+        int e = 0;
+        if (X >= Z) e = S_b;
+        else if (X > 0) {
+          const int sh = max(0, 40 - __clzll(Z));
+          e = (int)(__fdividef((float)(uint32_t)(X >> sh), (float)(uint32_t)(Z >> sh)) * (float)S_b);
+          e = min(max(e, 0), S_b);
+        }
+        const int j = e - w + (r >> 1);
+        const bool below = X > 0 && (X >= Z ? j < S_b : (j < 0 || (j < S_b && dr.theta(j) < X)));
+        const unsigned gbits = lph == 32 ? 0xffffffffu : ((1u << lph) - 1u);
+        const unsigned par = (r & 1) ? 0xaaaaaaaau : 0x55555555u;
+        const unsigned bal = (__ballot_sync(FULL, below) >> (lane - r)) & gbits & par;
+        int c = X <= 0 ? 0 : X >= Z ? S_b : e - w + __popc(bal);
+        const int last = lph - 2 + (r & 1);   // the lane testing j = e + w - 1
+        const bool miss = X > 0 && X < Z && (!((bal >> (r & 1)) & 1u) && e - w >= 0 || ((bal >> last) & 1u));
+        if (miss) c = dr.count_below(X, 0, lph, lane, 0);
         jlo = __shfl_sync(FULL, c, 0, lph);
         jhi = __shfl_sync(FULL, c, 1, lph);
       }
