@@ -5,7 +5,8 @@ CPU-baseline leg are the only users; the product path never imports this
 package.  It shares no code with the CUDA library: the arithmetic lives in
 ``santa_oracle.c`` (plain float64 C, built with gcc) and ``analysis.py``
 (closed forms in numpy).  Both follow "Stochastic Sparse Attention for
-Memory-Bound Inference" (Sec. 2, Eq. 1 and 4; Sec. 2.1; App. A; App. M).
+Memory-Bound Inference" (Sec. 2, Eq. 1 and 4; Sec. 2.1; App. A; App. M; the
+tile samplers S2ANTA-prop, App. O, and S2ANTA-flash, App. P).
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (worked example, library routines, closed forms, invariants, Philox against
@@ -29,6 +30,7 @@ _lib = None
 
 DTYPE_CODE = {"bf16": 0, "fp16": 1, "fp32": 2}
 VARIANT_CODE = {"iid": 0, "stratified": 1, "systematic": 2}
+SAMPLER_CODE = {"prop": 0, "flash": 1}
 
 
 def build(force: bool = False) -> str:
@@ -81,8 +83,12 @@ def _load():
             lib.santa_oracle_gather.argtypes = [P, i32, i32, i32, vp, vp]
             lib.santa_oracle_decode.argtypes = [P, i32, i32, vp, i32, u64, u32, vp, vp, vp, i32]
             lib.santa_oracle_dense.argtypes = [P, vp, i32]
+            lib.santa_oracle_prop_budgets.argtypes = [i32, vp, i32, vp]
+            lib.santa_oracle_tiled_head.argtypes = [P, i32, i32, i32, i32, i32, u64, u32, vp, vp, vp, vp, vp]
+            lib.santa_oracle_tiled_decode.argtypes = [P, i32, i32, vp, i32, u64, u32, vp, i32]
             for fn in ("santa_oracle_scores", "santa_oracle_tile_stats", "santa_oracle_sample_head",
-                       "santa_oracle_dense_head", "santa_oracle_gather", "santa_oracle_decode", "santa_oracle_dense"):
+                       "santa_oracle_dense_head", "santa_oracle_gather", "santa_oracle_decode", "santa_oracle_dense",
+                       "santa_oracle_prop_budgets", "santa_oracle_tiled_head", "santa_oracle_tiled_decode"):
                 getattr(lib, fn).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -211,3 +217,44 @@ def dense(P: Problem, n_threads: int = 0) -> np.ndarray:
 def decode_head(P: Problem, variant: str, S: int, seed: int, b: int, h: int, step: int = 0):
     """One head of a decode step (for sampled checks at full size)."""
     return sample_head(P, b, h, thresholds(variant, S, seed, b, h, step))
+
+
+def prop_budgets(W, S: int) -> np.ndarray:
+    """Largest-remainder budgets of App. O, Alg. 4 for tile masses W."""
+    W = np.ascontiguousarray(W, dtype=np.float64)
+    St = np.zeros(W.shape[0], np.int32)
+    if _load().santa_oracle_prop_budgets(W.shape[0], _ptr(W), S, _ptr(St)):
+        raise ValueError("oracle prop budgets: bad arguments")
+    return St
+
+
+def tiled_head(P: Problem, b: int, h: int, sampler: str, S: int, tile_len: int, seed: int, step: int = 0,
+               a0=None):
+    """One head through S2ANTA-prop or S2ANTA-flash.
+
+    Returns (estimate [d], counts [nk_b], delta [nk_b], budgets [T])."""
+    nk = P.nk(b)
+    T = -(-nk // tile_len)
+    a = None if a0 is None else np.ascontiguousarray(a0, dtype=np.float64)
+    if a is not None and a.shape[0] < T:
+        raise ValueError("a0 needs one offset per tile")
+    est = np.zeros(P.shape[3], np.float64)
+    counts = np.zeros(nk, np.int32)
+    delta = np.zeros(nk, np.float64)
+    St = np.zeros(T, np.int32)
+    if _load().santa_oracle_tiled_head(ctypes.byref(P.c), b, h, SAMPLER_CODE[sampler], S, tile_len, seed, step,
+                                       _ptr(a), _ptr(est), _ptr(counts), _ptr(delta), _ptr(St)):
+        raise ValueError("oracle tiled head: bad arguments")
+    return est, counts, delta, St
+
+
+def tiled_decode(P: Problem, sampler: str, S: int, tile_len: int, seed: int, step: int = 0, S_per_seq=None,
+                 n_threads: int = 0) -> np.ndarray:
+    """Whole step of a tile sampler: estimate [B, H, d]."""
+    B, H, _, d = P.shape
+    Sp = None if S_per_seq is None else np.ascontiguousarray(S_per_seq, dtype=np.int32)
+    est = np.zeros((B, H, d), np.float64)
+    if _load().santa_oracle_tiled_decode(ctypes.byref(P.c), SAMPLER_CODE[sampler], S, _ptr(Sp), tile_len, seed,
+                                         step, _ptr(est), n_threads):
+        raise ValueError("oracle tiled decode: bad arguments")
+    return est

@@ -285,6 +285,173 @@ int santa_oracle_dense_head(const oracle_problem* P, int32_t b, int32_t h, doubl
 }
 
 /* ------------------------------------------------------------------ */
+/* tile samplers: S2ANTA-prop (App. O, Alg. 2-5) and S2ANTA-flash       */
+/* (App. P, Alg. 6-8)                                                   */
+/* ------------------------------------------------------------------ */
+
+/* App. O, Alg. 4 lines 4-5: q_t = S W_t / Z, S_t = floor(q_t), and the
+ * S - sum_t S_t samples left over go one each to the tiles with the largest
+ * fractional parts q_t - S_t (largest remainder).  The pages do not say how
+ * equal fractional parts are ordered: the lower tile index goes first. */
+int santa_oracle_prop_budgets(int32_t T, const double* W, int32_t S, int32_t* St) {
+  if (T <= 0 || S < 0 || !W || !St) return -1;
+  double Z = 0.0;
+  for (int32_t t = 0; t < T; ++t) {
+    if (!(W[t] >= 0.0)) return -1;
+    Z += W[t];
+  }
+  if (!(Z > 0.0)) return -1;
+  double* frac = (double*)malloc(sizeof(double) * (size_t)T);
+  if (!frac) return -2;
+  int64_t given = 0;
+  for (int32_t t = 0; t < T; ++t) {
+    const double q = (double)S * W[t] / Z;
+    St[t] = (int32_t)floor(q);
+    frac[t] = q - (double)St[t];
+    given += St[t];
+  }
+  for (int64_t left = (int64_t)S - given; left > 0; --left) {
+    int32_t best = -1;
+    for (int32_t t = 0; t < T; ++t)
+      if (frac[t] >= 0.0 && (best < 0 || frac[t] > frac[best])) best = t;
+    if (best < 0) break;
+    St[best] += 1;
+    frac[best] = -1.0;   /* one extra sample per tile at most */
+  }
+  free(frac);
+  return 0;
+}
+
+/* Systematic counts inside one tile, App. O, Alg. 5 lines 5-9 (and App. P,
+ * Alg. 7 line 8): for the tile's keys in increasing order, x = inv_delta u_n,
+ * c_n = floor(a0 + p + x) - floor(a0 + p), p <- p + x.  delta_n (if not NULL)
+ * is the distance, in units of x, of the integers the key crossed to the
+ * nearer end of its interval (a0 + p, a0 + p + x]; -1 where it crossed none. */
+static void tile_counts(int64_t len, const double* u, double inv_delta, double a0, int32_t* c, double* dx) {
+  double pacc = 0.0;
+  for (int64_t n = 0; n < len; ++n) {
+    const double x = inv_delta * u[n];
+    const double lo = a0 + pacc, hi = a0 + pacc + x;
+    c[n] = (int32_t)(floor(hi) - floor(lo));
+    if (dx) {
+      dx[n] = -1.0;
+      if (c[n] > 0) {
+        const double k_first = floor(lo) + 1.0, k_last = floor(hi);
+        const double d1 = k_first - lo, d2 = hi - k_last;
+        dx[n] = d1 < d2 ? d1 : d2;
+      }
+    }
+    pacc += x;
+  }
+}
+
+/* One head through a tile sampler.
+ *   sampler 0, S2ANTA-prop: integer tile budgets S_t (Alg. 4), then the
+ *     systematic counts of Alg. 5 with inv_delta_t = S_t / l_t; est =
+ *     (1/S) sum_n c_n V_n (Alg. 2 line 5).
+ *   sampler 1, S2ANTA-flash: the same budget S_tile in every tile (Alg. 6
+ *     line 1), per-tile counts with inv_delta_t = S_tile / l_t and partial
+ *     O_t = sum_n c_n V_n (Alg. 7), merged as est = (1/Z) sum_t W_t O_t /
+ *     S_tile, W_t = exp(m_t - m*) l_t, Z = sum_t W_t (Alg. 8).
+ * Tiles are [t L, min((t + 1) L, nk)) for L = tile_len (Alg. 3 line 3); u_n =
+ * exp(s_n - m_t).  a0_t is a0[t] when a0 is not NULL, else uniform number t
+ * of head (b, h) (the pages draw a0 ~ U[0, 1) per head and tile and name no
+ * generator).  Outputs (any may be NULL): est [d]; counts [nk_b]; delta
+ * [nk_b], the counts' distance to an interval end in probability units
+ * (x units times W_t / (Z budget_t)), -1 for keys with no draw; St [T] the
+ * budgets. */
+int santa_oracle_tiled_head(const oracle_problem* P, int32_t b, int32_t h, int32_t sampler, int32_t S,
+                            int32_t tile_len, uint64_t seed, uint32_t step, const double* a0, double* est,
+                            int32_t* counts, double* delta, int32_t* St) {
+  if (check_head(P, b, h) || S <= 0 || tile_len <= 0 || (sampler != 0 && sampler != 1)) return -1;
+  const int64_t nk = nk_of(P, b);
+  if (nk <= 0) return -1;
+  const int32_t d = P->head_dim, Hkv = P->n_kv_heads;
+  const int32_t kvh = h / (P->n_q_heads / Hkv);
+  const int64_t row0 = P->kv_offsets[b];
+  const int64_t T = (nk + tile_len - 1) / tile_len;
+  double* s = (double*)malloc(sizeof(double) * (size_t)nk);
+  double* u = (double*)malloc(sizeof(double) * (size_t)nk);
+  double* dx = (double*)malloc(sizeof(double) * (size_t)nk);
+  int32_t* c = (int32_t*)malloc(sizeof(int32_t) * (size_t)nk);
+  double* m = (double*)malloc(sizeof(double) * (size_t)T);
+  double* l = (double*)malloc(sizeof(double) * (size_t)T);
+  double* W = (double*)malloc(sizeof(double) * (size_t)T);
+  int32_t* bud = (int32_t*)malloc(sizeof(int32_t) * (size_t)T);
+  double* acc = (double*)calloc((size_t)d, sizeof(double));
+  int rc = 0;
+  if (!s || !u || !dx || !c || !m || !l || !W || !bud || !acc) { rc = -2; goto done; }
+  santa_oracle_scores(P, b, h, s, NULL);
+  /* Alg. 3: tile max, exp-sum, and the stash u */
+  for (int64_t t = 0; t < T; ++t) {
+    const int64_t lo = t * tile_len, hi = (lo + tile_len < nk) ? lo + tile_len : nk;
+    double mx = s[lo];
+    for (int64_t n = lo + 1; n < hi; ++n) if (s[n] > mx) mx = s[n];
+    double sum = 0.0;
+    for (int64_t n = lo; n < hi; ++n) { u[n] = exp(s[n] - mx); sum += u[n]; }
+    m[t] = mx;
+    l[t] = sum;
+  }
+  /* global max, tile masses W_t and Z (Alg. 4 lines 2-3; Alg. 8 lines 2-3) */
+  double mstar = m[0];
+  for (int64_t t = 1; t < T; ++t) if (m[t] > mstar) mstar = m[t];
+  double Z = 0.0;
+  for (int64_t t = 0; t < T; ++t) { W[t] = exp(m[t] - mstar) * l[t]; Z += W[t]; }
+  if (sampler == 0) {
+    if (santa_oracle_prop_budgets((int32_t)T, W, S, bud)) { rc = -1; goto done; }
+  } else {
+    /* S_tile ~ S / T, rounded half up, at least one sample per tile */
+    int32_t st = (int32_t)floor((double)S / (double)T + 0.5);
+    if (st < 1) st = 1;
+    for (int64_t t = 0; t < T; ++t) bud[t] = st;
+  }
+  for (int64_t t = 0; t < T; ++t) {
+    const int64_t lo = t * tile_len, hi = (lo + tile_len < nk) ? lo + tile_len : nk;
+    const double inv_delta = bud[t] > 0 ? (double)bud[t] / l[t] : 0.0;
+    const double a = a0 ? a0[t] : santa_oracle_uniform(seed, (uint32_t)b, (uint32_t)h, step, (uint32_t)t);
+    tile_counts(hi - lo, u + lo, inv_delta, a, c + lo, dx + lo);
+    /* this tile's sum_n c_n V_n, weighted for the estimate */
+    const double wgt = sampler == 0 ? 1.0 / (double)S : (W[t] / Z) / (double)bud[t];
+    for (int64_t n = lo; n < hi; ++n) {
+      if (!c[n]) continue;
+      const int64_t base = ((row0 + n) * Hkv + kvh) * (int64_t)d;
+      for (int32_t k = 0; k < d; ++k) acc[k] += wgt * (double)c[n] * load_elem(P->dtype, P->V, base + k);
+    }
+    for (int64_t n = lo; n < hi; ++n)
+      if (dx[n] >= 0.0) dx[n] *= W[t] / (Z * (double)bud[t]);
+  }
+  if (est) memcpy(est, acc, sizeof(double) * (size_t)d);
+  if (counts) memcpy(counts, c, sizeof(int32_t) * (size_t)nk);
+  if (delta) memcpy(delta, dx, sizeof(double) * (size_t)nk);
+  if (St) memcpy(St, bud, sizeof(int32_t) * (size_t)T);
+done:
+  free(s); free(u); free(dx); free(c); free(m); free(l); free(W); free(bud); free(acc);
+  return rc;
+}
+
+/* Whole step of a tile sampler over all (b, h): est [batch, H, d].  S_per_seq
+ * (host, may be NULL) overrides S. */
+int santa_oracle_tiled_decode(const oracle_problem* P, int32_t sampler, int32_t S, const int32_t* S_per_seq,
+                              int32_t tile_len, uint64_t seed, uint32_t step, double* est, int32_t n_threads) {
+  if (!P) return -1;
+  const int32_t B = P->batch, H = P->n_q_heads, d = P->head_dim;
+  int status = 0;
+#ifdef _OPENMP
+  if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+  (void)n_threads;
+#endif
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : status)
+  for (int64_t bh = 0; bh < (int64_t)B * H; ++bh) {
+    const int32_t b = (int32_t)(bh / H), h = (int32_t)(bh % H);
+    const int32_t Sb = S_per_seq ? S_per_seq[b] : S;
+    if (santa_oracle_tiled_head(P, b, h, sampler, Sb, tile_len, seed, step, NULL, est + bh * d, NULL, NULL, NULL))
+      status |= 1;
+  }
+  return status ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------ */
 /* whole decode step                                                    */
 /* ------------------------------------------------------------------ */
 

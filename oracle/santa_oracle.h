@@ -12,6 +12,10 @@
  *   stratified / systematic . Sec. 2.1 ("Construction")
  *   inverse CDF ............. App. A.4, the indicator 1{F(j-1) <= t < F(j)}
  *   tile statistics ......... App. O, Algorithm 3 (per-tile max and exp-sum)
+ *   S2ANTA-prop ............. App. O, Algorithms 2, 4, 5 (largest-remainder
+ *                             tile budgets, per-tile systematic counts)
+ *   S2ANTA-flash ............ App. P, Algorithms 6-8 (uniform tile budgets,
+ *                             merge weighted by the tile masses)
  * The Philox4x32-10 generator follows Salmon, Moraes, Dror, Shaw, "Parallel
  * random numbers: as easy as 1, 2, 3" (SC'11); the pages name no generator.
  */
@@ -70,6 +74,23 @@ int santa_oracle_gather(const oracle_problem* P, int32_t b, int32_t h, int32_t S
 
 /* Exact attention of one head: sum_n p_n V_n. */
 int santa_oracle_dense_head(const oracle_problem* P, int32_t b, int32_t h, double* out);
+
+/* Largest-remainder integer budgets (App. O, Alg. 4): St[t] in {floor, ceil}
+ * of S W_t / Z with sum S; equal fractional parts favour the lower index. */
+int santa_oracle_prop_budgets(int32_t T, const double* W, int32_t S, int32_t* St);
+
+/* One head through a tile sampler: sampler 0 = S2ANTA-prop (App. O, Alg. 2-5),
+ * 1 = S2ANTA-flash (App. P, Alg. 6-8), tiles of tile_len keys.  a0 [T] (may be
+ * NULL: uniform number t of the head) are the per-tile offsets.  Outputs (any
+ * may be NULL): est [d]; counts [nk_b]; delta [nk_b] (probability-unit
+ * distance of a key's draws to its interval ends, -1 if none); St [T]. */
+int santa_oracle_tiled_head(const oracle_problem* P, int32_t b, int32_t h, int32_t sampler, int32_t S,
+                            int32_t tile_len, uint64_t seed, uint32_t step, const double* a0, double* est,
+                            int32_t* counts, double* delta, int32_t* St);
+
+/* Whole step of a tile sampler: est [batch, H, d]. */
+int santa_oracle_tiled_decode(const oracle_problem* P, int32_t sampler, int32_t S, const int32_t* S_per_seq,
+                              int32_t tile_len, uint64_t seed, uint32_t step, double* est, int32_t n_threads);
 
 /* Full decode step over all (b, h).  S_per_seq (host, may be NULL) overrides S.
  * est: [batch, H, d]; J / delta: [batch, H, S_stride] (entries j >= S_b get -1).

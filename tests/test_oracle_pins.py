@@ -376,3 +376,156 @@ def test_decode_layout_ragged_and_padding(oracle_lib):
             np.testing.assert_array_equal(est[b, h], e1)
             assert np.all(J[b, h, Sp[b]:] == -1)
             assert J1.max() < inp.nk_per_seq[b]
+
+
+# ---------------------------------------------------------------------------
+# tile samplers: S2ANTA-prop (App. O, Alg. 2-5) and S2ANTA-flash (App. P,
+# Alg. 6-8)
+# ---------------------------------------------------------------------------
+
+def test_prop_budgets_worked_examples(oracle_lib):
+    """Largest remainder (App. O, Alg. 4), cases worked by hand."""
+    g = json.load(open(os.path.join(HERE, "golden", "prop_budgets.json")))
+    for case in g["cases"]:
+        got = oracle_lib.prop_budgets(np.array(case["W"], np.float64), case["S"])
+        assert got.tolist() == case["budgets"], case
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_prop_budgets_brute_force(oracle_lib, seed):
+    """Among all vectors with S_t in {floor q_t, floor q_t + 1} summing to S,
+    the allocation puts the extra samples on the largest fractional parts:
+    it maximises the sum of the chosen fractional parts (searched over every
+    subset), and |S_t - q_t| < 1, sum S_t = S."""
+    import itertools
+    rng = np.random.default_rng(100 + seed)
+    T = int(rng.integers(2, 7))
+    S = int(rng.integers(1, 13))
+    W = rng.exponential(size=T) * (rng.random(T) > 0.2)
+    W[0] += 0.1
+    q = S * W / W.sum()
+    fl = np.floor(q).astype(int)
+    R = S - fl.sum()
+    fr = q - fl
+    best = max(itertools.combinations(range(T), R), key=lambda c: (sum(fr[list(c)]), [-i for i in c]))
+    want = fl.copy()
+    want[list(best)] += 1
+    got = oracle_lib.prop_budgets(W, S)
+    assert got.sum() == S and np.all(np.abs(got - q) < 1.0)
+    assert got.tolist() == want.tolist()
+
+
+def _tile_x_prefixes(P, b, h, tile_len, budgets):
+    """Per tile, the running sums of x_n = budget_t exp(s_n - m_t) / l_t (the
+    quantities of App. O, Alg. 5), from the pinned scores."""
+    s, _ = oracle_lib_scores(P, b, h)
+    out = []
+    for t in range(-(-len(s) // tile_len)):
+        st = s[t * tile_len:(t + 1) * tile_len]
+        u = np.exp(st - st.max())
+        x = budgets[t] * u / u.sum()
+        out.append(np.concatenate([[0.0], np.cumsum(x)]))
+    return out
+
+
+def oracle_lib_scores(P, b, h):
+    import oracle
+    return oracle.scores(P, b, h)
+
+
+def _offset_breakpoints(prefixes):
+    """Common offsets a0 in [0, 1) at which a0 + (a running sum) is an integer:
+    between them every tile's systematic counts are constant."""
+    pts = [np.mod(-pr, 1.0) for pr in prefixes]
+    return np.unique(np.concatenate([[0.0, 1.0]] + pts))
+
+
+@pytest.mark.parametrize("nk,tile_len,S", [(40, 16, 6), (37, 8, 11), (64, 64, 5)])
+def test_flash_exact_expectation_is_attention(oracle_lib, nk, tile_len, S):
+    """App. P, Alg. 8: with W_t / Z weights and E[c_n] = S_tile u_n / l_t, the
+    merged estimate's expectation over the tile offsets is softmax . V
+    exactly.  Integrated piece by piece over a common offset a0."""
+    rng = np.random.default_rng(nk + S)
+    P = random_problem(oracle_lib, rng, nk, 6, spread=1.0)
+    T = -(-nk // tile_len)
+    _, _, _, St = oracle_lib.tiled_head(P, 0, 0, "flash", S, tile_len, seed=0)
+    assert np.all(St == max(1, int(np.floor(S / T + 0.5))))
+    bps = _offset_breakpoints(_tile_x_prefixes(P, 0, 0, tile_len, St))
+    E = analysis.expectation_over_offset(
+        lambda a: oracle_lib.tiled_head(P, 0, 0, "flash", S, tile_len, seed=0, a0=np.full(T, a))[0], bps)
+    np.testing.assert_allclose(E, oracle_lib.dense(P)[0, 0], rtol=1e-10, atol=1e-11)
+
+
+@pytest.mark.parametrize("nk,tile_len,S", [(40, 16, 6), (37, 8, 11), (50, 10, 3)])
+def test_prop_exact_expectation_is_budget_mixture(oracle_lib, nk, tile_len, S):
+    """App. O, Alg. 2: E[c_n] = S_t u_n / l_t inside tile t, so the estimate's
+    expectation is sum_t (S_t / S) sum_n (u_n / l_t) V_n, the tile
+    distributions mixed by the integer budgets."""
+    rng = np.random.default_rng(7 * nk + S)
+    P = random_problem(oracle_lib, rng, nk, 5, spread=1.0)
+    T = -(-nk // tile_len)
+    _, _, _, St = oracle_lib.tiled_head(P, 0, 0, "prop", S, tile_len, seed=0)
+    s, _ = oracle_lib.scores(P, 0, 0)
+    V = values_of(P, 0, 0)
+    want = np.zeros(V.shape[1])
+    for t in range(T):
+        st = s[t * tile_len:(t + 1) * tile_len]
+        u = np.exp(st - st.max())
+        want += St[t] / S * (u / u.sum()) @ V[t * tile_len:(t + 1) * tile_len]
+    bps = _offset_breakpoints(_tile_x_prefixes(P, 0, 0, tile_len, St))
+    E = analysis.expectation_over_offset(
+        lambda a: oracle_lib.tiled_head(P, 0, 0, "prop", S, tile_len, seed=0, a0=np.full(T, a))[0], bps)
+    np.testing.assert_allclose(E, want, rtol=1e-10, atol=1e-11)
+
+
+def test_prop_proportional_budgets_are_unbiased_and_uniform_visits_every_key(oracle_lib):
+    """Equal tiles under uniform attention: S_t = S / T exactly, so prop is
+    unbiased; with S = nk every key is drawn exactly once whatever a0, giving
+    mean(V) = softmax . V."""
+    rng = np.random.default_rng(3)
+    nk, d, L = 64, 8, 16
+    V = rng.standard_normal((nk, 1, d)).astype(np.float32)
+    P = make_problem(oracle_lib, rng.standard_normal((1, d)), np.zeros((nk, 1, d)), V)
+    dense = oracle_lib.dense(P)[0, 0]
+    for a in (0.0, 0.3, 0.999):
+        est, counts, _, St = oracle_lib.tiled_head(P, 0, 0, "prop", nk, L, seed=0, a0=np.full(4, a))
+        assert St.tolist() == [16] * 4 and np.all(counts == 1)
+        np.testing.assert_allclose(est, dense, rtol=1e-12, atol=1e-13)
+    _, _, _, St = oracle_lib.tiled_head(P, 0, 0, "prop", 8, L, seed=0)
+    assert St.tolist() == [2] * 4
+
+
+@pytest.mark.parametrize("sampler", ["prop", "flash"])
+def test_tile_counts_sum_to_budgets(oracle_lib, sampler):
+    """Alg. 5 / Alg. 7: the counts of tile t add up to its budget (the x of
+    a tile sum to it), zero-budget tiles draw nothing."""
+    rng = np.random.default_rng(5)
+    nk, L, S = 300, 32, 17
+    P = random_problem(oracle_lib, rng, nk, 8, spread=2.5)
+    for seed in range(5):
+        _, counts, _, St = oracle_lib.tiled_head(P, 0, 0, sampler, S, L, seed=seed)
+        per_tile = np.add.reduceat(counts, np.arange(0, nk, L))
+        assert per_tile.tolist() == St.tolist()
+        if sampler == "prop":
+            assert St.sum() == S
+
+
+@pytest.mark.parametrize("S,a", [(5, 0.37), (16, 0.0), (9, 0.9)])
+def test_flash_single_tile_is_the_systematic_sampler(oracle_lib, S, a):
+    """One tile covering all keys: the count rule of Alg. 7 is systematic
+    sampling with thresholds (j + 1 - a0) / S, j = 0..S-1, read with intervals
+    open on the left; away from interval ends it draws what the pinned
+    inverse-CDF sampler draws, and the merge leaves (1/S) sum c_n V_n."""
+    rng = np.random.default_rng(S)
+    nk = 30
+    P = random_problem(oracle_lib, rng, nk, 4, spread=1.5)
+    est, counts, delta, St = oracle_lib.tiled_head(P, 0, 0, "flash", S, nk, seed=0, a0=np.array([a]))
+    assert St.tolist() == [S]
+    t = (np.arange(S) + 1.0 - a) / S
+    _, J, dl = oracle_lib.sample_head(P, 0, 0, t[t < 1.0])
+    ref = np.bincount(J, minlength=nk)
+    if a == 0.0:   # the last threshold is 1: it falls on the last key
+        ref[nk - 1] += 1
+    assert np.all(counts == ref) or np.all((counts == ref) | (delta < 1e-9) | (np.roll(delta, 1) < 1e-9)
+                                          | (np.roll(delta, -1) < 1e-9))
+    np.testing.assert_allclose(est, counts @ values_of(P, 0, 0) / S, rtol=1e-12, atol=1e-13)
