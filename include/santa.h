@@ -144,6 +144,39 @@ size_t santa_dense_workspace_size(const santa_params_t* p);
 santa_status_t santa_dense_decode(const santa_params_t* p, const void* q, const void* K, const void* V,
                                   float* out, void* workspace, size_t ws_bytes, santa_stream_t stream);
 
+/* The pages' tile samplers ("Stochastic Sparse Attention for Memory-Bound
+ * Inference", Sec. 3.2-3.3): the keys of each sequence are cut into tiles of
+ * tile_len keys, [t L, min((t + 1) L, nk_b)).
+ *   SANTA_TILE_PROP   S2ANTA-prop (App. O, Alg. 2-5): integer tile budgets
+ *                     S_t ~ S W_t / Z by largest remainder (equal fractional
+ *                     parts: the lower tile first), systematic counts inside
+ *                     each tile, out = (1/S_b) sum_n c_n V_n.
+ *   SANTA_TILE_FLASH  S2ANTA-flash (App. P, Alg. 6-8): every tile draws
+ *                     S_tile = max(1, round(S_b / T_b)) samples as if it held
+ *                     all the mass; out = (1/Z) sum_t W_t O_t / S_tile with O_t
+ *                     the tile's sum_n c_n V_n and W_t its mass.
+ * Inside tile t the count rule is the pages' c_n = floor(a0 + p + x_n) -
+ * floor(a0 + p), x_n = S_t exp(s_n - m_t) / l_t: key n takes the integers in
+ * (a0 + p, a0 + p + x_n].  a0 of tile t is uniform number t of the head in
+ * the Philox layout above (the pages name no generator).  Both run the
+ * score pass of santa_decode first.
+ *   tile_len   a multiple of SANTA_CHUNK in [SANTA_CHUNK, SANTA_MAX_TILE].
+ *   sample_idx optional device int32 [batch, n_q_heads, santa_tiled_max_draws]:
+ *              the drawn key index of every draw, tiles in order and keys
+ *              increasing inside a tile (prop: S_b draws; flash: T_b S_tile),
+ *              the rest -1.
+ * Other arguments and rules as santa_decode; the workspace must hold
+ * santa_tiled_workspace_size bytes (0 for invalid arguments).  The output is
+ * summed in a fixed order: equal inputs give equal bits. */
+#define SANTA_TILE_PROP 0
+#define SANTA_TILE_FLASH 1
+#define SANTA_MAX_TILE 1024
+size_t santa_tiled_workspace_size(const santa_params_t* p, int32_t sampler, int32_t tile_len);
+int32_t santa_tiled_max_draws(const santa_params_t* p, int32_t sampler, int32_t tile_len);
+santa_status_t santa_decode_tiled(const santa_params_t* p, int32_t sampler, int32_t tile_len, const void* q,
+                                  const void* K, const void* V, float* out, void* workspace, size_t ws_bytes,
+                                  santa_stream_t stream, int32_t* sample_idx);
+
 /* Byte offsets of the intermediate arrays inside a santa_decode workspace, for
  * inspection by tests and tools after the stream has synchronised:
  *   stash     float32 [batch, n_q_heads, nk]        scaled scores s_n

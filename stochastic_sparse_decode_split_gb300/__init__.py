@@ -28,10 +28,12 @@ from .build import LIB as _LIB_PATH
 __all__ = [
     "SantaError", "Params", "library", "santa_decode", "santa_decode_with_uniforms", "santa_dense_decode",
     "workspace_size", "dense_workspace_size", "workspace_layout", "get_error", "Decoder", "exported_symbols",
-    "VARIANTS", "DTYPES", "santa_decode_static", "static_scratch_bytes",
+    "VARIANTS", "DTYPES", "santa_decode_static", "static_scratch_bytes", "SAMPLERS", "santa_decode_tiled",
+    "tiled_workspace_size", "tiled_max_draws",
 ]
 
 VARIANTS = {"iid": 0, "stratified": 1, "systematic": 2}
+SAMPLERS = {"prop": 0, "flash": 1}   # SANTA_TILE_PROP, SANTA_TILE_FLASH
 DTYPES = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "santa.h")
 
@@ -94,13 +96,18 @@ def library():
             lib.santa_dense_decode.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
             lib.santa_decode_static.argtypes = [P, i32, vp, vp, vp, vp, vp, vp]
             lib.santa_workspace_layout.argtypes = [P, ctypes.POINTER(WsLayout)]
+            lib.santa_tiled_workspace_size.argtypes = [P, i32, i32]
+            lib.santa_tiled_workspace_size.restype = sz
+            lib.santa_tiled_max_draws.argtypes = [P, i32, i32]
+            lib.santa_tiled_max_draws.restype = i32
+            lib.santa_decode_tiled.argtypes = [P, i32, i32, vp, vp, vp, vp, vp, sz, vp, vp]
             lib.santa_get_error.argtypes = [vp, vp, ctypes.POINTER(i32)]
             lib.santa_status_string.argtypes = [i32]
             lib.santa_status_string.restype = ctypes.c_char_p
             lib.santa_version.restype = i32
             for fn in ("santa_workspace_init", "santa_decode", "santa_decode_profiled", "santa_score_pass",
                        "santa_decode_with_uniforms", "santa_dense_decode", "santa_decode_static",
-                       "santa_workspace_layout", "santa_get_error"):
+                       "santa_workspace_layout", "santa_get_error", "santa_decode_tiled"):
                 getattr(lib, fn).restype = i32
             _lib = lib
     return _lib
@@ -224,6 +231,36 @@ def santa_decode_with_uniforms(q, K, V, uniforms, S: int, variant: str, out=None
                                               _stream(stream), _ptr(sample_idx))
     if st != SANTA_OK:
         raise SantaError(st, "santa_decode_with_uniforms")
+    return out
+
+
+def tiled_workspace_size(p: Params, sampler: str, tile_len: int) -> int:
+    return library().santa_tiled_workspace_size(ctypes.byref(p), SAMPLERS[sampler], tile_len)
+
+
+def tiled_max_draws(p: Params, sampler: str, tile_len: int) -> int:
+    return library().santa_tiled_max_draws(ctypes.byref(p), SAMPLERS[sampler], tile_len)
+
+
+def santa_decode_tiled(q, K, V, S: int, sampler: str = "prop", tile_len: int = 256, seed: int = 0, step: int = 0,
+                       out=None, nk: Optional[int] = None, kv_offsets=None, S_per_seq=None, scale: float = 0.0,
+                       workspace=None, sample_idx=None, stream=None) -> torch.Tensor:
+    """One decode step through S2ANTA-prop or S2ANTA-flash; returns out [B, H, d]
+    float32.  sample_idx, if given, is int32 [B, H, tiled_max_draws(...)]."""
+    _check_tensors(q, K, V, out, kv_offsets, S_per_seq, sample_idx)
+    p = make_params(q, K, S, seed, step, nk, kv_offsets, S_per_seq, scale)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        n = tiled_workspace_size(p, sampler, tile_len)
+        if n == 0:
+            raise SantaError(1, "santa_tiled_workspace_size")
+        workspace = alloc_workspace(n, q.device)
+    st = library().santa_decode_tiled(ctypes.byref(p), SAMPLERS[sampler], tile_len, _ptr(q), _ptr(K), _ptr(V),
+                                      _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream),
+                                      _ptr(sample_idx))
+    if st != SANTA_OK:
+        raise SantaError(st, "santa_decode_tiled")
     return out
 
 

@@ -2,6 +2,7 @@
 // layout and the launch sequence of one decode step.  Every check here runs
 // before any CUDA call, so argument errors never reach the device.
 #include <math.h>
+#include <stdint.h>
 #include <string.h>
 
 #include "../../include/santa.h"
@@ -10,6 +11,7 @@
 
 static_assert(SANTA_MAX_GROUP == SANTA_MAX_GROUP_DEV, "group limit");
 static_assert(SANTA_CHUNK == santa::SUB, "chunk length");
+static_assert(SANTA_MAX_TILE == santa::TL_MAX_LEN, "tile length");
 
 namespace {
 
@@ -21,6 +23,8 @@ size_t up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
 
 struct Layout {
   size_t stash, tile_max, tile_sum, prefix, thresh, jstart, head_max, part_o, agg, ukeys, rcp_S, total;
+  size_t tl_pre, tl_w, tl_o;
+  int64_t tl_T;
   int64_t chunks, groups;
 };
 
@@ -72,6 +76,36 @@ Layout santa_layout(const santa_params_t* p) {
   L.part_o = 0;
   L.total = off;
   return L;
+}
+
+// santa_layout followed by the tile samplers' arrays (tl_T = tiles of the longest sequence).
+Layout tiled_layout(const santa_params_t* p, int32_t tile_len) {
+  Layout L = santa_layout(p);
+  const size_t B = (size_t)p->batch, H = (size_t)p->n_q_heads, D = (size_t)p->head_dim;
+  L.tl_T = (p->nk + tile_len - 1) / tile_len;
+  const size_t T = (size_t)L.tl_T;
+  size_t off = L.total;
+  L.tl_pre = off; off += up(B * H * (T + 1) * sizeof(int32_t));
+  L.tl_w = off;   off += up(B * H * 2 * T * sizeof(double));
+  L.tl_o = off;   off += up(B * H * T * D * sizeof(float));
+  L.total = off;
+  return L;
+}
+
+santa_status_t check_tiled(const santa_params_t* p, int32_t sampler, int32_t tile_len) {
+  santa_status_t st = check_params(p, true);
+  if (st != SANTA_OK) return st;
+  if (sampler != SANTA_TILE_PROP && sampler != SANTA_TILE_FLASH) return SANTA_ERR_INVALID_ARG;
+  if (tile_len < SANTA_CHUNK || tile_len > SANTA_MAX_TILE || tile_len % SANTA_CHUNK) return SANTA_ERR_INVALID_ARG;
+  const int64_t T = (p->nk + tile_len - 1) / tile_len;
+  if (T * (int64_t)p->batch * p->n_kv_heads > INT32_MAX) return SANTA_ERR_UNSUPPORTED;   // one CTA per tile
+  return SANTA_OK;
+}
+
+int32_t tiled_draws(const santa_params_t* p, int32_t sampler, int32_t tile_len) {
+  const int64_t T = (p->nk + tile_len - 1) / tile_len;
+  // flash: T_b round(S_b / T_b) <= S + T_b / 2, and T_b when S_b / T_b < 1/2
+  return sampler == SANTA_TILE_PROP ? p->S : (int32_t)(p->S + T);
 }
 
 Layout dense_layout(const santa_params_t* p) {
@@ -211,6 +245,42 @@ santa_status_t santa_decode_with_uniforms(const santa_params_t* p, int32_t varia
                                           size_t ws_bytes, santa_stream_t stream, int32_t* sample_idx) {
   if (!uniforms) return SANTA_ERR_INVALID_ARG;
   return decode_impl(p, variant, q, K, V, uniforms, out, workspace, ws_bytes, stream, sample_idx);
+}
+
+size_t santa_tiled_workspace_size(const santa_params_t* p, int32_t sampler, int32_t tile_len) {
+  if (check_tiled(p, sampler, tile_len) != SANTA_OK) return 0;
+  return tiled_layout(p, tile_len).total;
+}
+
+int32_t santa_tiled_max_draws(const santa_params_t* p, int32_t sampler, int32_t tile_len) {
+  if (check_tiled(p, sampler, tile_len) != SANTA_OK) return 0;
+  return tiled_draws(p, sampler, tile_len);
+}
+
+santa_status_t santa_decode_tiled(const santa_params_t* p, int32_t sampler, int32_t tile_len, const void* q,
+                                  const void* K, const void* V, float* out, void* workspace, size_t ws_bytes,
+                                  santa_stream_t stream, int32_t* sample_idx) {
+  santa_status_t st = check_tiled(p, sampler, tile_len);
+  if (st != SANTA_OK) return st;
+  const Layout L = tiled_layout(p, tile_len);
+  st = check_buffers(q, K, V, out, workspace, ws_bytes, L.total);
+  if (st != SANTA_OK) return st;
+  if (sample_idx && !aligned(sample_idx, 4)) return SANTA_ERR_INVALID_ARG;
+  santa::LaunchArgs a = base_args(p, L, q, K, V, nullptr, workspace, (cudaStream_t)stream);
+  unsigned char* w = static_cast<unsigned char*>(workspace);
+  a.stash = reinterpret_cast<float*>(w + L.stash);
+  a.head_max = reinterpret_cast<float*>(w + L.head_max);
+  a.sample_idx = sample_idx;
+  a.tl_sampler = sampler;
+  a.tl_len = tile_len;
+  a.tl_T = (int)L.tl_T;
+  a.tl_draws = tiled_draws(p, sampler, tile_len);
+  a.tl_pre = reinterpret_cast<int32_t*>(w + L.tl_pre);
+  a.tl_w = reinterpret_cast<double*>(w + L.tl_w);
+  a.tl_o = reinterpret_cast<float*>(w + L.tl_o);
+  if (santa::launch_score(a) != cudaSuccess) return SANTA_ERR_CUDA;   // out is not touched here
+  a.out = out;
+  return santa::launch_tiled(a) == cudaSuccess ? SANTA_OK : SANTA_ERR_CUDA;
 }
 
 size_t santa_dense_workspace_size(const santa_params_t* p) {

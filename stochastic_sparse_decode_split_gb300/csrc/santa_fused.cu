@@ -37,6 +37,7 @@
 
 #include "santa_common.cuh"
 #include "santa_launch.h"
+#include "santa_seq.cuh"
 #include "santa_stream.cuh"
 #include "santa_window.cuh"
 
@@ -287,20 +288,6 @@ __device__ __forceinline__ void for_each_piece(const LaunchArgs& a, int n_hg, in
   }
 }
 
-// Sequence metadata: length within [1, nk_max] and budget within [1, S_max].
-__device__ __forceinline__ int seq_error(const LaunchArgs& a, int b, int& S_b) {
-  int err = 0;
-  int64_t nk = a.nk_max, row0 = 0;
-  if (a.kv_offsets) {
-    row0 = a.kv_offsets[b];
-    nk = a.kv_offsets[b + 1] - row0;
-  }
-  if (nk < 1) err |= ERR_EMPTY;
-  else if (nk > a.nk_max || row0 < 0) err |= ERR_NK_BOUND;
-  S_b = a.S_per_seq ? a.S_per_seq[b] : a.S_max;
-  if (S_b < 1 || S_b > a.S_max) err |= ERR_S_RANGE;
-  return err;
-}
 
 // Per-head constants of the thresholds.
 struct HeadGeom {

@@ -48,6 +48,14 @@ struct LaunchArgs {
   void* agg;               // [B, H, MAX_CTAS] per-CTA aggregates (16 bytes each, see santa_fused.cu)
   uint32_t* ukeys;         // [B, H, S_max] sorted 24-bit uniform keys (i.i.d.)
   unsigned long long* rcp_S;  // [B] ceil(2^64 / S_b)
+  // tile samplers (S2ANTA-prop / S2ANTA-flash)
+  int tl_sampler;          // 0 prop, 1 flash
+  int tl_len;              // keys per tile (a multiple of SUB, <= TL_MAX_LEN)
+  int tl_T;                // tiles of the longest sequence
+  int tl_draws;            // row length of sample_idx
+  int32_t* tl_pre;         // [B, H, tl_T + 1] prop: exclusive prefix of the tile budgets
+  double* tl_w;            // [B, H, tl_T] scratch: tile masses
+  float* tl_o;             // [B, H, tl_T, D] flash: per-tile sums of count x V
   cudaStream_t stream;
 };
 
@@ -57,5 +65,7 @@ cudaError_t launch_sample_gather(const LaunchArgs& a);
 cudaError_t launch_dense(const LaunchArgs& a);
 // The whole decode step in one cooperative launch (16-bit caches, Philox uniforms).
 cudaError_t launch_fused(const LaunchArgs& a, unsigned* bar_count, unsigned* bar_gen);
+constexpr int TL_MAX_LEN = 1024;   // longest tile of the tile samplers
+cudaError_t launch_tiled(const LaunchArgs& a);   // after launch_score
 
 }  // namespace santa
