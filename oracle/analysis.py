@@ -11,7 +11,10 @@ Attention for Memory-Bound Inference":
   the value covariance of the within-stratum distribution (App. A.5,
   Thm. A.6; App. M);
 * systematic variance by replicates (App. M) -- no closed form exists;
-* vector Bernstein tail for i.i.d. SANTA (App. B, Thm. B.1).
+* vector Bernstein tail for i.i.d. SANTA (App. B, Thm. B.1);
+* expected number of distinct keys drawn (App. L, App. M.1 item 1) and the
+  expected share of V rows a causal prefill pass reads (App. F, Table 9),
+  both for i.i.d. SANTA, where draws are independent.
 
 Strata follow Sec. 2.1: I_m = [m/S, (m+1)/S), with the inverse CDF of App. A.4.
 """
@@ -119,3 +122,30 @@ def systematic_count_bounds(p: np.ndarray, S: int):
     (lattice points of spacing 1/S in an interval of length p_n)."""
     Sp = S * np.asarray(p, np.float64)
     return np.floor(Sp), np.ceil(Sp)
+
+
+def expected_unique_keys_iid(p: np.ndarray, S: int) -> float:
+    """App. M.1 (1): E|{J_1..J_S}| for S i.i.d. draws from p, sum_n 1 - (1 - p_n)^S."""
+    p = np.asarray(p, np.float64)
+    with np.errstate(divide="ignore"):   # p_n = 1 gives log(0) = -inf: the key is always drawn
+        return float(np.sum(-np.expm1(S * np.log1p(-p))))
+
+
+def causal_softmax(q: np.ndarray, k: np.ndarray, scale: float) -> np.ndarray:
+    """Rows i of softmax(q k^T scale) over keys 0..i (a causal prefill pass), float64."""
+    s = (np.asarray(q, np.float64) @ np.asarray(k, np.float64).T) * scale
+    n = s.shape[0]
+    s[np.triu_indices(n, 1)] = -np.inf
+    s -= s.max(axis=1, keepdims=True)
+    p = np.exp(s)
+    return p / p.sum(axis=1, keepdims=True)
+
+
+def prefill_coverage_iid(P: np.ndarray, S: int) -> float:
+    """App. F, Table 9: the expected share of the nk V rows drawn by at least
+    one query of a causal prefill pass when every query i draws S i.i.d.
+    keys from its row P[i]: mean over keys j of 1 - prod_{i >= j} (1 - P_ij)^S."""
+    P = np.asarray(P, np.float64)
+    with np.errstate(divide="ignore"):   # query 0 draws key 0 with probability 1
+        log_none = S * np.log1p(-P).sum(axis=0)
+    return float(np.mean(-np.expm1(log_none)))

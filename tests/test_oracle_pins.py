@@ -529,3 +529,109 @@ def test_flash_single_tile_is_the_systematic_sampler(oracle_lib, S, a):
     assert np.all(counts == ref) or np.all((counts == ref) | (delta < 1e-9) | (np.roll(delta, 1) < 1e-9)
                                           | (np.roll(delta, -1) < 1e-9))
     np.testing.assert_allclose(est, counts @ values_of(P, 0, 0) / S, rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# synthetic measurement pins: distinct keys and prefill coverage (App. F,
+# Table 9; App. L, Table 17; App. D, Fig. 7; App. M)
+# ---------------------------------------------------------------------------
+
+def _gaussian_fp16(rng, n, d):
+    return rng.standard_normal((n, d)).astype(np.float16).astype(np.float64)
+
+
+def test_prefill_coverage_reproduces_table9(oracle_lib):
+    """App. F, Table 9: share of V rows a causal prefill pass of i.i.d. SANTA
+    reads, Gaussian fp16 Q, K, d = 128, from the exact causal softmax; within
+    0.3 percentage points of the printed means."""
+    g = json.load(open(os.path.join(HERE, "golden", "table9_prefill_coverage.json")))
+    rng = np.random.default_rng(9)
+    for col, nk in enumerate(g["nk"][:2]):
+        Ps = [analysis.causal_softmax(_gaussian_fp16(rng, nk, 128), _gaussian_fp16(rng, nk, 128), 128 ** -0.5)
+              for _ in range(3)]
+        for S in g["S"]:
+            got = 100.0 * np.mean([analysis.prefill_coverage_iid(P, S) for P in Ps])
+            want = g["percent"][str(S)][col]
+            assert abs(got - want) < 0.3, (nk, S, got, want)
+
+
+def test_prefill_coverage_closed_form_matches_the_sampler(oracle_lib):
+    """The closed form against the oracle's own i.i.d. sampler (Philox
+    uniforms, inverse CDF): union of the draws of every query of a causal pass."""
+    rng = np.random.default_rng(4)
+    nk, d, S = 192, 16, 4
+    q = rng.standard_normal((nk, d)).astype(np.float32)
+    k = rng.standard_normal((nk, d)).astype(np.float32)
+    V = rng.standard_normal((nk, 1, d)).astype(np.float32)
+    want = analysis.prefill_coverage_iid(analysis.causal_softmax(q, k, d ** -0.5), S)
+    shares = []
+    for seed in range(12):
+        seen = np.zeros(nk, bool)
+        for i in range(nk):
+            P = make_problem(oracle_lib, q[i:i + 1], k[:i + 1, None, :], V[:i + 1])
+            _, J, _ = oracle_lib.sample_head(P, 0, 0, oracle_lib.thresholds("iid", S, seed, 0, i))
+            seen[J] = True
+        shares.append(seen.mean())
+    assert abs(np.mean(shares) - want) < 4 * np.std(shares) / np.sqrt(len(shares)) + 0.01
+
+
+def test_unique_keys_iid_closed_form_matches_the_sampler(oracle_lib):
+    """App. M.1 (1): E|U| = sum_n 1 - (1 - p_n)^S for i.i.d. draws."""
+    rng = np.random.default_rng(6)
+    P = random_problem(oracle_lib, rng, 400, 16, spread=2.0)
+    _, p = oracle_lib.scores(P, 0, 0)
+    for S in (8, 64):
+        want = analysis.expected_unique_keys_iid(p, S)
+        got = [np.unique(oracle_lib.decode(P, "iid", S, seed=s)[1][0, 0]).size for s in range(200)]
+        assert abs(np.mean(got) - want) < 4 * np.std(got) / np.sqrt(len(got)) + 1e-9, (S, np.mean(got), want)
+
+
+def _decode_head_8k():
+    """One synthetic decode head of the Llama shape at 8K keys (planted keys as
+    in the benchmark inputs), as an oracle problem."""
+    import oracle
+    inp = synth.generate(synth.llama32k(8192, 256, "systematic"), 0)
+    return oracle.Problem.from_inputs(inp)
+
+
+def test_stratified_variants_draw_more_distinct_keys(oracle_lib):
+    """App. L, Table 17 (model attention there; a synthetic 8K decode head
+    here): for each S the stratified and systematic samplers touch more
+    distinct keys than i.i.d. SANTA, and fewer than S."""
+    P = _decode_head_8k()
+    rows = []
+    for S in (32, 64, 128, 256):
+        U = {}
+        for variant in ("iid", "stratified", "systematic"):
+            _, J, _ = oracle_lib.decode(P, variant, S, seed=1)
+            U[variant] = np.mean([np.unique(J[0, h]).size for h in range(J.shape[1])])
+        rows.append((S, U["iid"], U["stratified"], U["systematic"]))
+        assert U["iid"] < U["stratified"] <= S and U["iid"] < U["systematic"] <= S, (S, U)
+    print("\nS, mean distinct keys per head: i.i.d., stratified, systematic")
+    for r in rows:
+        print("  %4d  %7.1f  %7.1f  %7.1f" % r)
+
+
+def test_variance_falls_with_S_and_stratification_helps(oracle_lib):
+    """App. D, Fig. 7 (model attention there; a synthetic 8K decode head here):
+    variance traces against S -- i.i.d. closed form (slope -1 on log-log),
+    stratified closed form, systematic by replicates (App. M) -- with
+    stratified and systematic below i.i.d. at every S (Thm. A.6 for
+    stratified; empirical for systematic)."""
+    P = _decode_head_8k()
+    _, p = oracle_lib.scores(P, 0, 0)
+    V = values_of(P, 0, 0)
+    mu = p @ V
+    Ss = np.array([32, 64, 128, 256])
+    vi, vs, vy = [], [], []
+    rng = np.random.default_rng(2)
+    for S in Ss:
+        vi.append(analysis.iid_variance_trace(p, V, int(S)))
+        vs.append(analysis.stratified_variance_trace(p, V, int(S)))
+        reps = [oracle_lib.sample_head(P, 0, 0, (np.arange(S) + u) / S)[0] for u in rng.random(48)]
+        vy.append(analysis.replicate_variance_trace(np.array(reps)))
+    slope = lambda v: float(np.polyfit(np.log(Ss), np.log(v), 1)[0])
+    assert abs(slope(vi) + 1.0) < 1e-9
+    assert np.all(np.array(vs) < np.array(vi)) and np.all(np.array(vy) < np.array(vi))
+    print("\nslopes of log variance trace against log S: i.i.d. %.2f, stratified %.2f, systematic %.2f"
+          % (slope(vi), slope(vs), slope(vy)))
