@@ -84,6 +84,10 @@ def _load():
             lib.santa_oracle_decode.argtypes = [P, i32, i32, vp, i32, u64, u32, vp, vp, vp, i32]
             lib.santa_oracle_dense.argtypes = [P, vp, i32]
             lib.santa_oracle_prop_budgets.argtypes = [i32, vp, i32, vp]
+            lib.santa_oracle_store_elem.argtypes = [i32, ctypes.c_float, vp]
+            lib.santa_oracle_store_elem.restype = None
+            lib.santa_oracle_bernoulli_group.argtypes = [P, i32, i32, i32, i32, u64, u32, vp, vp]
+            lib.santa_oracle_bernoulli_group.restype = ctypes.c_int
             lib.santa_oracle_tiled_head.argtypes = [P, i32, i32, i32, i32, i32, u64, u32, vp, vp, vp, vp, vp]
             lib.santa_oracle_tiled_decode.argtypes = [P, i32, i32, vp, i32, u64, u32, vp, i32]
             for fn in ("santa_oracle_scores", "santa_oracle_tile_stats", "santa_oracle_sample_head",
@@ -258,3 +262,40 @@ def tiled_decode(P: Problem, sampler: str, S: int, tile_len: int, seed: int, ste
                                          step, _ptr(est), n_threads):
         raise ValueError("oracle tiled decode: bad arguments")
     return est
+
+
+_STORAGE = {"bf16": np.uint16, "fp16": np.uint16, "fp32": np.float32}
+
+
+def store_elem(dtype: str, x: float):
+    """fp32 x rounded to the storage dtype (bits for bf16 / fp16)."""
+    out = np.zeros(1, _STORAGE[dtype])
+    _load().santa_oracle_store_elem(DTYPE_CODE[dtype], float(x), _ptr(out))
+    return out[0]
+
+
+def bernoulli_group(P: Problem, b: int, kvh: int, nsamp: int, stratified: bool, seed: int, step: int = 0):
+    """Bernoulli qK^T, mean group query (App. C.2): (q~ [G, d] in storage
+    dtype, counts [d])."""
+    B, H, Hkv, d = P.shape
+    qt = np.zeros((H // Hkv, d), _STORAGE[P.dtype])
+    counts = np.zeros(d, np.int32)
+    if _load().santa_oracle_bernoulli_group(ctypes.byref(P.c), b, kvh, nsamp, int(stratified), seed, step,
+                                            _ptr(qt), _ptr(counts)):
+        raise ValueError("oracle bernoulli: bad arguments")
+    return qt, counts
+
+
+def bernoulli_problem(P: Problem, nsamp: int, stratified: bool, seed: int, step: int = 0):
+    """The problem with every query replaced by its Bernoulli effective query
+    (App. C.2, Eq. 13), and the per-group feature counts [B, Hkv, d]."""
+    B, H, Hkv, d = P.shape
+    G = H // Hkv
+    q = np.array(P.q, copy=True)
+    counts = np.zeros((B, Hkv, d), np.int32)
+    for b in range(B):
+        for k in range(Hkv):
+            qt, c = bernoulli_group(P, b, k, nsamp, stratified, seed, step)
+            q[b, k * G:(k + 1) * G] = qt.view(q.dtype).reshape(G, d)
+            counts[b, k] = c
+    return Problem(q, P.K, P.V, P.kv_offsets, P.dtype, Hkv), counts

@@ -452,6 +452,115 @@ int santa_oracle_tiled_decode(const oracle_problem* P, int32_t sampler, int32_t 
 }
 
 /* ------------------------------------------------------------------ */
+/* Bernoulli qK^T with the mean group query (App. C, Eq. 8-13)          */
+/* ------------------------------------------------------------------ */
+
+/* fp32 -> bf16 bits, round to nearest even. */
+static uint16_t f32_to_bf16_rne(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x40u);   /* NaN stays NaN */
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+/* fp32 -> IEEE binary16 bits, round to nearest even, with subnormals and
+ * overflow to infinity. */
+static uint16_t f32_to_fp16_rne(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  const uint32_t sign = (u >> 16) & 0x8000u, a = u & 0x7fffffffu;
+  if (a > 0x7f800000u) return (uint16_t)(sign | 0x7e00u);
+  if (a >= 0x477ff000u) return (uint16_t)(sign | 0x7c00u);   /* >= 65520 rounds to infinity */
+  if (a < 0x33000000u) return (uint16_t)sign;                 /* < 2^-25 rounds to zero */
+  const int e = (int)(a >> 23);
+  uint32_t q, r, half;
+  if (e < 113) {   /* below 2^-14: subnormal, value = m 2^(e-150) = h 2^-24 */
+    const uint32_t m = (a & 0x7fffffu) | 0x800000u;
+    const int s = 126 - e;   /* 14..24 */
+    q = m >> s;
+    r = m & ((1u << s) - 1u);
+    half = 1u << (s - 1);
+  } else {         /* normal: exponent e - 112, 10 mantissa bits */
+    q = ((uint32_t)(e - 112) << 10) | ((a & 0x7fffffu) >> 13);
+    r = a & 0x1fffu;
+    half = 0x1000u;
+  }
+  if (r > half || (r == half && (q & 1u))) ++q;   /* a mantissa carry moves into the exponent */
+  return (uint16_t)(sign | q);
+}
+
+void santa_oracle_store_elem(int32_t dtype, float x, void* out) {
+  if (dtype == ORACLE_BF16) *(uint16_t*)out = f32_to_bf16_rne(x);
+  else if (dtype == ORACLE_FP16) *(uint16_t*)out = f32_to_fp16_rne(x);
+  else *(float*)out = x;
+}
+
+/* The effective queries of one GQA group under Bernoulli qK^T with the mean
+ * group query (App. C.2):
+ *   m_i = (1/G) sum_g |q_g,i|                                   (Eq. 10)
+ *   b_i^(n) ~ Bernoulli(m_i / norm), norm = max_i m_i            (Eq. 11)
+ *   m^_i = (norm / B) sum_n b_i^(n)                              (Eq. 12)
+ *   q~_g,i = m^_i q_g,i / m_i, so that q~_g . K_n = (m^ o q_g / m) . K_n   (Eq. 13)
+ * Stratified (App. C.1, Fig. 6): sample n of feature i is 1 when
+ * (n + u)/B < m_i / norm, i.e. one uniform per stratum of [0, 1).
+ * Arithmetic is fp32 in this fixed order (the pages fix no precision; the
+ * decode consumes the queries in the cache dtype): m_i summed over g in
+ * order then divided by G, p_i = m_i / norm, m^_i = (norm c_i) / B,
+ * q~ = (m^_i q_g,i) / m_i rounded to the storage dtype; the Bernoulli tests
+ * compare 24-bit uniforms exactly, a24 < p_i 2^24 (stratified:
+ * n 2^24 + a24 < B p_i 2^24, exact in float64).  Uniform r = n d + i of the
+ * group is word r % 4 of the Philox block at counter (r / 4, H + kvh, b,
+ * step), a stream of its own beside the query heads' (0..H-1).
+ * qt: storage dtype [G, d]; counts (may be NULL): [d] ones per feature. */
+int santa_oracle_bernoulli_group(const oracle_problem* P, int32_t b, int32_t kvh, int32_t nsamp, int32_t stratified,
+                                 uint64_t seed, uint32_t step, void* qt, int32_t* counts) {
+  if (!P || b < 0 || b >= P->batch || kvh < 0 || kvh >= P->n_kv_heads || nsamp < 1 || nsamp > 1024) return -1;
+  if (P->n_q_heads % P->n_kv_heads) return -1;
+  const int32_t G = P->n_q_heads / P->n_kv_heads, d = P->head_dim, H = P->n_q_heads;
+  const size_t es = P->dtype == ORACLE_FP32 ? 4 : 2;
+  float* q = (float*)malloc(sizeof(float) * (size_t)G * d);
+  float* m = (float*)malloc(sizeof(float) * (size_t)d);
+  if (!q || !m) { free(q); free(m); return -2; }
+  for (int32_t g = 0; g < G; ++g)
+    for (int32_t i = 0; i < d; ++i)
+      q[g * d + i] = (float)load_elem(P->dtype, P->q, ((int64_t)b * H + (int64_t)kvh * G + g) * d + i);
+  float norm = 0.f;
+  for (int32_t i = 0; i < d; ++i) {
+    float acc = 0.f;
+    for (int32_t g = 0; g < G; ++g) acc += fabsf(q[g * d + i]);
+    m[i] = acc / (float)G;
+    if (m[i] > norm) norm = m[i];
+  }
+  const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  for (int32_t i = 0; i < d; ++i) {
+    int32_t c = 0;
+    if (norm > 0.f && m[i] > 0.f) {
+      const float pr = m[i] / norm;
+      for (int32_t n = 0; n < nsamp; ++n) {
+        const uint32_t r = (uint32_t)(n * d + i);
+        const uint32_t ctr[4] = {r / 4, (uint32_t)(H + kvh), (uint32_t)b, step};
+        uint32_t w[4];
+        santa_oracle_philox4x32_10(ctr, key, w);
+        const double a24 = (double)(w[r % 4] >> 8);
+        const int hit = stratified ? ((double)n * 16777216.0 + a24 < (double)nsamp * (double)pr * 16777216.0)
+                                   : (a24 < (double)pr * 16777216.0);
+        c += hit;
+      }
+    }
+    if (counts) counts[i] = c;
+    const float mh = (norm * (float)c) / (float)nsamp;
+    for (int32_t g = 0; g < G; ++g) {
+      const float v = m[i] > 0.f ? (mh * q[g * d + i]) / m[i] : 0.f;
+      santa_oracle_store_elem(P->dtype, v, (unsigned char*)qt + ((size_t)g * d + i) * es);
+    }
+  }
+  free(q);
+  free(m);
+  return 0;
+}
+
+/* ------------------------------------------------------------------ */
 /* whole decode step                                                    */
 /* ------------------------------------------------------------------ */
 

@@ -16,6 +16,7 @@
  *                             tile budgets, per-tile systematic counts)
  *   S2ANTA-flash ............ App. P, Algorithms 6-8 (uniform tile budgets,
  *                             merge weighted by the tile masses)
+ *   Bernoulli qK^T .......... App. C, Eq. (8)-(13) (mean group query)
  * The Philox4x32-10 generator follows Salmon, Moraes, Dror, Shaw, "Parallel
  * random numbers: as easy as 1, 2, 3" (SC'11); the pages name no generator.
  */
@@ -91,6 +92,16 @@ int santa_oracle_tiled_head(const oracle_problem* P, int32_t b, int32_t h, int32
 /* Whole step of a tile sampler: est [batch, H, d]. */
 int santa_oracle_tiled_decode(const oracle_problem* P, int32_t sampler, int32_t S, const int32_t* S_per_seq,
                               int32_t tile_len, uint64_t seed, uint32_t step, double* est, int32_t n_threads);
+
+/* Storage rounding: fp32 x to the dtype (bf16 / fp16 round to nearest even). */
+void santa_oracle_store_elem(int32_t dtype, float x, void* out);
+
+/* Bernoulli qK^T with the mean group query (App. C.2, Eq. 10-13): the
+ * effective queries q~ [G, d] (storage dtype) of the group of KV head kvh,
+ * from nsamp Bernoulli samples per feature (stratified != 0: one uniform per
+ * stratum, App. C.1).  counts [d] (may be NULL) gets the ones per feature. */
+int santa_oracle_bernoulli_group(const oracle_problem* P, int32_t b, int32_t kvh, int32_t nsamp, int32_t stratified,
+                                 uint64_t seed, uint32_t step, void* qt, int32_t* counts);
 
 /* Full decode step over all (b, h).  S_per_seq (host, may be NULL) overrides S.
  * est: [batch, H, d]; J / delta: [batch, H, S_stride] (entries j >= S_b get -1).

@@ -635,3 +635,94 @@ def test_variance_falls_with_S_and_stratification_helps(oracle_lib):
     assert np.all(np.array(vs) < np.array(vi)) and np.all(np.array(vy) < np.array(vi))
     print("\nslopes of log variance trace against log S: i.i.d. %.2f, stratified %.2f, systematic %.2f"
           % (slope(vi), slope(vs), slope(vy)))
+
+
+# ---------------------------------------------------------------------------
+# Bernoulli qK^T, mean group query (App. C, Eq. 8-13; Fig. 6)
+# ---------------------------------------------------------------------------
+
+def test_storage_rounding_matches_numpy(oracle_lib):
+    """fp32 -> fp16 / bf16 round to nearest even, against numpy's float16 cast
+    and a bf16 rounding written from the bit layout in synth."""
+    rng = np.random.default_rng(1)
+    xs = np.concatenate([rng.standard_normal(2000) * 10.0 ** rng.integers(-9, 5, 2000),
+                         [0.0, -0.0, 65504.0, 65519.99, 65520.0, 2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26, 1e-30]])
+    xs = xs.astype(np.float32)
+    with np.errstate(over="ignore"):
+        want16 = xs.astype(np.float16).view(np.uint16)
+    got16 = np.array([oracle_lib.store_elem("fp16", float(x)) for x in xs], np.uint16)
+    np.testing.assert_array_equal(got16, want16)
+    gotb = np.array([oracle_lib.store_elem("bf16", float(x)) for x in xs], np.uint16)
+    np.testing.assert_array_equal(gotb, synth.f32_to_bf16_bits(xs))
+
+
+def _bern_problem(oracle_lib, rng, G=4, d=128, nk=64, dtype="fp32"):
+    q = rng.standard_normal((1, G, d)).astype(np.float32)
+    K = rng.standard_normal((nk, 1, d)).astype(np.float32)
+    V = rng.standard_normal((nk, 1, d)).astype(np.float32)
+    return oracle_lib.Problem(q, K, V, np.array([0, nk], np.int64), dtype, 1)
+
+
+@pytest.mark.parametrize("stratified", [False, True])
+def test_bernoulli_counts_law(oracle_lib, stratified):
+    """Eq. (11)-(12): the ones per feature over B samples have mean B p_i with
+    p_i = m_i / max m (so m^ is unbiased, Eq. 12, and q~ is unbiased for q,
+    Eq. 13); plain sampling is Binomial(B, p_i), stratified sampling takes only
+    floor(B p_i) or floor(B p_i) + 1."""
+    rng = np.random.default_rng(11)
+    P = _bern_problem(oracle_lib, rng)
+    m = np.abs(P.q[0].astype(np.float64)).mean(axis=0)
+    p = m / m.max()
+    Bs = 4
+    C = np.array([oracle_lib.bernoulli_group(P, 0, 0, Bs, stratified, seed)[1] for seed in range(600)])
+    mean, var = C.mean(axis=0), C.var(axis=0)
+    f = Bs * p - np.floor(Bs * p)
+    law_var = f * (1 - f) if stratified else Bs * p * (1 - p)   # variance of the count under the stated law
+    se = np.sqrt(law_var / C.shape[0])
+    assert np.all(np.abs(mean - Bs * p) < 5 * se + 0.01)
+    if stratified:
+        fl = np.floor(Bs * p)
+        assert np.all((C == fl) | (C == fl + 1))
+    else:
+        assert np.all(np.abs(var - Bs * p * (1 - p)) < 0.25 + 0.35 * Bs * p * (1 - p))
+    assert np.all(C[:, np.argmax(m)] == Bs)   # the largest feature has p = 1
+
+
+def test_bernoulli_effective_query_is_unbiased(oracle_lib):
+    """Eq. (13): E[q~] = q (averaged over seeds, fp32 storage)."""
+    rng = np.random.default_rng(12)
+    P = _bern_problem(oracle_lib, rng, G=2, d=64)
+    Bs, N = 8, 400
+    qs = np.array([oracle_lib.bernoulli_group(P, 0, 0, Bs, True, seed)[0] for seed in range(N)], np.float64)
+    q = P.q[0].astype(np.float64)
+    m = np.abs(q).mean(axis=0)
+    f = np.mod(Bs * m / m.max(), 1.0)
+    se = np.abs(q) * m.max() / (m * Bs) * np.sqrt(f * (1 - f) / N)   # q~ = (max m) (c / B) q / m
+    assert np.all(np.abs(qs.mean(axis=0) - q) < 5 * se + 1e-6 * np.abs(q) + 1e-9)
+
+
+def test_bernoulli_score_error_reproduces_fig6(oracle_lib):
+    """App. C.1, Fig. 6: relative L2 error of the Bernoulli scores for one query
+    (d = 128, nk = 1024, q ~ N(0, 1), K ~ N(0, 1)/sqrt(d)), about 60% at B = 4
+    for plain sampling and about 30% for stratified; plain falls like
+    B^-1/2 and stratified like B^-1."""
+    rng = np.random.default_rng(13)
+    d, nk, n_inst = 128, 1024, 40
+    err = {False: {}, True: {}}
+    for B in (4, 16, 64):
+        for strat in (False, True):
+            e = []
+            for inst in range(n_inst):
+                q = rng.standard_normal((1, 1, d)).astype(np.float32)
+                K = (rng.standard_normal((nk, 1, d)) / np.sqrt(d)).astype(np.float32)
+                P = oracle_lib.Problem(q, K, K, np.array([0, nk], np.int64), "fp32", 1)
+                qt, _ = oracle_lib.bernoulli_group(P, 0, 0, B, strat, seed=inst)
+                s = K[:, 0].astype(np.float64) @ q[0, 0].astype(np.float64)
+                sh = K[:, 0].astype(np.float64) @ qt[0].astype(np.float64)
+                e.append(np.linalg.norm(sh - s) / np.linalg.norm(s))
+            err[strat][B] = float(np.mean(e))
+    assert 0.5 < err[False][4] < 0.7 and 0.2 < err[True][4] < 0.4, err
+    slope = lambda d_: np.polyfit(np.log([4, 16, 64]), np.log([d_[4], d_[16], d_[64]]), 1)[0]
+    assert abs(slope(err[False]) + 0.5) < 0.1 and abs(slope(err[True]) + 1.0) < 0.15, err
+    print("\nBernoulli score error (B = 4, 16, 64): plain %s, stratified %s"
+          % ([round(err[False][b], 3) for b in (4, 16, 64)], [round(err[True][b], 3) for b in (4, 16, 64)]))
