@@ -60,6 +60,9 @@ def parse_args():
                     help="global: the single-launch sampler (the benchmark line); prop / flash: the pages' "
                          "tile samplers S2ANTA-prop and S2ANTA-flash")
     ap.add_argument("--tile", type=int, default=256, help="keys per tile for --sampler prop / flash")
+    ap.add_argument("--bernoulli", type=int, default=0,
+                    help="Bernoulli qK^T (mean group query, stratified) with this many samples per feature "
+                         "in front of the single-launch decode; 0: exact scores")
     ap.add_argument("--l2", choices=["auto", "replicas", "flush"], default="auto",
                     help="inputs larger than L2 (rotating K/V copies) or an L2 flush between steps; "
                          "auto: copies when the cache is at least 128 MiB")
@@ -630,12 +633,115 @@ def run_tiled(args):
     return 0
 
 
+def run_bernoulli(args):
+    """Decode step on Bernoulli qK^T effective queries (one small kernel, then
+    the single-launch decode), launched back to back over rotating K/V copies.
+    The decode still reads every key feature: the bytes are the main line's;
+    the share of features the groups need is reported beside them."""
+    import ctypes
+    import numpy as np
+    import torch
+    import synth
+    import stochastic_sparse_decode_split_gb300 as santa
+
+    world, rank, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    lib = santa.library()
+    wl = make_workload(args)
+    inp = synth.generate(wl, 0)
+    t = synth.to_torch(inp, dev)
+    ragged = wl.ragged is not None
+    nk = int(inp.nk_per_seq.max()) if ragged else None
+    offs = t["kv_offsets"] if ragged else None
+    S_max = inp.S_max
+    B, H, d = inp.q.shape
+    p = santa.make_params(t["q"], t["K"], S_max, 0, 0, nk, offs, t["S_per_seq"])
+    nbytes = santa.bernoulli_workspace_size(p)
+    kv_bytes = t["K"].numel() * t["K"].element_size() * 2
+    R = max(2, -(-FLUSH_BYTES // kv_bytes))
+    reps = [(t["K"], t["V"])] + [(t["K"].clone(), t["V"].clone()) for _ in range(R - 1)]
+    ws = santa.alloc_workspace(nbytes, dev)
+    out = torch.empty((B, H, d), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    sid = ctypes.c_void_p(stream.cuda_stream)
+    ptrs = [(ctypes.c_void_p(Kr.data_ptr()), ctypes.c_void_p(Vr.data_ptr())) for Kr, Vr in reps]
+    qp, op, wp = (ctypes.c_void_p(x.data_ptr()) for x in (t["q"], out, ws))
+    var = santa.VARIANTS[wl.variant]
+
+    def step(i, idx=None, cnt=None):
+        Kp, Vp = ptrs[i % R]
+        st = lib.santa_decode_bernoulli(ctypes.byref(p), var, args.bernoulli, 1, qp, Kp, Vp, op, wp, nbytes, sid,
+                                        None if idx is None else ctypes.c_void_p(idx.data_ptr()),
+                                        None if cnt is None else ctypes.c_void_p(cnt.data_ptr()))
+        if st != 0:
+            raise RuntimeError(f"santa_decode_bernoulli: status {st}")
+
+    idx = torch.full((B, H, S_max), -1, dtype=torch.int32, device=dev)
+    cnt = torch.zeros((B, wl.n_kv_heads, d), dtype=torch.int32, device=dev)
+    step(0, idx, cnt)
+    torch.cuda.synchronize()
+    unique_rows = count_unique_rows(inp, idx.cpu().numpy())
+    share = float((cnt.cpu().numpy() > 0).mean())
+    for i in range(args.warmup):
+        step(i)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local_rank).start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1), dev) / args.steps
+    peak, peak_kind = hbm_peak()
+    stb = step_bytes(inp, unique_rows)
+    achieved = stb / (ms * 1e-3) / 1e9
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": ms * 1e3 / world, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "variant": wl.variant, "bernoulli_samples": args.bernoulli,
+                   "bernoulli": "stratified, mean group query", "S": S_max, "nk": wl.nk, "batch": B,
+                   "n_q_heads": H, "n_kv_heads": wl.n_kv_heads, "head_dim": d,
+                   "l2": f"inputs larger than L2: {R} replicas of the K/V cache used in turn "
+                         f"({R * kv_bytes >> 20} MiB)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": "step: bernoulli_query_kernel + fused_decode_kernel",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "peak_kind": f"of {peak_kind}", "alg_bytes_per_launch": stb,
+                     "timing": "steps launched back to back over rotating replicas"},
+        "step": {"alg_bytes": stb, "unique_v_rows": unique_rows, "key_feature_share": share},
+        "cpu_baseline": None,
+        "e2e": None,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
     if args.sampler != "global":
         return run_tiled(args)
+    if args.bernoulli:
+        return run_bernoulli(args)
     return run_ours(args)
 
 

@@ -177,6 +177,28 @@ santa_status_t santa_decode_tiled(const santa_params_t* p, int32_t sampler, int3
                                   const void* K, const void* V, float* out, void* workspace, size_t ws_bytes,
                                   santa_stream_t stream, int32_t* sample_idx);
 
+/* santa_decode on Bernoulli qK^T scores with the mean group query ("Stochastic
+ * Sparse Attention for Memory-Bound Inference", Sec. 5.1, App. C.2, Eq. 10-13).
+ * For each (sequence, KV head) group: m_i = mean_g |q_g,i|, norm = max_i m_i,
+ * c_i of n_samples Bernoulli(m_i / norm) draws are one (stratified != 0: draw
+ * n is one when (n + u)/n_samples < m_i / norm, one uniform per stratum,
+ * App. C.1), m^_i = norm c_i / n_samples, and each head's query becomes
+ * q~_g,i = m^_i q_g,i / m_i (fp32, rounded to nearest even into the cache
+ * dtype); the step then runs as santa_decode on q~ (features with c_i = 0
+ * multiply zero in every head of the group).  Uniform r = n d + i of a group
+ * is word r % 4 of the Philox block at counter (r / 4, n_q_heads + kvh, b, step).
+ *   n_samples       1..1024
+ *   feature_counts  optional device int32 [batch, n_kv_heads, head_dim]: c_i.
+ * The workspace must hold santa_bernoulli_workspace_size(p) bytes; the
+ * effective queries are left in it, [batch, n_q_heads, head_dim] in the cache
+ * dtype, starting at byte santa_workspace_size(p) rounded up to 256.  Other
+ * arguments, results and errors as santa_decode. */
+size_t santa_bernoulli_workspace_size(const santa_params_t* p);
+santa_status_t santa_decode_bernoulli(const santa_params_t* p, int32_t variant, int32_t n_samples, int32_t stratified,
+                                      const void* q, const void* K, const void* V, float* out, void* workspace,
+                                      size_t ws_bytes, santa_stream_t stream, int32_t* sample_idx,
+                                      int32_t* feature_counts);
+
 /* Byte offsets of the intermediate arrays inside a santa_decode workspace, for
  * inspection by tests and tools after the stream has synchronised:
  *   stash     float32 [batch, n_q_heads, nk]        scaled scores s_n

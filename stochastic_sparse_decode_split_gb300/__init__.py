@@ -29,7 +29,7 @@ __all__ = [
     "SantaError", "Params", "library", "santa_decode", "santa_decode_with_uniforms", "santa_dense_decode",
     "workspace_size", "dense_workspace_size", "workspace_layout", "get_error", "Decoder", "exported_symbols",
     "VARIANTS", "DTYPES", "santa_decode_static", "static_scratch_bytes", "SAMPLERS", "santa_decode_tiled",
-    "tiled_workspace_size", "tiled_max_draws",
+    "tiled_workspace_size", "tiled_max_draws", "santa_decode_bernoulli", "bernoulli_workspace_size",
 ]
 
 VARIANTS = {"iid": 0, "stratified": 1, "systematic": 2}
@@ -101,13 +101,16 @@ def library():
             lib.santa_tiled_max_draws.argtypes = [P, i32, i32]
             lib.santa_tiled_max_draws.restype = i32
             lib.santa_decode_tiled.argtypes = [P, i32, i32, vp, vp, vp, vp, vp, sz, vp, vp]
+            lib.santa_bernoulli_workspace_size.argtypes = [P]
+            lib.santa_bernoulli_workspace_size.restype = sz
+            lib.santa_decode_bernoulli.argtypes = [P, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp, vp, vp]
             lib.santa_get_error.argtypes = [vp, vp, ctypes.POINTER(i32)]
             lib.santa_status_string.argtypes = [i32]
             lib.santa_status_string.restype = ctypes.c_char_p
             lib.santa_version.restype = i32
             for fn in ("santa_workspace_init", "santa_decode", "santa_decode_profiled", "santa_score_pass",
                        "santa_decode_with_uniforms", "santa_dense_decode", "santa_decode_static",
-                       "santa_workspace_layout", "santa_get_error", "santa_decode_tiled"):
+                       "santa_workspace_layout", "santa_get_error", "santa_decode_tiled", "santa_decode_bernoulli"):
                 getattr(lib, fn).restype = i32
             _lib = lib
     return _lib
@@ -261,6 +264,30 @@ def santa_decode_tiled(q, K, V, S: int, sampler: str = "prop", tile_len: int = 2
                                       _ptr(sample_idx))
     if st != SANTA_OK:
         raise SantaError(st, "santa_decode_tiled")
+    return out
+
+
+def bernoulli_workspace_size(p: Params) -> int:
+    return library().santa_bernoulli_workspace_size(ctypes.byref(p))
+
+
+def santa_decode_bernoulli(q, K, V, S: int, n_samples: int, stratified: bool = True, variant: str = "systematic",
+                           seed: int = 0, step: int = 0, out=None, nk: Optional[int] = None, kv_offsets=None,
+                           S_per_seq=None, scale: float = 0.0, workspace=None, sample_idx=None, feature_counts=None,
+                           stream=None) -> torch.Tensor:
+    """santa_decode on Bernoulli qK^T scores with the mean group query;
+    feature_counts, if given, is int32 [B, H_kv, d] (ones per feature)."""
+    _check_tensors(q, K, V, out, kv_offsets, S_per_seq, sample_idx, feature_counts)
+    p = make_params(q, K, S, seed, step, nk, kv_offsets, S_per_seq, scale)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(bernoulli_workspace_size(p), q.device)
+    st = library().santa_decode_bernoulli(ctypes.byref(p), VARIANTS[variant], n_samples, int(bool(stratified)),
+                                          _ptr(q), _ptr(K), _ptr(V), _ptr(out), _ptr(workspace), workspace.numel(),
+                                          _stream(stream), _ptr(sample_idx), _ptr(feature_counts))
+    if st != SANTA_OK:
+        raise SantaError(st, "santa_decode_bernoulli")
     return out
 
 

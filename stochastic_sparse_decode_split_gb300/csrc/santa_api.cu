@@ -283,6 +283,31 @@ santa_status_t santa_decode_tiled(const santa_params_t* p, int32_t sampler, int3
   return santa::launch_tiled(a) == cudaSuccess ? SANTA_OK : SANTA_ERR_CUDA;
 }
 
+size_t santa_bernoulli_workspace_size(const santa_params_t* p) {
+  if (check_params(p, true) != SANTA_OK) return 0;
+  const size_t es = p->dtype == SANTA_FP32 ? 4 : 2;
+  return up(santa_layout(p).total) + up((size_t)p->batch * p->n_q_heads * p->head_dim * es);
+}
+
+santa_status_t santa_decode_bernoulli(const santa_params_t* p, int32_t variant, int32_t n_samples, int32_t stratified,
+                                      const void* q, const void* K, const void* V, float* out, void* workspace,
+                                      size_t ws_bytes, santa_stream_t stream, int32_t* sample_idx,
+                                      int32_t* feature_counts) {
+  santa_status_t st = check_params(p, true);
+  if (st != SANTA_OK) return st;
+  if (n_samples < 1 || n_samples > 1024) return SANTA_ERR_INVALID_ARG;
+  if (feature_counts && !aligned(feature_counts, 4)) return SANTA_ERR_INVALID_ARG;
+  const size_t need = santa_bernoulli_workspace_size(p);
+  st = check_buffers(q, K, V, out, workspace, ws_bytes, need);
+  if (st != SANTA_OK) return st;
+  const Layout L = santa_layout(p);
+  void* qt = static_cast<unsigned char*>(workspace) + up(L.total);
+  santa::LaunchArgs a = base_args(p, L, q, K, V, out, workspace, (cudaStream_t)stream);
+  if (santa::launch_bernoulli_query(a, qt, feature_counts, n_samples, stratified ? 1 : 0) != cudaSuccess)
+    return SANTA_ERR_CUDA;
+  return santa_decode(p, variant, qt, K, V, out, workspace, ws_bytes, stream, sample_idx);
+}
+
 size_t santa_dense_workspace_size(const santa_params_t* p) {
   if (check_params(p, false) != SANTA_OK) return 0;
   return dense_layout(p).total;
