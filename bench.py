@@ -437,10 +437,27 @@ def run_ours(args):
         return e0.elapsed_time(e1) / n
 
     launch_ms = score_launch_ms = None
+    read_probe = None
     if flush is None:
         n_back = min(args.steps, 400)
         launch_ms = back_to_back(lambda i: decs[i % R](step=0), n_back)
         score_launch_ms = back_to_back(lambda i: decs[i % R].score_pass(), n_back)
+        # read ceiling of this transfer size: a plain streaming read of the K
+        # bytes, launched back to back over the same replicas
+        import ctypes
+        lib = santa.library()
+        sink = torch.empty(lib.santa_read_probe_sink_words(), dtype=torch.int32, device=dev)
+        k_bytes = t["K"].numel() * t["K"].element_size()
+        sid = ctypes.c_void_p(stream.cuda_stream)
+
+        def read_k(i):
+            if lib.santa_read_probe(ctypes.c_void_p(reps[i % R][0].data_ptr()), k_bytes,
+                                    ctypes.c_void_p(sink.data_ptr()), sid) != 0:
+                raise RuntimeError("santa_read_probe failed")
+
+        probe_ms = back_to_back(read_k, n_back)
+        read_probe = {"kernel": "read_probe_kernel (16-byte streaming read, no compute)", "bytes": k_bytes,
+                      "us_per_read": probe_ms * 1e3, "GBps": k_bytes / (probe_ms * 1e-3) / 1e9}
 
     # dense comparator, same protocol
     denses = [santa.Decoder(t["q"], Kr, Vr, S=1, variant=wl.variant, dense=True, **kw) for (Kr, Vr) in reps]
@@ -505,6 +522,7 @@ def run_ours(args):
                                 else "events around each step")},
         "step": {"alg_bytes": stb, "unique_v_rows": unique_rows, "achieved_GBps": step_achieved,
                  "frac": step_achieved / peak},
+        "read_probe": (dict(read_probe, frac_of_peak=read_probe["GBps"] / peak) if read_probe else None),
         "staged_path": {"stage_us": {"score": stage_ms[0] * 1e3, "combine": stage_ms[1] * 1e3,
                                      "sample_gather": stage_ms[2] * 1e3},
                         "score_pass_us_per_launch": score_launch_ms * 1e3 if score_launch_ms else None,

@@ -247,6 +247,15 @@ santa_status_t santa_get_error(void* workspace, santa_stream_t stream, int32_t* 
 santa_status_t santa_decode_static(const santa_params_t* p, int32_t variant, const void* q, const void* K,
                                    const void* V, float* out, santa_stream_t stream, int32_t* sample_idx);
 
+/* Measurement helper, not part of the method: reads `bytes` bytes at `src`
+ * (device, 16-byte aligned, a multiple of 16) once with 16-byte
+ * non-allocating loads, 2 CTAs of 512 threads per SM, on `stream`, and writes
+ * one word per thread to `sink` (device, santa_read_probe_sink_words()
+ * uint32 words).  Timed by the caller, it gives the read ceiling of a transfer
+ * of that size (launch, ramp and tail included) beside a kernel's roofline. */
+int32_t santa_read_probe_sink_words(void);
+santa_status_t santa_read_probe(const void* src, size_t bytes, uint32_t* sink, santa_stream_t stream);
+
 /* Static description of a status code. */
 const char* santa_status_string(santa_status_t status);
 

@@ -101,6 +101,9 @@ def library():
             lib.santa_tiled_max_draws.argtypes = [P, i32, i32]
             lib.santa_tiled_max_draws.restype = i32
             lib.santa_decode_tiled.argtypes = [P, i32, i32, vp, vp, vp, vp, vp, sz, vp, vp]
+            lib.santa_read_probe_sink_words.restype = i32
+            lib.santa_read_probe.argtypes = [vp, sz, vp, vp]
+            lib.santa_read_probe.restype = i32
             lib.santa_bernoulli_workspace_size.argtypes = [P]
             lib.santa_bernoulli_workspace_size.restype = sz
             lib.santa_decode_bernoulli.argtypes = [P, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp, vp, vp]

@@ -308,6 +308,15 @@ santa_status_t santa_decode_bernoulli(const santa_params_t* p, int32_t variant, 
   return santa_decode(p, variant, qt, K, V, out, workspace, ws_bytes, stream, sample_idx);
 }
 
+int32_t santa_read_probe_sink_words(void) { return 2 * 512 * device_sms(); }
+
+santa_status_t santa_read_probe(const void* src, size_t bytes, uint32_t* sink, santa_stream_t stream) {
+  if (!src || !sink || !aligned(src, 16) || !aligned(sink, 4) || bytes == 0 || bytes % 16) return SANTA_ERR_INVALID_ARG;
+  return santa::launch_read_probe(src, bytes, sink, 2 * device_sms(), (cudaStream_t)stream) == cudaSuccess
+             ? SANTA_OK
+             : SANTA_ERR_CUDA;
+}
+
 size_t santa_dense_workspace_size(const santa_params_t* p) {
   if (check_params(p, false) != SANTA_OK) return 0;
   return dense_layout(p).total;
