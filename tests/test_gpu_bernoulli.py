@@ -92,3 +92,33 @@ def test_llama_32k_feature_access():
     share = float((counts > 0).mean())
     assert 0.3 < share < 1.0
     print(f"\nkey features needed per KV-head group (B = 8, stratified): {100 * share:.1f}%")
+
+
+def test_device_flags_bad_ragged_metadata():
+    """Bad ragged metadata is flagged as in santa_decode; the other sequences
+    are unaffected."""
+    wl = synth.Workload("flags_b", 3, 4, 2, 128, 600, "bf16", 32, "systematic", ragged=(600, 600))
+    inp = synth.generate(wl, 1)
+    t = synth.to_torch(inp)
+    S_per = torch.tensor([32, 0, 16], dtype=torch.int32, device="cuda")
+    offs = torch.tensor([0, 600, 1200, 1800], dtype=torch.int64, device="cuda")
+    p = santa.make_params(t["q"], t["K"], 32, nk=500, kv_offsets=offs, S_per_seq=S_per)
+    ws = santa.alloc_workspace(santa.bernoulli_workspace_size(p), "cuda")
+    out = santa.santa_decode_bernoulli(t["q"], t["K"], t["V"], S=32, n_samples=4, nk=500, kv_offsets=offs,
+                                       S_per_seq=S_per, workspace=ws)
+    code = santa.get_error(ws)
+    assert code & 1 and code & 2
+    assert torch.count_nonzero(out) == 0
+    offs_ok = torch.tensor([0, 600, 1000, 1800], dtype=torch.int64, device="cuda")
+    out = santa.santa_decode_bernoulli(t["q"], t["K"], t["V"], S=32, n_samples=4, nk=800, kv_offsets=offs_ok,
+                                       S_per_seq=S_per)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out[1]) == 0 and torch.count_nonzero(out[0]) > 0
+
+
+def test_invalid_sample_counts_are_rejected():
+    inp = synth.generate(synth.Workload("bad_b", 1, 4, 1, 64, 300, "bf16", 16, "systematic"), 0)
+    t = synth.to_torch(inp)
+    for n in (0, 1025):
+        with pytest.raises(santa.SantaError):
+            santa.santa_decode_bernoulli(t["q"], t["K"], t["V"], S=16, n_samples=n)

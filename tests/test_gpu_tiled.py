@@ -188,3 +188,31 @@ def test_invalid_tile_lengths_are_rejected():
         assert santa.tiled_workspace_size(p, "prop", L) == 0
         with pytest.raises(santa.SantaError):
             santa.santa_decode_tiled(t["q"], t["K"], t["V"], S=16, sampler="prop", tile_len=L)
+
+
+@pytest.mark.parametrize("sampler", ["prop", "flash"])
+def test_device_flags_bad_ragged_metadata(sampler):
+    """A sequence longer than the stated bound or a budget out of range is
+    flagged in the workspace error word; its heads come out zero with their
+    sample_idx rows -1, and the other sequences are unaffected."""
+    wl = synth.Workload("flags_t", 3, 4, 2, 128, 600, "bf16", 32, "systematic", ragged=(600, 600))
+    inp = synth.generate(wl, 1)
+    t = synth.to_torch(inp)
+    S_per = torch.tensor([32, 0, 16], dtype=torch.int32, device="cuda")    # S_1 = 0 is out of range
+    offs = torch.tensor([0, 600, 1200, 1800], dtype=torch.int64, device="cuda")
+    p = santa.make_params(t["q"], t["K"], 32, nk=500, kv_offsets=offs, S_per_seq=S_per)   # bound 500 < 600
+    ws = santa.alloc_workspace(santa.tiled_workspace_size(p, sampler, 64), "cuda")
+    out = santa.santa_decode_tiled(t["q"], t["K"], t["V"], S=32, sampler=sampler, tile_len=64, nk=500,
+                                   kv_offsets=offs, S_per_seq=S_per, workspace=ws)
+    code = santa.get_error(ws)
+    assert code & 1 and code & 2
+    assert torch.count_nonzero(out) == 0
+    offs_ok = torch.tensor([0, 600, 1000, 1800], dtype=torch.int64, device="cuda")
+    p = santa.make_params(t["q"], t["K"], 32, nk=800, kv_offsets=offs_ok, S_per_seq=S_per)
+    nd = santa.tiled_max_draws(p, sampler, 64)
+    idx = torch.full((3, 4, nd), -7, dtype=torch.int32, device="cuda")
+    out = santa.santa_decode_tiled(t["q"], t["K"], t["V"], S=32, sampler=sampler, tile_len=64, nk=800,
+                                   kv_offsets=offs_ok, S_per_seq=S_per, sample_idx=idx)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out[1]) == 0 and torch.count_nonzero(out[0]) > 0 and torch.count_nonzero(out[2]) > 0
+    assert bool(torch.all(idx[1] == -1)) and bool(torch.all(idx[0] != -7))
