@@ -256,6 +256,15 @@ santa_status_t santa_decode_static(const santa_params_t* p, int32_t variant, con
 int32_t santa_read_probe_sink_words(void);
 santa_status_t santa_read_probe(const void* src, size_t bytes, uint32_t* sink, santa_stream_t stream);
 
+/* Self-test of the bounded grid-barrier wait (no counterpart in the paper):
+ * one CTA waits on the workspace's barrier generation word, which nothing
+ * advances, for limit_ns nanoseconds (1 ms .. 2 s) of %globaltimer time; the
+ * wait must then end with ERR_TIMEOUT (8) in the workspace error word, read
+ * by santa_get_error, and the GPU context stays usable.  The workspace (at
+ * least 256 bytes, initialised) must not be in use by a decode meanwhile. */
+santa_status_t santa_selftest_wait_timeout(void* workspace, size_t ws_bytes, uint64_t limit_ns,
+                                           santa_stream_t stream);
+
 /* Static description of a status code. */
 const char* santa_status_string(santa_status_t status);
 

@@ -101,6 +101,8 @@ def library():
             lib.santa_tiled_max_draws.argtypes = [P, i32, i32]
             lib.santa_tiled_max_draws.restype = i32
             lib.santa_decode_tiled.argtypes = [P, i32, i32, vp, vp, vp, vp, vp, sz, vp, vp]
+            lib.santa_selftest_wait_timeout.argtypes = [vp, sz, ctypes.c_uint64, vp]
+            lib.santa_selftest_wait_timeout.restype = i32
             lib.santa_read_probe_sink_words.restype = i32
             lib.santa_read_probe.argtypes = [vp, sz, vp, vp]
             lib.santa_read_probe.restype = i32

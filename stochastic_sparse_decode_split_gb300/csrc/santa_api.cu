@@ -308,6 +308,18 @@ santa_status_t santa_decode_bernoulli(const santa_params_t* p, int32_t variant, 
   return santa_decode(p, variant, qt, K, V, out, workspace, ws_bytes, stream, sample_idx);
 }
 
+santa_status_t santa_selftest_wait_timeout(void* workspace, size_t ws_bytes, uint64_t limit_ns,
+                                           santa_stream_t stream) {
+  if (!workspace || !aligned(workspace, ALIGN) || ws_bytes < HEADER) return SANTA_ERR_WORKSPACE;
+  if (limit_ns < 1000000ull || limit_ns > 2000000000ull) return SANTA_ERR_INVALID_ARG;
+  unsigned char* w = static_cast<unsigned char*>(workspace);
+  return santa::launch_wait_timeout_selftest(reinterpret_cast<const unsigned*>(w + BAR_GEN),
+                                             reinterpret_cast<int*>(w), limit_ns,
+                                             (cudaStream_t)stream) == cudaSuccess
+             ? SANTA_OK
+             : SANTA_ERR_CUDA;
+}
+
 int32_t santa_read_probe_sink_words(void) { return 2 * 512 * device_sms(); }
 
 santa_status_t santa_read_probe(const void* src, size_t bytes, uint32_t* sink, santa_stream_t stream) {

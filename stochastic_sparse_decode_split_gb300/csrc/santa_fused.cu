@@ -225,11 +225,12 @@ __device__ __forceinline__ unsigned grid_arrive(unsigned* count, unsigned* gen) 
 }
 // Waiting half: thread 0 spins until the generation moves past g (bounded),
 // then the CTA proceeds together.
-__device__ __forceinline__ void grid_wait(const unsigned* gen, unsigned g, int* err) {
+__device__ __forceinline__ void grid_wait(const unsigned* gen, unsigned g, int* err,
+                                          unsigned long long limit_ns = WAIT_LIMIT_NS) {
   if (threadIdx.x == 0) {
     const unsigned long long t0 = global_ns();
     while (ld_acquire(gen) == g) {
-      if (global_ns() - t0 > WAIT_LIMIT_NS) {
+      if (global_ns() - t0 > limit_ns) {
         flag_error(err, ERR_TIMEOUT);
         break;
       }
@@ -928,6 +929,22 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
     }
   });
   cp_async_wait_all();   // no copy outlives the CTA (a staged piece that was skipped)
+}
+
+// Self-test of the bounded wait: one CTA waits on a generation word that no
+// other CTA advances; the wait must end after limit_ns with ERR_TIMEOUT
+// flagged, and the CTA returns normally.
+__global__ void wait_timeout_selftest_kernel(const unsigned* gen, int* err, unsigned long long limit_ns) {
+  __shared__ unsigned g;
+  if (threadIdx.x == 0) g = ld_acquire(gen);
+  __syncthreads();
+  grid_wait(gen, g, err, limit_ns);
+}
+
+cudaError_t launch_wait_timeout_selftest(const unsigned* gen, int* err, unsigned long long limit_ns,
+                                         cudaStream_t stream) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(gen, err, limit_ns);
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------

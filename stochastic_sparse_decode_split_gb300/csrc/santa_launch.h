@@ -68,6 +68,8 @@ cudaError_t launch_fused(const LaunchArgs& a, unsigned* bar_count, unsigned* bar
 constexpr int TL_MAX_LEN = 1024;   // longest tile of the tile samplers
 cudaError_t launch_tiled(const LaunchArgs& a);   // after launch_score
 // Bernoulli qK^T effective queries qt [B, H, D] (cache dtype) from a.q; counts [B, Hkv, D] may be NULL.
+cudaError_t launch_wait_timeout_selftest(const unsigned* gen, int* err, unsigned long long limit_ns,
+                                         cudaStream_t stream);
 cudaError_t launch_read_probe(const void* src, size_t bytes, uint32_t* sink, int ctas, cudaStream_t stream);
 cudaError_t launch_bernoulli_query(const LaunchArgs& a, void* qt, int32_t* counts, int nsamp, int stratified);
 

@@ -8,6 +8,8 @@ relative L2 per head (against the oracle's gather of the GPU's own indices
 where a boundary draw differs); over 10^4 seeds the mean estimate lies within
 4 sigma of the exact attention output.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -329,3 +331,21 @@ def test_mean_over_10k_seeds_within_4_sigma(variant, which):
     z_allowed = max(4.0, float(norm.isf(0.5e-3 / n)))
     assert z.max() <= z_allowed, f"max z {z.max():.2f} over {n} coordinates (allowed {z_allowed:.2f})"
     assert np.mean(z * z) <= 1.0 + 5.0 * np.sqrt(2.0 / n), f"mean z^2 {np.mean(z * z):.3f}"
+
+
+def test_bounded_wait_times_out():
+    """The grid barrier's bounded wait, on a generation word nothing advances,
+    ends after its limit with ERR_TIMEOUT (8) in the error word, and the GPU
+    context stays usable."""
+    import time
+    lib = santa.library()
+    ws = santa.alloc_workspace(4096, "cuda")
+    t0 = time.perf_counter()
+    st = lib.santa_selftest_wait_timeout(ctypes.c_void_p(ws.data_ptr()), ws.numel(), 50_000_000,
+                                         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    assert santa.get_error(ws) == 8
+    assert time.perf_counter() - t0 >= 0.05
+    inp = synth.generate(synth.tiny("systematic"), 0)
+    out, idx = run_gpu(inp, "systematic", 0)
+    assert check_parity(inp, "systematic", 0, out, idx)["differing"] == 0
