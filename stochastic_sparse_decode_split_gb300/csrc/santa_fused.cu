@@ -372,13 +372,26 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
   }
   __syncthreads();   // statistics of the whole range written; the ring is free
 
-  // i.i.d.: sorted 24-bit uniform keys of the heads bh = cta (mod P)
+  // i.i.d.: sorted 24-bit uniform keys of every head.  When the units do not
+  // divide evenly, the CTAs with one unit fewer (done streaming about a unit
+  // earlier) sort, head j going to the (j mod n)-th of them; else CTA
+  // bh mod P.  Up to 1024 keys a head are placed by rank (each thread counts
+  // the keys below its own: one barrier), more by a bitonic network.
   if (a.variant == VAR_IID) {
+    const long long Tu = range[0], qu = Tu / P, rem = Tu % P;
+    int srank = cta, nsort = P;
+    if (rem != 0) {
+      const long long mine = Tu * (cta + 1) / P - Tu * cta / P;
+      const long long large_before = Tu * cta / P - (long long)cta * qu;
+      nsort = (int)(P - rem);
+      srank = mine == qu ? (int)(cta - large_before) : -1;
+    }
     uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
-    for (int64_t bh = cta; bh < (int64_t)a.B * a.H; bh += P) {
+    for (int64_t bh = srank; srank >= 0 && bh < (int64_t)a.B * a.H; bh += nsort) {
       const int b = (int)(bh / a.H), h = (int)(bh % a.H);
       int S_b;
       if (seq_error(a, b, S_b)) continue;
+      uint32_t* dst = a.ukeys + bh * a.S_max;
       int S2 = 1;
       while (S2 < S_b) S2 <<= 1;
       for (int i = tid; i < S2; i += SB_THREADS) {
@@ -391,23 +404,35 @@ fused_decode_kernel(LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
         keys[i] = k;
       }
       __syncthreads();
-      for (int kk = 2; kk <= S2; kk <<= 1) {
-        for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-          for (int i = tid; i < S2; i += SB_THREADS) {
-            const int ixj = i ^ jj;
-            if (ixj > i) {
-              const uint32_t x = keys[i], y = keys[ixj];
-              if ((x > y) == ((i & kk) == 0)) {
-                keys[i] = y;
-                keys[ixj] = x;
+      if (S_b <= 1024) {
+        for (int i = tid; i < S_b; i += SB_THREADS) {
+          const uint32_t ki = keys[i];
+          int rank = 0;
+          for (int u = 0; u < S_b; ++u) {
+            const uint32_t ku = keys[u];
+            rank += (ku < ki || (ku == ki && u < i)) ? 1 : 0;
+          }
+          dst[rank] = ki;
+        }
+      } else {
+        for (int kk = 2; kk <= S2; kk <<= 1) {
+          for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+            for (int i = tid; i < S2; i += SB_THREADS) {
+              const int ixj = i ^ jj;
+              if (ixj > i) {
+                const uint32_t x = keys[i], y = keys[ixj];
+                if ((x > y) == ((i & kk) == 0)) {
+                  keys[i] = y;
+                  keys[ixj] = x;
+                }
               }
             }
+            __syncthreads();
           }
-          __syncthreads();
         }
+        for (int i = tid; i < S_b; i += SB_THREADS) dst[i] = keys[i];
       }
-      for (int i = tid; i < S_b; i += SB_THREADS) a.ukeys[bh * a.S_max + i] = keys[i];
-      __syncthreads();
+      __syncthreads();   // keys is rewritten for the next head
     }
   }
 
