@@ -304,7 +304,9 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "variant": wl.variant, "S": wl.S, "nk": wl.nk},
+        "config": {"workload": wl.name, "variant": wl.variant, "S": inp.S_max, "nk": wl.nk, "batch": B,
+                   "n_q_heads": H, "n_kv_heads": wl.n_kv_heads, "head_dim": inp.q.shape[2],
+                   "l2": "host memory (CPU oracle)", "parallelism": "single host thread"},
         "cpu_baseline": {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"{per_step} of {len(heads)} heads per step (single thread), "
                                    f"time scaled to all heads"},
