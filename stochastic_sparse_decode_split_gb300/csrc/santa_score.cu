@@ -389,6 +389,14 @@ dense_chunks_kernel(const T* __restrict__ q, const T* __restrict__ K, const T* _
 
   const int64_t tile_off = ((cx.row0 + key0) * Hkv + kvh) * (int64_t)D;
   stage_rows<T, D, SC_THREADS>(kbase, K + tile_off, (int64_t)Hkv * D, len);
+  // start the chunk's V rows towards L2 while its K rows are scored, so that
+  // their staging below waits for L2 rather than HBM
+  {
+    constexpr int LINES = (R::ROWB + 127) / 128;   // 128-byte lines per row
+    const unsigned char* vt = reinterpret_cast<const unsigned char*>(V + tile_off);
+    for (int i = threadIdx.x; i < len * LINES; i += SC_THREADS)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(vt + (int64_t)(i / LINES) * Hkv * R::ROWB + (i % LINES) * 128));
+  }
   load_group_q<T, D>(qs, q, b, H, G, kvh);
   cp_async_wait_all();
   __syncthreads();
