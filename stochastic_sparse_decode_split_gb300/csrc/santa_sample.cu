@@ -277,7 +277,7 @@ sample_gather_kernel(LaunchArgs a) {
   const int w0 = grp * SPC + warp * NSW;   // first window of this warp
   const int cm1 = a.chunks_max + 1;
 
-  // round 1: threshold range [js, je) and mass prefix of every (head, window)
+  // first pass: threshold range [js, je) and mass prefix of every (head, window)
   int js[GM][NSW], je[GM][NSW];
   long long pb[GM][NSW];
   float mst[GM];
@@ -294,7 +294,7 @@ sample_gather_kernel(LaunchArgs a) {
       pb[g][i] = act ? a.prefix[base + 2 * w] : 0;
     }
   }
-  // round 2: scores and first 32 thresholds of the (head, window) pairs that draw
+  // second pass: scores and first 32 thresholds of the (head, window) pairs that draw
   float sv[GM][NSW];
   long long th[GM][NSW];
 #pragma unroll
