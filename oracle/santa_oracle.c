@@ -289,7 +289,7 @@ int santa_oracle_dense_head(const oracle_problem* P, int32_t b, int32_t h, doubl
 /* (App. P, Alg. 6-8)                                                   */
 /* ------------------------------------------------------------------ */
 
-/* App. O, Alg. 4 lines 4-5: q_t = S W_t / Z, S_t = floor(q_t), and the
+/* App. O, Alg. 4: q_t = S W_t / Z, S_t = floor(q_t), and the
  * S - sum_t S_t samples left over go one each to the tiles with the largest
  * fractional parts q_t - S_t (largest remainder).  The pages do not say how
  * equal fractional parts are ordered: the lower tile index goes first. */
@@ -322,8 +322,8 @@ int santa_oracle_prop_budgets(int32_t T, const double* W, int32_t S, int32_t* St
   return 0;
 }
 
-/* Systematic counts inside one tile, App. O, Alg. 5 lines 5-9 (and App. P,
- * Alg. 7 line 8): for the tile's keys in increasing order, x = inv_delta u_n,
+/* Systematic counts inside one tile, App. O, Alg. 5 (and App. P,
+ * Alg. 7): for the tile's keys in increasing order, x = inv_delta u_n,
  * c_n = floor(a0 + p + x) - floor(a0 + p), p <- p + x.  delta_n (if not NULL)
  * is the distance, in units of x, of the integers the key crossed to the
  * nearer end of its interval (a0 + p, a0 + p + x]; -1 where it crossed none. */
@@ -348,12 +348,12 @@ static void tile_counts(int64_t len, const double* u, double inv_delta, double a
 /* One head through a tile sampler.
  *   sampler 0, S2ANTA-prop: integer tile budgets S_t (Alg. 4), then the
  *     systematic counts of Alg. 5 with inv_delta_t = S_t / l_t; est =
- *     (1/S) sum_n c_n V_n (Alg. 2 line 5).
- *   sampler 1, S2ANTA-flash: the same budget S_tile in every tile (Alg. 6
- *     line 1), per-tile counts with inv_delta_t = S_tile / l_t and partial
+ *     (1/S) sum_n c_n V_n (Alg. 2).
+ *   sampler 1, S2ANTA-flash: the same budget S_tile in every tile (Alg. 6),
+ *     per-tile counts with inv_delta_t = S_tile / l_t and partial
  *     O_t = sum_n c_n V_n (Alg. 7), merged as est = (1/Z) sum_t W_t O_t /
  *     S_tile, W_t = exp(m_t - m*) l_t, Z = sum_t W_t (Alg. 8).
- * Tiles are [t L, min((t + 1) L, nk)) for L = tile_len (Alg. 3 line 3); u_n =
+ * Tiles are [t L, min((t + 1) L, nk)) for L = tile_len (Alg. 3); u_n =
  * exp(s_n - m_t).  a0_t is a0[t] when a0 is not NULL, else uniform number t
  * of head (b, h) (the pages draw a0 ~ U[0, 1) per head and tile and name no
  * generator).  Outputs (any may be NULL): est [d]; counts [nk_b]; delta
@@ -392,7 +392,7 @@ int santa_oracle_tiled_head(const oracle_problem* P, int32_t b, int32_t h, int32
     m[t] = mx;
     l[t] = sum;
   }
-  /* global max, tile masses W_t and Z (Alg. 4 lines 2-3; Alg. 8 lines 2-3) */
+  /* global max, tile masses W_t and Z (Alg. 4; Alg. 8) */
   double mstar = m[0];
   for (int64_t t = 1; t < T; ++t) if (m[t] > mstar) mstar = m[t];
   double Z = 0.0;

@@ -44,7 +44,7 @@ __device__ __forceinline__ int64_t seq_rows(const LaunchArgs& a, int b, int64_t&
   return a.nk_max;
 }
 
-// S_tile of S2ANTA-flash: S / T rounded half up, at least 1 (App. P, Alg. 6 line 1).
+// S_tile of S2ANTA-flash: S / T rounded half up, at least 1 (App. P, Alg. 6).
 __device__ __forceinline__ int flash_tile_budget(int S_b, int T) { return max(1, (2 * S_b + T) / (2 * T)); }
 
 struct OpMax {
@@ -70,11 +70,10 @@ __device__ __forceinline__ V_ block_reduce(V_ v, Op op, V_* red) {
   return v;
 }
 
-// Tile masses of one head (App. O, Alg. 4 lines 2-3; App. P, Alg. 8 lines
-// 2-3) from the chunk statistics: m_t = max of the tile's chunk maxima,
-// l_t = sum_c sum_c-chunk * exp(max_c - m_t), W_t = exp(m_t - m*) l_t into
-// w[0..T); returns Z = sum_t W_t (float64 sums of fp32 terms, the same in
-// every call).
+// Tile masses of one head (App. O, Alg. 4; App. P, Alg. 8) from the chunk
+// statistics: m_t = max of the tile's chunk maxima, l_t = sum_c sum_c-chunk *
+// exp(max_c - m_t), W_t = exp(m_t - m*) l_t into w[0..T); returns
+// Z = sum_t W_t (float64 sums of fp32 terms, the same in every call).
 __device__ double tile_masses(const LaunchArgs& a, int64_t bh, int64_t nk, int T, double* w, double* red) {
   const int C = a.tl_len / SUB;
   const int nch = (int)((nk + SUB - 1) / SUB);
@@ -184,7 +183,7 @@ __global__ void __launch_bounds__(TB_THREADS) tiled_budget_kernel(LaunchArgs a) 
 
 // ---------------------------------------------------------------------------
 // Per-tile systematic counts and the count-weighted gather (App. O, Alg. 5;
-// App. P, Alg. 7 line 8).  One CTA per (tile, sequence, KV head): each head
+// App. P, Alg. 7).  One CTA per (tile, sequence, KV head): each head
 // of the group takes its S_t thresholds; then every row drawn by any head is
 // read once and added, times its per-head counts, into the tile's partial
 // sums tl_o[bh][t] (zero for a head with no draws in the tile).
@@ -369,7 +368,7 @@ __global__ void __launch_bounds__(TS_THREADS) tiled_sample_kernel(LaunchArgs a) 
 // ---------------------------------------------------------------------------
 // Merge (one CTA per head, thread per output column): out = sum_t w_t O_t
 // with w_t = 1 / S for prop (tiles with a budget) and W_t / (Z S_tile) for
-// flash (App. P, Alg. 8 line 4).  Also flags bad sequence metadata and marks
+// flash (App. P, Alg. 8).  Also flags bad sequence metadata and marks
 // the unused entries of the head's sample_idx row with -1.
 // ---------------------------------------------------------------------------
 template <int D>

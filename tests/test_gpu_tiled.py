@@ -52,7 +52,7 @@ def run_tiled(inp, sampler, tile_len, seed=0, step=0):
 
 
 def tile_weights(P, b, h, tile_len):
-    """W_t / Z from the oracle's tile statistics (App. O, Alg. 4 lines 2-3)."""
+    """W_t / Z from the oracle's tile statistics (App. O, Alg. 4)."""
     m, l = oracle.tile_stats(P, b, h, tile_len)
     W = np.exp(m - m.max()) * l
     return W / W.sum()
