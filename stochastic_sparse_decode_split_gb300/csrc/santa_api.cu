@@ -296,7 +296,9 @@ santa_status_t santa_decode_bernoulli(const santa_params_t* p, int32_t variant, 
   santa_status_t st = check_params(p, true);
   if (st != SANTA_OK) return st;
   if (n_samples < 1 || n_samples > 1024) return SANTA_ERR_INVALID_ARG;
+  if (variant < SANTA_IID || variant > SANTA_SYSTEMATIC) return SANTA_ERR_INVALID_ARG;
   if (feature_counts && !aligned(feature_counts, 4)) return SANTA_ERR_INVALID_ARG;
+  if (sample_idx && !aligned(sample_idx, 4)) return SANTA_ERR_INVALID_ARG;
   const size_t need = santa_bernoulli_workspace_size(p);
   st = check_buffers(q, K, V, out, workspace, ws_bytes, need);
   if (st != SANTA_OK) return st;

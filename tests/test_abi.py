@@ -102,3 +102,43 @@ def test_python_binding_rejects_cpu_tensors():
     K = torch.zeros(16, 1, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         santa.santa_decode(q, K, K, S=4)
+
+
+def test_host_validation_of_the_tile_samplers_bernoulli_and_helpers(lib):
+    """The other entry points' argument checks, all before any CUDA call."""
+    vp = ctypes.c_void_p
+    good = params()
+    n_t = santa.tiled_workspace_size(good, "prop", 256)
+    assert n_t > santa.workspace_size(good)
+    assert santa.tiled_max_draws(good, "prop", 256) == good.S
+    assert santa.tiled_max_draws(good, "flash", 256) == good.S + 32768 // 256
+    for L in (0, 8, 24, 2048):
+        assert santa.tiled_workspace_size(good, "prop", L) == 0
+    assert lib.santa_tiled_workspace_size(ctypes.byref(good), 2, 256) == 0           # no third sampler
+
+    def tiled(p=good, sampler=0, L=256, q=256, ws=512, nbytes=n_t):
+        return lib.santa_decode_tiled(ctypes.byref(p), sampler, L, vp(q), vp(256), vp(256), vp(256), vp(ws), nbytes,
+                                      None, None)
+    assert tiled(L=40) == INVALID
+    assert tiled(sampler=5) == INVALID
+    assert tiled(p=params(S=0)) == INVALID
+    assert tiled(q=0) == INVALID
+    assert tiled(nbytes=n_t - 256) == WORKSPACE
+
+    n_b = santa.bernoulli_workspace_size(good)
+    assert n_b > santa.workspace_size(good)
+
+    def bern(n=4, variant=2, ws=512, nbytes=n_b):
+        return lib.santa_decode_bernoulli(ctypes.byref(good), variant, n, 1, vp(256), vp(256), vp(256), vp(256),
+                                          vp(ws), nbytes, None, None, None)
+    assert bern(n=0) == INVALID and bern(n=1025) == INVALID
+    assert bern(variant=7) == INVALID
+    assert bern(nbytes=n_b - 256) == WORKSPACE
+
+    assert lib.santa_read_probe(None, 1024, vp(256), None) == INVALID
+    assert lib.santa_read_probe(vp(256), 1000, vp(256), None) == INVALID               # not a multiple of 16
+    assert lib.santa_read_probe(vp(264), 1024, vp(256), None) == INVALID               # not 16-byte aligned
+    assert lib.santa_read_probe_sink_words() >= 2 * 512
+    assert lib.santa_selftest_wait_timeout(None, 4096, 50_000_000, None) == WORKSPACE
+    assert lib.santa_selftest_wait_timeout(vp(512), 4096, 10, None) == INVALID          # below 1 ms
+    assert lib.santa_selftest_wait_timeout(vp(512), 4096, 3_000_000_000, None) == INVALID
