@@ -170,6 +170,8 @@ GRID = [
     (1, 4, 1, 128, 257, "bf16", 4096, "stratified"),    # maximum S
     (1, 6, 2, 128, 2049, "bf16", 100, "iid"),           # group 3
     (3, 10, 2, 64, 777, "fp32", 33, "stratified"),      # group 5
+    (2, 15, 3, 128, 1800, "bf16", 128, "systematic"),   # 3 KV heads: units of one head, group 5
+    (1, 12, 6, 64, 2500, "fp16", 64, "iid"),            # 6 KV heads: units of two heads, group 2
 ]
 
 
