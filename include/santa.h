@@ -57,7 +57,7 @@ typedef enum { SANTA_BF16 = 0, SANTA_FP16 = 1, SANTA_FP32 = 2 } santa_dtype_t;
 typedef enum {
   SANTA_OK = 0,
   SANTA_ERR_INVALID_ARG = 1, /* NULL pointer, bad shape, misalignment, S or nk out of range */
-  SANTA_ERR_UNSUPPORTED = 2, /* head_dim / dtype / group size this build does not provide */
+  SANTA_ERR_UNSUPPORTED = 2, /* head_dim / dtype / group size the library does not provide */
   SANTA_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned or smaller than *_workspace_size */
   SANTA_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch, copy, sync) */
   SANTA_ERR_DEVICE = 5,      /* the device flagged bad ragged metadata (see santa_get_error) */
@@ -79,7 +79,7 @@ typedef struct {
   uint32_t step;             /* decode step, part of the Philox counter */
 } santa_params_t;
 
-/* Limits of this build. */
+/* Limits of the library. */
 #define SANTA_MAX_S 4096        /* S (and every S_b) */
 #define SANTA_MAX_NK (1 << 21)  /* keys per sequence */
 #define SANTA_MAX_GROUP 8       /* n_q_heads / n_kv_heads */
