@@ -30,8 +30,9 @@
  *
  * Errors: arguments are validated on the host before any launch and reported
  * as a status.  Conditions only visible on the device (a ragged length above
- * the stated bound, a per-sequence budget out of range) set an error word in
- * the workspace and leave that head's output zero; santa_get_error reports it.
+ * the stated bound or empty, a per-sequence budget out of range) set an error
+ * word in the workspace (SANTA_DEVERR_* bits) and leave the heads of that
+ * sequence zero; santa_get_error reports it.
  * Kernels never trap.
  */
 #ifndef SANTA_H
@@ -215,9 +216,16 @@ typedef struct {
 } santa_ws_layout_t;
 int32_t santa_workspace_layout(const santa_params_t* p, santa_ws_layout_t* layout);
 
+/* Bits of the device error word (the *code of santa_get_error).  A flagged
+ * sequence's heads come out zero; the other sequences are computed as usual. */
+#define SANTA_DEVERR_NK_BOUND 1 /* nk_b = kv_offsets[b+1] - kv_offsets[b] above p->nk, or kv_offsets[b] < 0 */
+#define SANTA_DEVERR_S_RANGE 2  /* S_per_seq[b] outside [1, S] */
+#define SANTA_DEVERR_EMPTY 4    /* a sequence with no keys (nk_b < 1): its softmax is undefined */
+#define SANTA_DEVERR_TIMEOUT 8  /* a bounded grid-wide wait ran out (the single-launch paths) */
+
 /* Synchronises `stream`, reads and clears the workspace error word.
  * Returns SANTA_OK, SANTA_ERR_DEVICE (device flagged bad metadata; *code gets
- * the flag bits when code != NULL) or SANTA_ERR_CUDA. */
+ * the SANTA_DEVERR_* bits when code != NULL) or SANTA_ERR_CUDA. */
 santa_status_t santa_get_error(void* workspace, santa_stream_t stream, int32_t* code);
 
 /* santa_decode without a caller-supplied workspace, for callers that cannot
@@ -259,7 +267,7 @@ santa_status_t santa_read_probe(const void* src, size_t bytes, uint32_t* sink, s
 /* Self-test of the bounded grid-barrier wait (no counterpart in the paper):
  * one CTA waits on the workspace's barrier generation word, which nothing
  * advances, for limit_ns nanoseconds (1 ms .. 2 s) of %globaltimer time; the
- * wait must then end with ERR_TIMEOUT (8) in the workspace error word, read
+ * wait must then end with SANTA_DEVERR_TIMEOUT in the workspace error word, read
  * by santa_get_error, and the GPU context stays usable.  The workspace (at
  * least 256 bytes, initialised) must not be in use by a decode meanwhile. */
 santa_status_t santa_selftest_wait_timeout(void* workspace, size_t ws_bytes, uint64_t limit_ns,

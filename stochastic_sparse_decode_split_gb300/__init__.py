@@ -38,6 +38,8 @@ DTYPES = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "santa.h")
 
 SANTA_OK, SANTA_ERR_DEVICE = 0, 5
+# bits of the device error word returned by get_error (SANTA_DEVERR_* in santa.h)
+DEVERR_NK_BOUND, DEVERR_S_RANGE, DEVERR_EMPTY, DEVERR_TIMEOUT = 1, 2, 4, 8
 
 
 class SantaError(RuntimeError):

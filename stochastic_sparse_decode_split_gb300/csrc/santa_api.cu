@@ -12,6 +12,9 @@
 static_assert(SANTA_MAX_GROUP == SANTA_MAX_GROUP_DEV, "group limit");
 static_assert(SANTA_CHUNK == santa::SUB, "chunk length");
 static_assert(SANTA_MAX_TILE == santa::TL_MAX_LEN, "tile length");
+static_assert(SANTA_DEVERR_NK_BOUND == santa::ERR_NK_BOUND && SANTA_DEVERR_S_RANGE == santa::ERR_S_RANGE &&
+                  SANTA_DEVERR_EMPTY == santa::ERR_EMPTY && SANTA_DEVERR_TIMEOUT == santa::ERR_TIMEOUT,
+              "device error bits");
 
 namespace {
 

@@ -39,6 +39,18 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, n)
 
 
+def test_device_error_bits_match_the_header():
+    """The binding's DEVERR_* constants are the header's SANTA_DEVERR_* values
+    (the library itself static_asserts the header against the kernels)."""
+    import os
+    import re
+    hdr = open(os.path.join(santa_build.ROOT, "include", "santa.h")).read()
+    found = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define SANTA_DEVERR_(\w+) (\d+)", hdr)}
+    assert found == {"NK_BOUND": santa.DEVERR_NK_BOUND, "S_RANGE": santa.DEVERR_S_RANGE,
+                     "EMPTY": santa.DEVERR_EMPTY, "TIMEOUT": santa.DEVERR_TIMEOUT}
+    assert sorted(found.values()) == [1, 2, 4, 8]
+
+
 def test_status_strings_and_version(lib):
     for code in range(6):
         assert lib.santa_status_string(code)

@@ -240,6 +240,43 @@ def test_device_flags_bad_ragged_metadata():
     assert torch.count_nonzero(out[1]) == 0 and torch.count_nonzero(out[0]) > 0
 
 
+@pytest.mark.parametrize("dtype,variant", [("bf16", "systematic"), ("bf16", "iid"), ("fp32", "stratified")])
+def test_empty_sequence_in_a_ragged_batch(dtype, variant):
+    """A sequence with no keys has no softmax: it is flagged DEVERR_EMPTY, its
+    heads come out zero with sample_idx rows -1, and the sequences around it
+    match the oracle (bf16 takes the single launch, fp32 the staged path)."""
+    wl = wl_of("empty", 3, 8, 2, 128, 700, dtype, 48, variant, ragged=(700, 700))
+    inp = synth.generate(wl, 2)
+    t = synth.to_torch(inp)
+    offs_np = np.array([0, 700, 700, 1400], dtype=np.int64)   # sequence 1 is empty
+    offs = torch.tensor(offs_np, device="cuda")
+    p = santa.make_params(t["q"], t["K"], 48, nk=700, kv_offsets=offs)
+    ws = santa.alloc_workspace(santa.workspace_size(p), "cuda")
+    idx = torch.full((3, 8, 48), -7, dtype=torch.int32, device="cuda")
+    seed = 5
+    out = santa.santa_decode(t["q"], t["K"], t["V"], S=48, variant=variant, seed=seed, nk=700, kv_offsets=offs,
+                             sample_idx=idx, workspace=ws)
+    assert santa.get_error(ws) == santa.DEVERR_EMPTY
+    out, idx = out.double().cpu().numpy(), idx.cpu().numpy()
+    assert np.count_nonzero(out[1]) == 0 and np.all(idx[1] == -1)
+    P = oracle.Problem(inp.q, inp.K, inp.V, offs_np, dtype, 2)
+    for b in (0, 2):
+        for h in range(8):
+            est, J, delta = oracle.decode_head(P, variant, 48, seed, b, h)   # i.i.d. thresholds come sorted
+            strict = delta > BAND
+            assert np.all(idx[b, h][strict] == J[strict]), (b, h)
+            if np.array_equal(idx[b, h], J):
+                rel = np.linalg.norm(out[b, h] - est) / np.linalg.norm(est)
+                assert rel <= OUT_TOL, (b, h, rel)
+    dense = santa.santa_dense_decode(t["q"], t["K"], t["V"], nk=700, kv_offsets=offs)
+    assert torch.count_nonzero(dense[1]) == 0 and torch.count_nonzero(dense[0]) > 0
+    tws = santa.alloc_workspace(santa.tiled_workspace_size(p, "prop", 64), "cuda")
+    tiled = santa.santa_decode_tiled(t["q"], t["K"], t["V"], S=48, sampler="prop", tile_len=64, nk=700,
+                                     kv_offsets=offs, workspace=tws)
+    assert santa.get_error(tws) == santa.DEVERR_EMPTY
+    assert torch.count_nonzero(tiled[1]) == 0 and torch.count_nonzero(tiled[2]) > 0
+
+
 # ---------------------------------------------------------------------------
 # full-size workloads (every head checked)
 # ---------------------------------------------------------------------------
