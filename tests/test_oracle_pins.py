@@ -726,3 +726,19 @@ def test_bernoulli_score_error_reproduces_fig6(oracle_lib):
     assert abs(slope(err[False]) + 0.5) < 0.1 and abs(slope(err[True]) + 1.0) < 0.15, err
     print("\nBernoulli score error (B = 4, 16, 64): plain %s, stratified %s"
           % ([round(err[False][b], 3) for b in (4, 16, 64)], [round(err[True][b], 3) for b in (4, 16, 64)]))
+
+
+def test_empty_sequence_is_rejected(oracle_lib):
+    """A sequence with no keys has no softmax (Eq. 1 normalises over an empty
+    set): the oracle refuses it rather than invent an output, for the
+    whole-step decode and for a single head, and still serves the others."""
+    rng = np.random.default_rng(3)
+    q = rng.standard_normal((2, 2, 64)).astype(np.float32)
+    K = rng.standard_normal((40, 1, 64)).astype(np.float32)
+    P = oracle_lib.Problem(q, K, K, np.array([0, 40, 40], np.int64), "fp32", 1)
+    with pytest.raises(ValueError):
+        oracle_lib.decode_head(P, "systematic", 4, 0, 1, 0)
+    with pytest.raises(ValueError):
+        oracle_lib.decode(P, "systematic", 4, 0)
+    est, J, _ = oracle_lib.decode_head(P, "systematic", 4, 0, 0, 1)
+    assert np.all((J >= 0) & (J < 40)) and np.all(np.isfinite(est))
