@@ -466,27 +466,56 @@ def run_ours(args):
     n_dense = min(args.steps, 1000)
     dms = timed_loop(lambda i: denses[i % R](), n_dense, args.warmup)
 
-    # end to end through the public API with host buffers: H2D of q, K, V from
-    # pinned memory, the decode, D2H of the output, all inside the timed region
-    e2e = None
+    # end to end through the public API with host buffers, the D2H of the
+    # output inside the timed region.  e2e: the cache stays in pinned host
+    # memory and santa_decode_host_kv reads K and the drawn V rows in place
+    # (H2D bytes: q, K, the unique drawn V rows); R pinned replicas are used in
+    # turn as on the device, so no step finds its cache in L2.  e2e_copy: the
+    # whole cache copied to the device first, then santa_decode.
+    e2e = e2e_copy = None
     if not args.no_e2e:
-        hq, hK, hV = (x.cpu().pin_memory() for x in (t["q"], t["K"], t["V"]))
+        hq = t["q"].cpu().pin_memory()
         hout = torch.empty((B, H, d), dtype=torch.float32).pin_memory()
-        dq, dK, dV = torch.empty_like(t["q"]), torch.empty_like(t["K"]), torch.empty_like(t["V"])
+        dq = torch.empty_like(t["q"])
+        n_e2e = min(args.steps, 200)
+        row_bytes = d * t["V"].element_size()
+        q_bytes = hq.numel() * hq.element_size()
+        k_bytes = t["K"].numel() * t["K"].element_size()
+        d2h = hout.numel() * hout.element_size()
+
+        hreps = [(Kr.cpu().pin_memory(), Vr.cpu().pin_memory()) for (Kr, Vr) in reps]
+        ws_h = santa.alloc_workspace(dec.workspace.numel(), dev)
+        out_h = torch.empty((B, H, d), dtype=torch.float32, device=dev)
+
+        def e2e_host_step(i):
+            dq.copy_(hq, non_blocking=True)
+            hK, hV = hreps[i % len(hreps)]
+            santa.santa_decode_host_kv(dq, hK, hV, S=S_max, variant=wl.variant, seed=0, out=out_h, workspace=ws_h,
+                                       S_per_seq=t["S_per_seq"], **kw)
+            hout.copy_(out_h, non_blocking=True)
+
+        ems = timed_loop(e2e_host_step, n_e2e, 3)
+        e2e = {"value": statistics.mean(ems) * 1e3 / world, "unit": UNIT,
+               "h2d_bytes_per_step": q_bytes + k_bytes + unique_rows * row_bytes, "d2h_bytes_per_step": d2h,
+               "mode": "K/V cache in pinned host memory, read in place (santa_decode_host_kv)",
+               "replicas": len(hreps)}
+        del hreps
+
+        hK, hV = t["K"].cpu().pin_memory(), t["V"].cpu().pin_memory()
+        dK, dV = torch.empty_like(t["K"]), torch.empty_like(t["V"])
         dec_e = santa.Decoder(dq, dK, dV, S=S_max, variant=wl.variant, seed=0, S_per_seq=t["S_per_seq"], **kw)
 
-        def e2e_step(i):
+        def e2e_copy_step(i):
             dq.copy_(hq, non_blocking=True)
             dK.copy_(hK, non_blocking=True)
             dV.copy_(hV, non_blocking=True)
             o = dec_e(step=0)
             hout.copy_(o, non_blocking=True)
 
-        n_e2e = min(args.steps, 200)
-        ems = timed_loop(e2e_step, n_e2e, 3)
-        h2d = sum(x.numel() * x.element_size() for x in (hq, hK, hV))
-        e2e = {"value": statistics.mean(ems) * 1e3 / world, "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": hout.numel() * hout.element_size()}
+        ems = timed_loop(e2e_copy_step, n_e2e, 3)
+        e2e_copy = {"value": statistics.mean(ems) * 1e3 / world, "unit": UNIT,
+                    "h2d_bytes_per_step": q_bytes + 2 * k_bytes, "d2h_bytes_per_step": d2h,
+                    "mode": "q, K, V copied from pinned host memory, then santa_decode"}
 
     peak, peak_kind = hbm_peak()
     sb = score_pass_bytes(inp)
@@ -534,6 +563,7 @@ def run_ours(args):
                   "speedup_santa_vs_dense": statistics.mean(dms) / mean_ms},
         "cpu_baseline": cpu_baseline,
         "e2e": e2e,
+        "e2e_copy": e2e_copy,
         "gpu_launches": (1 if single else 3) * args.steps,
         "clocks": clocks,
     }

@@ -111,6 +111,22 @@ santa_status_t santa_decode(const santa_params_t* p, int32_t variant, const void
                             const void* V, float* out, void* workspace, size_t ws_bytes,
                             santa_stream_t stream, int32_t* sample_idx);
 
+/* santa_decode with the K/V cache left in host memory.  K_host and V_host are
+ * page-locked host buffers (cudaHostAlloc / cudaMallocHost, or host memory
+ * registered with cudaHostRegister) in the K/V layout above, covering every
+ * row the offsets name; the GPU reads them in place through their mapped
+ * device addresses, so one step moves K once and, of V, only the drawn rows
+ * across the host link instead of copying the whole cache first.  This is the
+ * sparse read of V (Sec. 2.2, Eq. 4) carried over to a cache kept in host
+ * memory.  q, out, workspace, sample_idx, kv_offsets and S_per_seq are device
+ * memory as in santa_decode, and the results equal santa_decode's on the same
+ * data.  Returns SANTA_ERR_INVALID_ARG, before any launch, when K_host or
+ * V_host is not page-locked host memory that the device can address
+ * (pageable or device memory included). */
+santa_status_t santa_decode_host_kv(const santa_params_t* p, int32_t variant, const void* q, const void* K_host,
+                                    const void* V_host, float* out, void* workspace, size_t ws_bytes,
+                                    santa_stream_t stream, int32_t* sample_idx);
+
 /* santa_decode that also records stage_events[i] (cudaEvent_t, created by the
  * caller) on `stream` before stage i (0 score pass, 1 combine, 2 sample and
  * gather) and stage_events[3] after the last stage, so a caller can time each

@@ -26,7 +26,8 @@ import torch
 from .build import LIB as _LIB_PATH
 
 __all__ = [
-    "SantaError", "Params", "library", "santa_decode", "santa_decode_with_uniforms", "santa_dense_decode",
+    "SantaError", "Params", "library", "santa_decode", "santa_decode_host_kv", "santa_decode_with_uniforms",
+    "santa_dense_decode",
     "workspace_size", "dense_workspace_size", "workspace_layout", "get_error", "Decoder", "exported_symbols",
     "VARIANTS", "DTYPES", "santa_decode_static", "static_scratch_bytes", "SAMPLERS", "santa_decode_tiled",
     "tiled_workspace_size", "tiled_max_draws", "santa_decode_bernoulli", "bernoulli_workspace_size",
@@ -92,6 +93,7 @@ def library():
             lib.santa_dense_workspace_size.restype = sz
             lib.santa_workspace_init.argtypes = [vp, sz, vp]
             lib.santa_decode.argtypes = [P, i32, vp, vp, vp, vp, vp, sz, vp, vp]
+            lib.santa_decode_host_kv.argtypes = [P, i32, vp, vp, vp, vp, vp, sz, vp, vp]
             lib.santa_decode_profiled.argtypes = [P, i32, vp, vp, vp, vp, vp, sz, vp, vp, vp]
             lib.santa_score_pass.argtypes = [P, vp, vp, vp, sz, vp]
             lib.santa_decode_with_uniforms.argtypes = [P, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp]
@@ -115,7 +117,8 @@ def library():
             lib.santa_status_string.argtypes = [i32]
             lib.santa_status_string.restype = ctypes.c_char_p
             lib.santa_version.restype = i32
-            for fn in ("santa_workspace_init", "santa_decode", "santa_decode_profiled", "santa_score_pass",
+            for fn in ("santa_workspace_init", "santa_decode", "santa_decode_host_kv", "santa_decode_profiled",
+                       "santa_score_pass",
                        "santa_decode_with_uniforms", "santa_dense_decode", "santa_decode_static",
                        "santa_workspace_layout", "santa_get_error", "santa_decode_tiled", "santa_decode_bernoulli"):
                 getattr(lib, fn).restype = i32
@@ -221,6 +224,28 @@ def santa_decode(q, K, V, S: int, variant: str = "systematic", seed: int = 0, st
                                 _ptr(workspace), workspace.numel(), _stream(stream), _ptr(sample_idx))
     if st != SANTA_OK:
         raise SantaError(st, "santa_decode")
+    return out
+
+
+def santa_decode_host_kv(q, K, V, S: int, variant: str = "systematic", seed: int = 0, step: int = 0, out=None,
+                         nk: Optional[int] = None, kv_offsets=None, S_per_seq=None, scale: float = 0.0,
+                         workspace=None, sample_idx=None, stream=None) -> torch.Tensor:
+    """santa_decode with K and V left in page-locked host memory (contiguous
+    pinned CPU tensors); the GPU reads K and the drawn V rows in place.  q and
+    the optional tensors are CUDA tensors as in santa_decode."""
+    _check_tensors(q, out, kv_offsets, S_per_seq, sample_idx)
+    for t in (K, V):
+        if t.is_cuda or not t.is_contiguous() or not t.is_pinned():
+            raise ValueError("K and V must be contiguous pinned CPU tensors")
+    p = make_params(q, K, S, seed, step, nk, kv_offsets, S_per_seq, scale)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(workspace_size(p), q.device)
+    st = library().santa_decode_host_kv(ctypes.byref(p), VARIANTS[variant], _ptr(q), _ptr(K), _ptr(V), _ptr(out),
+                                        _ptr(workspace), workspace.numel(), _stream(stream), _ptr(sample_idx))
+    if st != SANTA_OK:
+        raise SantaError(st, "santa_decode_host_kv")
     return out
 
 

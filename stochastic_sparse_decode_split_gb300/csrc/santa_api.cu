@@ -231,6 +231,32 @@ santa_status_t santa_decode(const santa_params_t* p, int32_t variant, const void
   return decode_impl(p, variant, q, K, V, nullptr, out, workspace, ws_bytes, stream, sample_idx);
 }
 
+// The device address of page-locked host memory (cudaHostAlloc'd or
+// cudaHostRegister'ed, mapped), or INVALID_ARG for anything else: pageable
+// memory, device memory, a pointer CUDA does not know.  Nothing is launched.
+static santa_status_t mapped_host(const void* h, const void** d) {
+  if (!h) return SANTA_ERR_INVALID_ARG;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, h) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return SANTA_ERR_INVALID_ARG;
+  }
+  if (at.type != cudaMemoryTypeHost || !at.devicePointer) return SANTA_ERR_INVALID_ARG;
+  *d = at.devicePointer;
+  return SANTA_OK;
+}
+
+santa_status_t santa_decode_host_kv(const santa_params_t* p, int32_t variant, const void* q, const void* K_host,
+                                    const void* V_host, float* out, void* workspace, size_t ws_bytes,
+                                    santa_stream_t stream, int32_t* sample_idx) {
+  santa_status_t st = check_params(p, true);
+  if (st != SANTA_OK) return st;
+  if (!K_host || !V_host) return SANTA_ERR_INVALID_ARG;
+  const void *K = nullptr, *V = nullptr;
+  if ((st = mapped_host(K_host, &K)) != SANTA_OK || (st = mapped_host(V_host, &V)) != SANTA_OK) return st;
+  return decode_impl(p, variant, q, K, V, nullptr, out, workspace, ws_bytes, stream, sample_idx);
+}
+
 santa_status_t santa_score_pass(const santa_params_t* p, const void* q, const void* K, void* workspace,
                                 size_t ws_bytes, santa_stream_t stream) {
   return decode_impl(p, SANTA_SYSTEMATIC, q, K, K, nullptr, nullptr, workspace, ws_bytes, stream, nullptr, nullptr,

@@ -106,6 +106,13 @@ def test_host_validation_statuses(lib):
                                   1 << 30, None) == UNSUPPORTED
     assert lib.santa_workspace_init(None, 1024, None) == WORKSPACE
     assert lib.santa_get_error(vp(512 + 8), None, None) == WORKSPACE
+    # host-resident K/V: parameters and NULL buffers are refused before the pointer queries
+    assert lib.santa_decode_host_kv(ctypes.byref(params(batch=0)), 2, vp(256), vp(256), vp(256), vp(256), vp(512),
+                                    n, None, None) == INVALID
+    assert lib.santa_decode_host_kv(ctypes.byref(good), 2, vp(256), None, vp(256), vp(256), vp(512), n, None,
+                                    None) == INVALID
+    assert lib.santa_decode_host_kv(ctypes.byref(good), 2, vp(256), vp(256), None, vp(256), vp(512), n, None,
+                                    None) == INVALID
 
 
 def test_python_binding_rejects_cpu_tensors():
