@@ -111,20 +111,21 @@ santa_status_t santa_decode(const santa_params_t* p, int32_t variant, const void
                             const void* V, float* out, void* workspace, size_t ws_bytes,
                             santa_stream_t stream, int32_t* sample_idx);
 
-/* santa_decode with the K/V cache left in host memory.  K_host and V_host are
- * page-locked host buffers (cudaHostAlloc / cudaMallocHost, or host memory
- * registered with cudaHostRegister) in the K/V layout above, covering every
- * row the offsets name; the GPU reads them in place through their mapped
- * device addresses, so one step moves K once and, of V, only the drawn rows
- * across the host link instead of copying the whole cache first.  This is the
- * sparse read of V (Sec. 2.2, Eq. 4) carried over to a cache kept in host
- * memory.  q, out, workspace, sample_idx, kv_offsets and S_per_seq are device
- * memory as in santa_decode, and the results equal santa_decode's on the same
- * data.  Returns SANTA_ERR_INVALID_ARG, before any launch, when K_host or
- * V_host is not page-locked host memory that the device can address
- * (pageable or device memory included). */
-santa_status_t santa_decode_host_kv(const santa_params_t* p, int32_t variant, const void* q, const void* K_host,
-                                    const void* V_host, float* out, void* workspace, size_t ws_bytes,
+/* santa_decode with the K/V cache wholly or partly in host memory.  K and V
+ * are each device memory or page-locked host memory (cudaHostAlloc /
+ * cudaMallocHost, or host memory registered with cudaHostRegister), in the
+ * K/V layout above and covering every row the offsets name; the GPU reads host
+ * buffers in place through their mapped device addresses.  A step reads K in
+ * full but, of V, only the drawn rows (Sec. 2.2, Eq. 4), so V can stay in
+ * host memory at the cost of a few hundred row reads across the host link
+ * while K stays in (or is copied to) device memory; both in host memory also
+ * works.  q, out, workspace, sample_idx, kv_offsets and S_per_seq are device
+ * memory as in santa_decode, and the drawn keys equal santa_decode's on the
+ * same data.  Returns SANTA_ERR_INVALID_ARG, before any launch, when K or V is
+ * neither device memory nor page-locked host memory that the device can
+ * address (pageable memory, for one). */
+santa_status_t santa_decode_host_kv(const santa_params_t* p, int32_t variant, const void* q, const void* K,
+                                    const void* V, float* out, void* workspace, size_t ws_bytes,
                                     santa_stream_t stream, int32_t* sample_idx);
 
 /* santa_decode that also records stage_events[i] (cudaEvent_t, created by the

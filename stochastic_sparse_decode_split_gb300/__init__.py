@@ -230,13 +230,13 @@ def santa_decode(q, K, V, S: int, variant: str = "systematic", seed: int = 0, st
 def santa_decode_host_kv(q, K, V, S: int, variant: str = "systematic", seed: int = 0, step: int = 0, out=None,
                          nk: Optional[int] = None, kv_offsets=None, S_per_seq=None, scale: float = 0.0,
                          workspace=None, sample_idx=None, stream=None) -> torch.Tensor:
-    """santa_decode with K and V left in page-locked host memory (contiguous
-    pinned CPU tensors); the GPU reads K and the drawn V rows in place.  q and
-    the optional tensors are CUDA tensors as in santa_decode."""
+    """santa_decode with K and V each either a CUDA tensor or a contiguous
+    pinned CPU tensor, read in place by the GPU (of V only the drawn rows).
+    q and the optional tensors are CUDA tensors as in santa_decode."""
     _check_tensors(q, out, kv_offsets, S_per_seq, sample_idx)
     for t in (K, V):
-        if t.is_cuda or not t.is_contiguous() or not t.is_pinned():
-            raise ValueError("K and V must be contiguous pinned CPU tensors")
+        if not t.is_contiguous() or not (t.is_cuda or t.is_pinned()):
+            raise ValueError("K and V must be contiguous CUDA or pinned CPU tensors")
     p = make_params(q, K, S, seed, step, nk, kv_offsets, S_per_seq, scale)
     if out is None:
         out = torch.empty(q.shape, dtype=torch.float32, device=q.device)

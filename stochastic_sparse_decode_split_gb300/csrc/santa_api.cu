@@ -231,30 +231,36 @@ santa_status_t santa_decode(const santa_params_t* p, int32_t variant, const void
   return decode_impl(p, variant, q, K, V, nullptr, out, workspace, ws_bytes, stream, sample_idx);
 }
 
-// The device address of page-locked host memory (cudaHostAlloc'd or
-// cudaHostRegister'ed, mapped), or INVALID_ARG for anything else: pageable
-// memory, device memory, a pointer CUDA does not know.  Nothing is launched.
-static santa_status_t mapped_host(const void* h, const void** d) {
+// The address the device reads a K or V buffer through: device (or managed)
+// memory as it is, page-locked host memory (cudaHostAlloc'd or
+// cudaHostRegister'ed) through its mapped device address; INVALID_ARG for
+// anything else (pageable memory, a pointer CUDA does not know).  Nothing is
+// launched.
+static santa_status_t kv_address(const void* h, const void** d) {
   if (!h) return SANTA_ERR_INVALID_ARG;
   cudaPointerAttributes at;
   if (cudaPointerGetAttributes(&at, h) != cudaSuccess) {
     (void)cudaGetLastError();
     return SANTA_ERR_INVALID_ARG;
   }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) {
+    *d = h;
+    return SANTA_OK;
+  }
   if (at.type != cudaMemoryTypeHost || !at.devicePointer) return SANTA_ERR_INVALID_ARG;
   *d = at.devicePointer;
   return SANTA_OK;
 }
 
-santa_status_t santa_decode_host_kv(const santa_params_t* p, int32_t variant, const void* q, const void* K_host,
-                                    const void* V_host, float* out, void* workspace, size_t ws_bytes,
+santa_status_t santa_decode_host_kv(const santa_params_t* p, int32_t variant, const void* q, const void* K,
+                                    const void* V, float* out, void* workspace, size_t ws_bytes,
                                     santa_stream_t stream, int32_t* sample_idx) {
   santa_status_t st = check_params(p, true);
   if (st != SANTA_OK) return st;
-  if (!K_host || !V_host) return SANTA_ERR_INVALID_ARG;
-  const void *K = nullptr, *V = nullptr;
-  if ((st = mapped_host(K_host, &K)) != SANTA_OK || (st = mapped_host(V_host, &V)) != SANTA_OK) return st;
-  return decode_impl(p, variant, q, K, V, nullptr, out, workspace, ws_bytes, stream, sample_idx);
+  if (!K || !V) return SANTA_ERR_INVALID_ARG;
+  const void *Kd = nullptr, *Vd = nullptr;
+  if ((st = kv_address(K, &Kd)) != SANTA_OK || (st = kv_address(V, &Vd)) != SANTA_OK) return st;
+  return decode_impl(p, variant, q, Kd, Vd, nullptr, out, workspace, ws_bytes, stream, sample_idx);
 }
 
 santa_status_t santa_score_pass(const santa_params_t* p, const void* q, const void* K, void* workspace,

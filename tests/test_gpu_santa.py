@@ -279,35 +279,36 @@ def test_empty_sequence_in_a_ragged_batch(dtype, variant):
 
 @pytest.mark.parametrize("dtype,variant", [("bf16", "systematic"), ("fp16", "iid"), ("fp32", "stratified")])
 def test_host_resident_kv(dtype, variant):
-    """santa_decode_host_kv reads K and V from pinned host memory in place: it
-    draws the keys santa_decode draws on device copies of the same cache, its
-    output agrees (the gather's fp32 additions may land in another order) and
-    matches the oracle.  Device and pageable host buffers are refused before
+    """santa_decode_host_kv reads K and V in place, each from pinned host or
+    device memory: with V in host memory (K on the device, or both in host
+    memory) it draws the keys santa_decode draws on device copies of the same
+    cache, its output agrees (the gather's fp32 additions may land in another
+    order) and matches the oracle.  Pageable host buffers are refused before
     any launch."""
     inp = synth.generate(wl_of("hostkv", 2, 8, 2, 128, 3000, dtype, 64, variant), 6)
     t = synth.to_torch(inp)
     hK, hV = t["K"].cpu().pin_memory(), t["V"].cpu().pin_memory()
     idx_d = torch.full((2, 8, 64), -7, dtype=torch.int32, device="cuda")
-    idx_h = torch.full((2, 8, 64), -7, dtype=torch.int32, device="cuda")
     out_d = santa.santa_decode(t["q"], t["K"], t["V"], S=64, variant=variant, seed=4, sample_idx=idx_d)
-    out_h = santa.santa_decode_host_kv(t["q"], hK, hV, S=64, variant=variant, seed=4, sample_idx=idx_h)
-    torch.cuda.synchronize()
-    assert torch.equal(idx_d, idx_h)
-    assert float((out_h - out_d).norm() / out_d.norm()) < 1e-6
+    for K_, V_ in ((t["K"], hV), (hK, hV)):
+        idx_h = torch.full((2, 8, 64), -7, dtype=torch.int32, device="cuda")
+        out_h = santa.santa_decode_host_kv(t["q"], K_, V_, S=64, variant=variant, seed=4, sample_idx=idx_h)
+        torch.cuda.synchronize()
+        assert torch.equal(idx_d, idx_h)
+        assert float((out_h - out_d).norm() / out_d.norm()) < 1e-6
     check_parity(inp, variant, 4, out_h.double().cpu().numpy(), idx_h.cpu().numpy())
     lib = santa.library()
     p = santa.make_params(t["q"], t["K"], 64)
     ws = santa.alloc_workspace(santa.workspace_size(p), "cuda")
     out = torch.empty(t["q"].shape, dtype=torch.float32, device="cuda")
-    pageable = t["K"].cpu()
+    pageable = t["V"].cpu()
     vp = ctypes.c_void_p
-    for k_ptr in (t["K"].data_ptr(), pageable.data_ptr()):
-        st = lib.santa_decode_host_kv(ctypes.byref(p), santa.VARIANTS[variant], vp(t["q"].data_ptr()), vp(k_ptr),
-                                      vp(hV.data_ptr()), vp(out.data_ptr()), vp(ws.data_ptr()), ws.numel(),
-                                      vp(torch.cuda.current_stream().cuda_stream), None)
-        assert st == 1, st
+    st = lib.santa_decode_host_kv(ctypes.byref(p), santa.VARIANTS[variant], vp(t["q"].data_ptr()),
+                                  vp(t["K"].data_ptr()), vp(pageable.data_ptr()), vp(out.data_ptr()),
+                                  vp(ws.data_ptr()), ws.numel(), vp(torch.cuda.current_stream().cuda_stream), None)
+    assert st == 1, st
     with pytest.raises(ValueError):
-        santa.santa_decode_host_kv(t["q"], pageable, hV, S=64)
+        santa.santa_decode_host_kv(t["q"], t["K"], pageable, S=64)
 
 
 # ---------------------------------------------------------------------------
