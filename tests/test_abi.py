@@ -2,6 +2,7 @@
 exports every function include/santa.h declares, and rejects bad arguments on
 the host (before any CUDA call) with the documented status codes."""
 import ctypes
+import os
 import subprocess
 
 import pytest
@@ -42,7 +43,6 @@ def test_every_declared_symbol_is_exported(lib):
 def test_device_error_bits_match_the_header():
     """The binding's DEVERR_* constants are the header's SANTA_DEVERR_* values
     (the library itself static_asserts the header against the kernels)."""
-    import os
     import re
     hdr = open(os.path.join(santa_build.ROOT, "include", "santa.h")).read()
     found = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define SANTA_DEVERR_(\w+) (\d+)", hdr)}
@@ -161,3 +161,33 @@ def test_host_validation_of_the_tile_samplers_bernoulli_and_helpers(lib):
     assert lib.santa_selftest_wait_timeout(None, 4096, 50_000_000, None) == WORKSPACE
     assert lib.santa_selftest_wait_timeout(vp(512), 4096, 10, None) == INVALID          # below 1 ms
     assert lib.santa_selftest_wait_timeout(vp(512), 4096, 3_000_000_000, None) == INVALID
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include "santa.h"
+int main(void) {
+  santa_params_t p = {0};
+  p.batch = 1; p.n_q_heads = 32; p.n_kv_heads = 8; p.head_dim = 128;
+  p.dtype = SANTA_BF16; p.nk = 32768; p.S = 256;
+  size_t n = santa_workspace_size(&p);
+  p.n_kv_heads = 3;   /* 32 query heads do not split into 3 groups */
+  santa_status_t st = santa_decode(&p, SANTA_SYSTEMATIC, NULL, NULL, NULL, NULL, NULL, 0, NULL, NULL);
+  printf("%d %zu %d %s\n", santa_version(), n, (int)st, santa_status_string(st));
+  return n == 0 || st != SANTA_ERR_INVALID_ARG;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    """include/santa.h compiles as strict C99 (gcc -pedantic -Werror) and a C
+    program links against the library and calls its host-side functions."""
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = santa_build.BUILD
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I",
+                    os.path.join(santa_build.ROOT, "include"), str(src), "-o", str(exe), "-L", libdir,
+                    "-l:libsanta.so", "-Wl,-rpath," + libdir], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
+    assert int(out[0]) >= 100 and int(out[1]) == santa.workspace_size(params()) and int(out[2]) == INVALID
