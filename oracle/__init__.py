@@ -10,7 +10,9 @@ tile samplers S2ANTA-prop, App. O, and S2ANTA-flash, App. P).
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (worked example, library routines, closed forms, invariants, Philox against
-an independent implementation).
+an independent implementation); ``tests/test_oracle_mutants.py`` plants
+plausible mistakes in copies of ``santa_oracle.c`` (wrong index, sign,
+constant, rounding rule, dropped term) and checks that each one fails a pin.
 """
 from __future__ import annotations
 
@@ -67,7 +69,9 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
+            # SANTA_ORACLE_LIB names another build of santa_oracle.c (the
+            # mutation tests load deliberately broken copies through it)
+            lib = ctypes.CDLL(os.environ.get("SANTA_ORACLE_LIB") or build())
             P = ctypes.POINTER(_Problem)
             vp, i32, u32, u64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_uint64
             lib.santa_oracle_philox4x32_10.argtypes = [vp, vp, vp]

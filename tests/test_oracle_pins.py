@@ -179,9 +179,50 @@ def test_inverse_cdf_left_closed_boundary(oracle_lib):
     is exactly (0.25, 0.5, 0.75, 1); a threshold on an edge picks the next key."""
     V = np.arange(12, dtype=np.float32).reshape(4, 1, 3)
     P = make_problem(oracle_lib, np.ones((1, 3)), np.zeros((4, 1, 3)), V)
-    _, J, delta = oracle_lib.sample_head(P, 0, 0, np.array([0.0, 0.25, 0.5, 0.75, 0.2499999, 0.9999]))
-    assert list(J) == [0, 1, 2, 3, 0, 3]
-    assert delta[0] == 0.0 and delta[1] == 0.0
+    _, J, delta = oracle_lib.sample_head(P, 0, 0, np.array([0.0, 0.25, 0.5, 0.75, 0.2499999, 0.9999, 0.3]))
+    assert list(J) == [0, 1, 2, 3, 0, 3, 1]
+    # delta: distance to the nearer end of the drawn key's interval [F(J-1), F(J))
+    np.testing.assert_allclose(delta, [0.0, 0.0, 0.0, 0.0, 1e-7, 1e-4, 0.05], rtol=1e-6, atol=1e-15)
+
+
+def test_threshold_at_the_total_mass_goes_to_the_last_key_with_mass(oracle_lib):
+    """Reading of the clamp: a threshold at or past the rounded total mass goes
+    to the last key with nonzero mass.  Keys whose mass underflows to zero in
+    float64 (score 1000 below the others) are never drawn, because
+    F(n-1) <= t < F(n) holds for no such key (App. A.4)."""
+    d = 4
+    q = np.zeros((1, d), np.float32)
+    q[0, 0] = 1.0
+    K = np.zeros((6, 1, d), np.float32)
+    K[:, 0, 0] = [0.5, -0.2, 0.1, -1000.0, -1000.0, -1000.0]
+    V = np.arange(6 * d, dtype=np.float32).reshape(6, 1, d)
+    P = make_problem(oracle_lib, q, K, V, scale=1.0)
+    _, p = oracle_lib.scores(P, 0, 0)
+    assert p[3:].max() == 0.0 and p[:3].min() > 0.1
+    _, J, _ = oracle_lib.sample_head(P, 0, 0, np.array([1.0, np.nextafter(1.0, 0.0), 0.0]))
+    assert list(J) == [2, 2, 0]
+
+
+def test_estimate_reads_the_rows_of_its_own_sequence(oracle_lib):
+    """Eq. 4 in a packed ragged batch: the estimate of head (b, h) is
+    (1/S) sum_j V[kv_offsets[b] + J_j, h // G], here by numpy indexing from
+    the drawn keys."""
+    rng = np.random.default_rng(21)
+    lens = [37, 50, 23]
+    offs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    H, Hkv, d, S = 4, 2, 16, 16
+    q = rng.standard_normal((3, H, d)).astype(np.float32)
+    K = rng.standard_normal((offs[-1], Hkv, d)).astype(np.float32)
+    V = rng.standard_normal((offs[-1], Hkv, d)).astype(np.float32)
+    P = oracle_lib.Problem(q, K, V, offs, "fp32", Hkv)
+    for b in range(3):
+        for h in range(H):
+            t = oracle_lib.thresholds("stratified", S, 5, b, h)
+            est, J, _ = oracle_lib.sample_head(P, b, h, t)
+            assert J.min() >= 0 and J.max() < lens[b]
+            want = V[offs[b] + J, h // (H // Hkv)].astype(np.float64).mean(axis=0)
+            np.testing.assert_allclose(est, want, rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(oracle_lib.gather(P, b, h, J), want, rtol=1e-12, atol=1e-12)
 
 
 def test_all_rows_equal_gives_that_row(oracle_lib):
@@ -510,6 +551,66 @@ def test_tile_counts_sum_to_budgets(oracle_lib, sampler):
             assert St.sum() == S
 
 
+@pytest.mark.parametrize("sampler", ["prop", "flash"])
+def test_tile_count_rule_on_exact_interval_ends(oracle_lib, sampler):
+    """Alg. 5 / Alg. 7 by hand: c_n = floor(a0 + p + x) - floor(a0 + p) gives
+    key n the integers in (a0 + p, a0 + p + x], open on the left.  One tile of
+    four keys with equal scores (u_n = 1, l = 4) and budget 2 has x = 1/2,
+    so every interval end is a multiple of 1/2: a0 = 0 draws keys 1 and 3,
+    a0 = 1/2 keys 0 and 2."""
+    V = np.arange(8, dtype=np.float32).reshape(4, 1, 2)
+    P = make_problem(oracle_lib, np.ones((1, 2)), np.zeros((4, 1, 2)), V)
+    for a, want in ((0.0, [0, 1, 0, 1]), (0.5, [1, 0, 1, 0])):
+        est, counts, _, St = oracle_lib.tiled_head(P, 0, 0, sampler, 2, 4, seed=0, a0=np.array([a]))
+        assert St.tolist() == [2] and counts.tolist() == want, (a, counts)
+        np.testing.assert_allclose(est, V[np.nonzero(want)[0], 0].astype(np.float64).mean(axis=0), rtol=1e-15)
+
+
+def test_tile_boundary_distances_by_hand(oracle_lib):
+    """The tile samplers' boundary distance: for a key that draws, the
+    distance from its interval ends (a0 + p, a0 + p + x] to the nearest
+    integer inside, in probability units (x units times W_t / (Z S_t)).
+    Two tiles of four equal-score keys, the second tile's scores ln 3 higher
+    (W = 4, 12: W/Z = 1/4, 3/4), flash with S = 4 (S_tile = 2, x = 1/2) and
+    a0 = 0.1: keys 1 and 3 of each tile draw once, 0.1 x-units from an end."""
+    q = np.ones((1, 1), np.float32)
+    K = np.zeros((8, 1, 1), np.float32)
+    K[4:, 0, 0] = np.float32(np.log(3.0))
+    V = np.arange(8, dtype=np.float32).reshape(8, 1, 1)
+    P = make_problem(oracle_lib, q, K, V, scale=1.0)
+    _, counts, delta, St = oracle_lib.tiled_head(P, 0, 0, "flash", 4, 4, seed=0, a0=np.array([0.1, 0.1]))
+    assert St.tolist() == [2, 2] and counts.tolist() == [0, 1, 0, 1, 0, 1, 0, 1]
+    np.testing.assert_allclose(delta, [-1, 0.0125, -1, 0.0125, -1, 0.0375, -1, 0.0375], rtol=1e-5)
+
+
+def test_tile_offsets_come_from_the_heads_philox_stream(oracle_lib, torch_philox):
+    """a0 of tile t is uniform number t of head (b, h) (the Philox layout of
+    the global samplers; the pages draw a0 ~ U[0, 1) per tile and name no
+    generator): drawing with a0 = None equals passing those uniforms, taken
+    here from PyTorch's Philox engine."""
+    rng = np.random.default_rng(30)
+    P = random_problem(oracle_lib, rng, 100, 8)
+    seed, step, T = 11, 2, 7
+    words = np.concatenate([torch_philox(seed, (step << 32) | 0, (0 << 32) | i) for i in range(2)])
+    a0 = (words[:T] >> 8).astype(np.float64) / 2.0 ** 24
+    for sampler in ("prop", "flash"):
+        e1, c1, _, _ = oracle_lib.tiled_head(P, 0, 0, sampler, 24, 16, seed=seed, step=step)
+        e2, c2, _, _ = oracle_lib.tiled_head(P, 0, 0, sampler, 24, 16, seed=seed, step=step, a0=a0)
+        np.testing.assert_array_equal(c1, c2)
+        np.testing.assert_array_equal(e1, e2)
+
+
+def test_flash_tile_budget_rounds_to_nearest(oracle_lib):
+    """Alg. 6 gives every tile about S / T samples: the reading taken is
+    S_tile = max(1, floor(S / T + 1/2)); three tiles of 16 keys."""
+    rng = np.random.default_rng(8)
+    P = random_problem(oracle_lib, rng, 48, 4)
+    for S, want in ((1, 1), (4, 1), (5, 2), (7, 2), (8, 3)):
+        _, counts, _, St = oracle_lib.tiled_head(P, 0, 0, "flash", S, 16, seed=1)
+        assert St.tolist() == [want] * 3, (S, St)
+        assert counts.sum() == 3 * want
+
+
 @pytest.mark.parametrize("S,a", [(5, 0.37), (16, 0.0), (9, 0.9)])
 def test_flash_single_tile_is_the_systematic_sampler(oracle_lib, S, a):
     """One tile covering all keys: the count rule of Alg. 7 is systematic
@@ -654,6 +755,14 @@ def test_storage_rounding_matches_numpy(oracle_lib):
     np.testing.assert_array_equal(got16, want16)
     gotb = np.array([oracle_lib.store_elem("bf16", float(x)) for x in xs], np.uint16)
     np.testing.assert_array_equal(gotb, synth.f32_to_bf16_bits(xs))
+    # exact halfway cases (bf16 keeps 8 significant bits, fp16 11), against
+    # PyTorch's conversions, which round to nearest even
+    ties = np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8), 3 + 2.0 ** -7, 1 + 2.0 ** -11,
+                     1 + 3 * 2.0 ** -11, 2.0 ** -24 * 1.5, 2.0 ** -24 * 2.5], np.float32)
+    tb = torch.from_numpy(ties).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    th = torch.from_numpy(ties).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal([oracle_lib.store_elem("bf16", float(x)) for x in ties], tb)
+    np.testing.assert_array_equal([oracle_lib.store_elem("fp16", float(x)) for x in ties], th)
 
 
 def _bern_problem(oracle_lib, rng, G=4, d=128, nk=64, dtype="fp32"):
@@ -686,6 +795,36 @@ def test_bernoulli_counts_law(oracle_lib, stratified):
     else:
         assert np.all(np.abs(var - Bs * p * (1 - p)) < 0.25 + 0.35 * Bs * p * (1 - p))
     assert np.all(C[:, np.argmax(m)] == Bs)   # the largest feature has p = 1
+
+
+@pytest.mark.parametrize("stratified", [False, True])
+def test_bernoulli_draws_use_their_own_philox_stream_and_a_strict_test(oracle_lib, torch_philox, stratified):
+    """Eq. 11 draws b ~ Bernoulli(p) as a24 < p 2^24 with a24 the top 24 bits
+    of a Philox word: for p 2^24 an integer that is probability p exactly
+    (a non-strict test would add 2^-24).  Sample n of feature i in group
+    (b, kvh) takes word r % 4, r = n d + i, of the block at counter
+    (r / 4, H + kvh, b, step), here from PyTorch's Philox engine.  With
+    G = 1, fp32 queries and one feature at |q| = 1 (so norm = 1), feature i
+    is given p_i = a24_i / 2^24 (no draw) or (a24_i + 1) / 2^24 (one draw).
+    With one sample the stratified rule (n + u)/B < p (App. C.1) is the same
+    test."""
+    seed, step, b, kvh, H, d = 77, 3, 1, 1, 2, 64
+    words = np.concatenate([torch_philox(seed, (step << 32) | b, ((H + kvh) << 32) | i) for i in range(d // 4)])
+    a24 = (words >> 8).astype(np.int64)
+    rng = np.random.default_rng(4)
+    hit = rng.integers(0, 2, d).astype(bool)
+    hit[0] = True
+    num = np.where(hit, a24 + 1, a24)
+    num[0] = 1 << 24
+    num = np.where(num == 0, 1, num)              # p = 0 would skip the feature
+    hit = np.where((a24 == 0) & ~hit, True, hit)  # ...and a24 = 0 < 1 draws
+    q = np.zeros((2, H, d), np.float32)
+    q[b, kvh] = (num / 2.0 ** 24).astype(np.float32) * np.where(rng.integers(0, 2, d) == 1, 1, -1)
+    q[b, 0] = rng.standard_normal(d).astype(np.float32)
+    K = rng.standard_normal((8, H, d)).astype(np.float32)
+    P = oracle_lib.Problem(q, K, K, np.array([0, 4, 8], np.int64), "fp32", H)
+    _, counts = oracle_lib.bernoulli_group(P, b, kvh, 1, stratified, seed, step)
+    np.testing.assert_array_equal(counts, hit.astype(np.int32))
 
 
 def test_bernoulli_effective_query_is_unbiased(oracle_lib):
