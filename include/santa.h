@@ -122,8 +122,8 @@ santa_status_t santa_decode(const santa_params_t* p, int32_t variant, const void
  * works.  q, out, workspace, sample_idx, kv_offsets and S_per_seq are device
  * memory as in santa_decode, and the drawn keys equal santa_decode's on the
  * same data.  Returns SANTA_ERR_INVALID_ARG, before any launch, when K or V is
- * neither device memory nor page-locked host memory that the device can
- * address (pageable memory, for one). */
+ * neither memory of the current device nor page-locked host memory that the
+ * device can address (pageable memory, for one). */
 santa_status_t santa_decode_host_kv(const santa_params_t* p, int32_t variant, const void* q, const void* K,
                                     const void* V, float* out, void* workspace, size_t ws_bytes,
                                     santa_stream_t stream, int32_t* sample_idx);

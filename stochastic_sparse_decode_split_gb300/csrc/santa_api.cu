@@ -231,18 +231,20 @@ santa_status_t santa_decode(const santa_params_t* p, int32_t variant, const void
   return decode_impl(p, variant, q, K, V, nullptr, out, workspace, ws_bytes, stream, sample_idx);
 }
 
-// The address the device reads a K or V buffer through: device (or managed)
-// memory as it is, page-locked host memory (cudaHostAlloc'd or
-// cudaHostRegister'ed) through its mapped device address; INVALID_ARG for
-// anything else (pageable memory, a pointer CUDA does not know).  Nothing is
-// launched.
+// The address the device reads a K or V buffer through: device memory of the
+// current device (or managed memory) as it is, page-locked host memory
+// (cudaHostAlloc'd or cudaHostRegister'ed) through its mapped device address;
+// INVALID_ARG for anything else (pageable memory, another GPU's memory, a
+// pointer CUDA does not know).  Nothing is launched.
 static santa_status_t kv_address(const void* h, const void** d) {
   if (!h) return SANTA_ERR_INVALID_ARG;
   cudaPointerAttributes at;
-  if (cudaPointerGetAttributes(&at, h) != cudaSuccess) {
+  int cur = -1;
+  if (cudaPointerGetAttributes(&at, h) != cudaSuccess || cudaGetDevice(&cur) != cudaSuccess) {
     (void)cudaGetLastError();
     return SANTA_ERR_INVALID_ARG;
   }
+  if (at.type == cudaMemoryTypeDevice && at.device != cur) return SANTA_ERR_INVALID_ARG;
   if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) {
     *d = h;
     return SANTA_OK;
