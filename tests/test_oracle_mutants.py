@@ -1,10 +1,11 @@
 """The oracle's pins catch plausible mistakes.
 
-Each case below plants one mistake in a copy of oracle/santa_oracle.c on the
-CPU: a wrong operand, index, sign, constant or rounding rule, or a dropped
-term.  It then builds the copy and runs the pins of tests/test_oracle_pins.py
-against it (through SANTA_ORACLE_LIB).  Every mutant must make at least one
-pin fail.  The mistakes are planted in the oracle only; the CUDA library is
+Each case below plants one mistake in a copy of oracle/santa_oracle.c or of
+oracle/analysis.py on the CPU: a wrong operand, index, sign, constant or
+rounding rule, or a dropped term.  It then builds or loads the copy and runs
+the pins of tests/test_oracle_pins.py against it (the C copy through
+SANTA_ORACLE_LIB, the Python copy in place of oracle.analysis).  Every
+mutant must make at least one pin fail.  The mistakes are planted in the oracle only; the CUDA library is
 not involved.
 """
 import os
@@ -90,6 +91,41 @@ MUTANTS = [
 ]
 
 
+# the closed forms of oracle/analysis.py, same format
+PY_MUTANTS = [
+    ("iid_trace_drops_mean", "- mu @ mu)", ")", 0, 1),
+    ("iid_trace_not_over_S", "    return tr / S", "    return tr", 0, 1),
+    ("iid_coordinate_drops_mean", "(V * V) - mu * mu) / S", "(V * V)) / S", 0, 1),
+    ("stratum_upper_edge", "((m + 1) / S)", "((m + 2) / S)", 0, 1),
+    ("stratified_trace_over_S", "return float(tr_m.sum()) / (S * S)", "return float(tr_m.sum()) / S", 0, 1),
+    ("stratified_coordinate_over_S", "return var_m.sum(axis=0) / (S * S)", "return var_m.sum(axis=0) / S", 0, 1),
+    ("breakpoints_sign", "u = (S * F)[:, None] - np.arange(S)[None, :]", "u = (S * F)[:, None] + np.arange(S)[None, :]",
+     0, 1),
+    ("offset_piece_length", "* (b - a)", "* (b + a)", 0, 1),
+    ("replicate_divisor", "/ (R - 1)", "/ R", 0, 1),
+    ("count_bounds_swapped", "return np.floor(Sp), np.ceil(Sp)", "return np.ceil(Sp), np.floor(Sp)", 0, 1),
+    ("unique_keys_exponent", "-np.expm1(S * np.log1p(-p))", "-np.expm1((S - 1) * np.log1p(-p))", 0, 1),
+    ("causal_mask_off_by_one", "np.triu_indices(n, 1)", "np.triu_indices(n, 2)", 0, 1),
+    ("coverage_complement", "np.mean(-np.expm1(log_none))", "np.mean(np.exp(log_none))", 0, 1),
+    ("coverage_axis", "np.log1p(-P).sum(axis=0)", "np.log1p(-P).sum(axis=1)", 0, 1),
+]
+PY_SRC = os.path.join(ROOT, "oracle", "analysis.py")
+
+# loads a mutated analysis.py in place of oracle.analysis, then runs the pins
+PY_DRIVER = """
+import importlib.util, sys
+sys.path.insert(0, sys.argv[1])
+import oracle
+spec = importlib.util.spec_from_file_location("oracle.analysis", sys.argv[2])
+mod = importlib.util.module_from_spec(spec)
+spec.loader.exec_module(mod)
+sys.modules["oracle.analysis"] = mod
+oracle.analysis = mod
+import pytest
+sys.exit(pytest.main([sys.argv[3], "-x", "-q", "-p", "no:cacheprovider", "-m", "not gpu"]))
+"""
+
+
 def mutate(src: str, orig: str, repl: str, occ: int, total: int) -> str:
     assert src.count(orig) == total, f"{orig!r} occurs {src.count(orig)} times, expected {total}"
     pos = -1
@@ -136,3 +172,24 @@ def test_every_mutant_fails_a_pin(tmp_path):
         results = list(ex.map(one, MUTANTS))
     survivors = [(n, tail) for n, rc, tail in results if rc == 0]
     assert not survivors, f"mutants no pin catches: {survivors}"
+
+
+def test_every_closed_form_mutant_fails_a_pin(tmp_path):
+    import oracle
+    oracle.build()
+
+    def one(m):
+        name, orig, repl, occ, total = m
+        path = os.path.join(str(tmp_path), f"analysis_{name}.py")
+        with open(path, "w") as f:
+            f.write(mutate(open(PY_SRC).read(), orig, repl, occ, total))
+        r = subprocess.run([sys.executable, "-c", PY_DRIVER, ROOT, path, os.path.join(HERE, "test_oracle_pins.py")],
+                           cwd=ROOT, env=dict(os.environ, OMP_NUM_THREADS="2"), capture_output=True, text=True,
+                           timeout=600)
+        return name, r.returncode, r.stdout.strip().splitlines()[-1:] if r.stdout else []
+
+    with ThreadPoolExecutor(max_workers=max(1, min(6, (os.cpu_count() or 2) // 2))) as ex:
+        results = list(ex.map(one, PY_MUTANTS))
+    assert all(rc in (0, 1) for _, rc, _ in results), results   # 1: a pin failed; anything else is a harness error
+    survivors = [(n, tail) for n, rc, tail in results if rc == 0]
+    assert not survivors, f"closed-form mutants no pin catches: {survivors}"

@@ -333,6 +333,30 @@ def test_mean_over_seeds_within_4_sigma(oracle_lib, variant):
     assert np.all(np.abs(E.mean(axis=0) - mu) <= 4.0 * sigma)
 
 
+def test_closed_form_variances_special_cases():
+    """Identities the closed forms must meet whatever the data: with all V
+    rows equal every estimate is that row, so every variance is zero (App. A:
+    the estimators average rows of V); a trace is the sum of the per-coordinate
+    variances; the App. M replicate estimator is numpy's unbiased variance
+    (ddof = 1) summed over coordinates."""
+    rng = np.random.default_rng(40)
+    p = rng.dirichlet(np.ones(30))
+    row = rng.standard_normal(6) * 5.0 + 10.0
+    V_eq = np.tile(row, (30, 1))
+    V = rng.standard_normal((30, 6)) + 3.0
+    for S in (1, 7, 32):
+        assert abs(analysis.iid_variance_trace(p, V_eq, S)) < 1e-10
+        assert np.abs(analysis.iid_coordinate_variance(p, V_eq, S)).max() < 1e-10
+        assert abs(analysis.stratified_variance_trace(p, V_eq, S)) < 1e-10
+        assert np.abs(analysis.stratified_coordinate_variance(p, V_eq, S)).max() < 1e-10
+        np.testing.assert_allclose(analysis.iid_coordinate_variance(p, V, S).sum(),
+                                   analysis.iid_variance_trace(p, V, S), rtol=1e-12)
+        np.testing.assert_allclose(analysis.stratified_coordinate_variance(p, V, S).sum(),
+                                   analysis.stratified_variance_trace(p, V, S), rtol=1e-12)
+    E = rng.standard_normal((9, 6))
+    np.testing.assert_allclose(analysis.replicate_variance_trace(E), np.var(E, axis=0, ddof=1).sum(), rtol=1e-13)
+
+
 @pytest.mark.parametrize("variant", ["iid", "stratified"])
 def test_empirical_variance_matches_closed_form(oracle_lib, variant):
     rng = np.random.default_rng(31)
@@ -639,6 +663,19 @@ def test_flash_single_tile_is_the_systematic_sampler(oracle_lib, S, a):
 
 def _gaussian_fp16(rng, n, d):
     return rng.standard_normal((n, d)).astype(np.float16).astype(np.float64)
+
+
+def test_causal_softmax_rows_match_scipy():
+    """The causal prefill attention of App. F: query i attends to keys 0..i
+    only; each row equals scipy's softmax over those keys, zero beyond."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(41)
+    q, k = rng.standard_normal((12, 8)), rng.standard_normal((12, 8))
+    P = analysis.causal_softmax(q, k, 0.5)
+    s = q @ k.T * 0.5
+    for i in range(12):
+        np.testing.assert_allclose(P[i, :i + 1], softmax(s[i, :i + 1]), rtol=1e-13, atol=1e-15)
+        assert np.all(P[i, i + 1:] == 0.0)
 
 
 def test_prefill_coverage_reproduces_table9(oracle_lib):
