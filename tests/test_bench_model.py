@@ -76,3 +76,30 @@ def test_traffic_record_follows_the_kernel_sources(tmp_path, monkeypatch):
     rec["source_hash"] = "0" * 16
     f.write_text(json.dumps(rec))
     assert bench.recorded_traffic("w") is None
+
+
+def _run_bench(args, **env):
+    import json
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py")] + args, cwd=ROOT, capture_output=True,
+                       text=True, timeout=600, env=dict(os.environ, **env))
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    return [json.loads(ln) for ln in lines]
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` (the CPU oracle as the reference arm) prints
+    one JSON line with the GPU arm's metric, unit and config keys, its own
+    cpu_baseline and a zero-byte e2e; ranks other than 0 exit quietly."""
+    out = _run_bench(["--impl", "reference", "--workload", "tiny", "--steps", "3", "--warmup", "3"])
+    assert len(out) == 1
+    line = out[0]
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
+    assert line["value"] > 0 and line["higher_is_better"] is False and line["steps"] == 3 and line["warmup"] == 3
+    assert line["config"]["workload"] == synth.tiny("systematic").name
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert _run_bench(["--impl", "reference", "--workload", "tiny", "--steps", "3", "--warmup", "3"],
+                      RANK="1", WORLD_SIZE="2", LOCAL_RANK="1") == []
