@@ -35,8 +35,9 @@ METRIC = "S²ANTA decode-attn µs/step and achieved HBM GB/s vs peak, 32K ctx bf
 UNIT = "us/step"
 FALLBACK_HBM_GBS = 6800.0
 FLUSH_BYTES = 512 * 1024 * 1024
-KERNEL_SOURCES = ["stochastic_sparse_decode_split_gb300/csrc/santa_fused.cu",
-                  "stochastic_sparse_decode_split_gb300/csrc/santa_stream.cuh",
+KERNEL_SOURCES = ["stochastic_sparse_decode_split_gb300/csrc/santa_fused.cuh",
+                  "stochastic_sparse_decode_split_gb300/csrc/santa_fused.cu",
+                  "stochastic_sparse_decode_split_gb300/csrc/santa_tma.cuh",
                   "stochastic_sparse_decode_split_gb300/csrc/santa_window.cuh",
                   "stochastic_sparse_decode_split_gb300/csrc/santa_common.cuh",
                   "stochastic_sparse_decode_split_gb300/csrc/santa_seq.cuh"]

@@ -10,6 +10,7 @@
 #include "santa_launch.h"
 
 static_assert(SANTA_MAX_GROUP == SANTA_MAX_GROUP_DEV, "group limit");
+static_assert(SANTA_MAX_S == santa::MAX_S, "sample budget limit");
 static_assert(SANTA_CHUNK == santa::SUB, "chunk length");
 static_assert(SANTA_MAX_TILE == santa::TL_MAX_LEN, "tile length");
 static_assert(SANTA_DEVERR_NK_BOUND == santa::ERR_NK_BOUND && SANTA_DEVERR_S_RANGE == santa::ERR_S_RANGE &&
@@ -167,7 +168,8 @@ santa::LaunchArgs base_args(const santa_params_t* p, const Layout& L, const void
 
 santa_status_t decode_impl(const santa_params_t* p, int32_t variant, const void* q, const void* K, const void* V,
                            const double* uniforms, float* out, void* ws, size_t ws_bytes, santa_stream_t stream,
-                           int32_t* sample_idx, void* const* events = nullptr, bool score_only = false) {
+                           int32_t* sample_idx, void* const* events = nullptr, bool score_only = false,
+                           bool k_host = false) {
   santa_status_t st = check_params(p, true);
   if (st != SANTA_OK) return st;
   if (variant < SANTA_IID || variant > SANTA_SYSTEMATIC) return SANTA_ERR_INVALID_ARG;
@@ -181,6 +183,7 @@ santa_status_t decode_impl(const santa_params_t* p, int32_t variant, const void*
   santa::LaunchArgs a = base_args(p, L, q, K, V, out, ws, (cudaStream_t)stream);
   unsigned char* w = static_cast<unsigned char*>(ws);
   a.variant = variant;
+  a.k_host = k_host ? 1 : 0;
   a.uniforms = uniforms;
   a.sample_idx = sample_idx;
   a.stash = reinterpret_cast<float*>(w + L.stash);
@@ -236,7 +239,7 @@ santa_status_t santa_decode(const santa_params_t* p, int32_t variant, const void
 // (cudaHostAlloc'd or cudaHostRegister'ed) through its mapped device address;
 // INVALID_ARG for anything else (pageable memory, another GPU's memory, a
 // pointer CUDA does not know).  Nothing is launched.
-static santa_status_t kv_address(const void* h, const void** d) {
+static santa_status_t kv_address(const void* h, const void** d, bool* host = nullptr) {
   if (!h) return SANTA_ERR_INVALID_ARG;
   cudaPointerAttributes at;
   int cur = -1;
@@ -251,6 +254,7 @@ static santa_status_t kv_address(const void* h, const void** d) {
   }
   if (at.type != cudaMemoryTypeHost || !at.devicePointer) return SANTA_ERR_INVALID_ARG;
   *d = at.devicePointer;
+  if (host) *host = true;
   return SANTA_OK;
 }
 
@@ -261,8 +265,10 @@ santa_status_t santa_decode_host_kv(const santa_params_t* p, int32_t variant, co
   if (st != SANTA_OK) return st;
   if (!K || !V) return SANTA_ERR_INVALID_ARG;
   const void *Kd = nullptr, *Vd = nullptr;
-  if ((st = kv_address(K, &Kd)) != SANTA_OK || (st = kv_address(V, &Vd)) != SANTA_OK) return st;
-  return decode_impl(p, variant, q, Kd, Vd, nullptr, out, workspace, ws_bytes, stream, sample_idx);
+  bool k_host = false;
+  if ((st = kv_address(K, &Kd, &k_host)) != SANTA_OK || (st = kv_address(V, &Vd)) != SANTA_OK) return st;
+  return decode_impl(p, variant, q, Kd, Vd, nullptr, out, workspace, ws_bytes, stream, sample_idx, nullptr, false,
+                     k_host);
 }
 
 santa_status_t santa_score_pass(const santa_params_t* p, const void* q, const void* K, void* workspace,

@@ -312,6 +312,13 @@ __device__ __forceinline__ double word_to_unit(uint32_t w) { return (double)(w >
 
 __device__ __forceinline__ void flag_error(int* err, int bits) { atomicOr(err, bits); }
 
+// Nanoseconds of the global timer (for bounded waits).
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialization may start while its predecessor is still running; it must
 // wait here before touching anything the predecessor writes.  Without that

@@ -1,0 +1,1308 @@
+// santa_fused.cuh -- one decode step of SANTA / S2ANTA in a single persistent
+// launch for 16-bit caches (sm_103a); instantiated per cache dtype in
+// santa_fused_bf16.cu and santa_fused_fp16.cu, launched from santa_fused.cu.
+//
+// "Stochastic Sparse Attention for Memory-Bound Inference":
+//   scores and per-chunk statistics   Sec. 2 Eq. (1); App. O, Alg. 3
+//   cross-chunk combine               App. O, Alg. 4
+//   thresholds                        Sec. 2.1 (i.i.d. Eq. 4; stratified; systematic)
+//   inverse CDF, left-closed          App. A.4
+//   GQA-deduplicated gather-and-add   Eq. (4), Fig. 1; App. O, Alg. 5
+//
+// Work is cut into blocks of 16 keys x 1 KV head (one tensor-core m-tile, one
+// statistics chunk), enumerated in (sequence, KV head, key block) order; a
+// "piece" is the run of blocks of one (sequence, KV head).  One 512-thread CTA
+// per SM, launched cooperatively; CTA i takes blocks [iT/P, (i+1)T/P), so the
+// K bytes per CTA differ by at most one block.
+//
+// Phase A (stream): warp w of a CTA scores blocks w, w + 16, ... of its range.
+// Each warp owns a ring of shared-memory stages filled by TMA (one 2 KiB box
+// per 64 features, 128-byte swizzle) and waits on its own mbarriers only.  It
+// scores a block on the tensor cores (16 keys x the G query heads of the KV
+// head), writes the fp32 scores (the stash the sampler reads back) and the
+// 16-key (max, exp-sum), and keeps running statistics of the pieces its CTA
+// shares with neighbours.
+//
+// Phase B (sample).  Masses are fixed-point integers (units of 2^-40) relative
+// to a power of two.  Inside its own range a CTA uses its own power 2^e_own;
+// the head's thresholds use 2^E*, the largest of the covering CTAs' powers,
+// and a threshold maps into the CTA's units exactly by a shift.  So all that
+// needs the other CTAs comes last: a CTA publishes one aggregate per head of
+// the (at most two) pieces it shares (max, and the mass in its own units),
+// arrives at the one grid barrier, and while it waits stages its chunk
+// statistics and scores in shared memory and forms the exact chunk prefixes
+// in its own units.  After the barrier one warp per head reads the covering
+// CTAs' aggregates (about 20 at a 32K context), which give E*, the head's
+// total mass Z and the prefix and mass of this CTA's range; places the
+// thresholds that fall in the range; and resolves them one per lane (chunk by
+// binary search over the prefixes, key by the chunk's 16 key masses).  The
+// group's warps then gather the drawn V rows, each distinct row once for every
+// head of the KV group, into shared-memory sums that go to out.  A piece
+// wholly inside one range needs no other CTA and is done before the wait; the
+// two shared pieces of a CTA run on two halves of the CTA at once.
+//
+// Difference from the pages' kernels: Alg. 4 rounds per-tile budgets by
+// largest remainder and samples each tile on its own; here the S thresholds of
+// a head are placed globally and each CTA resolves the ones in its own mass
+// interval, which reproduces the global i.i.d. / stratified / systematic
+// estimators.  Thresholds are exact integers, theta_j = floor(t_j * Z), with
+// t_j a rational of 24-bit uniforms, so no FP64 arithmetic runs per draw.
+#pragma once
+
+#include <climits>
+
+#include "santa_common.cuh"
+#include "santa_launch.h"
+#include "santa_seq.cuh"
+#include "santa_tma.cuh"
+#include "santa_window.cuh"
+
+// Phase boundaries of one CTA, for timing builds that define SANTA_STAMP
+// (thread 0 records the global timer at boundary k); nothing otherwise.
+#ifndef SANTA_STAMP
+#define SANTA_STAMP(k) ((void)0)
+#endif
+
+namespace santa {
+
+constexpr int FW = 16;              // warps per CTA
+constexpr int FT = FW * 32;         // threads per CTA
+constexpr int BK = SUB;             // keys per block (== statistics chunk)
+constexpr int REG = 64 * 1024;      // phase-B shared-memory region
+constexpr int BAR_G0 = 1, BAR_G1 = 2, BAR_INT = 3;   // named barriers of the phase-B groups
+constexpr unsigned long long GRID_WAIT_NS = 2000000000ull;
+
+template <int D>
+struct FGeom {
+  static constexpr int STAGE = BK * D * 2;               // bytes of one block of K
+  static constexpr int NSTAGE = D == 128 ? 3 : 6;        // ring depth per warp (same bytes in flight)
+  static constexpr int RING = FW * NSTAGE * STAGE;       // 192 KiB
+  static constexpr size_t SMEM = (size_t)RING + 1024;    // + alignment of the swizzled stages
+  static constexpr int CPL = D / 32;                     // output columns per lane in the gather
+  static constexpr int CPB = BK * D / 8 / 32;            // 16-byte copies per lane per block (cp.async path)
+  static_assert(RING >= 3 * REG, "phase-B regions fit the ring");
+};
+
+// ---------------------------------------------------------------------------
+// Exact thresholds.  A threshold is theta = floor(N * Z / (div * 2^24)) for an
+// integer numerator N < div * 2^24:
+//   systematic  N = j * 2^24 + k          (k: the head's one 24-bit uniform), div = S_b
+//   stratified  N = j * 2^24 + k_j        (k_j: uniform j),                  div = S_b
+//   i.i.d.      N = k_(j), sorted keys,                                      div = 1
+// so theta_j = floor(t_j * Z) with t_j = (j + u_j) / S_b or u_(j), u = k 2^-24.
+// ---------------------------------------------------------------------------
+struct ThetaCtx {
+  unsigned long long Zq, Zr;  // Z / div, Z % div
+  unsigned long long rcp;     // ceil(2^64 / div) (div > 1)
+  unsigned div;
+  long long Z;
+};
+// rcp = ceil(2^64 / div) when div > 1 (precomputed: a 64-bit division is slow here)
+__device__ __forceinline__ ThetaCtx theta_ctx_rcp(long long Z, unsigned div, unsigned long long rcp) {
+  ThetaCtx c;
+  c.Z = Z;
+  c.div = div;
+  c.rcp = rcp;
+  if (div > 1) {
+    // Z < 2^62: mulhi(Z, rcp) is floor(Z / div) or one more
+    unsigned long long q = __umul64hi((unsigned long long)Z, c.rcp);
+    if (q * div > (unsigned long long)Z) --q;
+    c.Zq = q;
+    c.Zr = (unsigned long long)Z - q * div;
+  } else {
+    c.Zq = (unsigned long long)Z;
+    c.Zr = 0ull;
+  }
+  return c;
+}
+// floor(N Z / (div 2^24)) = floor((N Zq + floor(N Zr / div)) / 2^24), exact in 128 bits.
+// N Zr < 2^36 * 2^12 = 2^48 and div <= 2^12, so the quotient by multiply-high
+// with rcp is exact: its error is below 2^-16 while the fraction of a
+// non-integer quotient is at most 1 - 2^-12.
+__device__ __forceinline__ long long theta_of(const ThetaCtx& c, unsigned long long N) {
+  unsigned long long lo = N * c.Zq, hi = __umul64hi(N, c.Zq);
+  const unsigned long long add = c.div > 1 ? __umul64hi(N * c.Zr, c.rcp) : 0ull;
+  lo += add;
+  hi += (lo < add) ? 1ull : 0ull;
+  return (long long)((hi << 40) | (lo >> 24));
+}
+
+template <int V>
+struct Draws {
+  int S, h, b;
+  uint32_t step, k0, k1;
+  uint32_t ksys;               // systematic: the head's uniform key
+  const uint32_t* sorted;      // i.i.d.: the head's sorted uniform keys
+  ThetaCtx tc;
+
+  __device__ __forceinline__ uint32_t key_at(int j) const {
+    const uint4 w = philox4x32_10(make_uint4((uint32_t)(j >> 2), (uint32_t)h, (uint32_t)b, step), k0, k1);
+    const uint32_t x = (j & 3) == 0 ? w.x : (j & 3) == 1 ? w.y : (j & 3) == 2 ? w.z : w.w;
+    return x >> 8;
+  }
+  __device__ __forceinline__ long long theta(int j) const {
+    if constexpr (V == VAR_IID) return theta_of(tc, sorted[j]);
+    const uint32_t k = V == VAR_SYS ? ksys : key_at(j);
+    return theta_of(tc, ((unsigned long long)j << 24) | k);
+  }
+  __device__ __forceinline__ int count_serial(long long X, int e) const {
+    while (e > 0 && theta(e - 1) >= X) --e;
+    while (e < S && theta(e) < X) ++e;
+    return e;
+  }
+  // {#{j < S : theta_j < X1}, #{j < S : theta_j < X2}} (thresholds are
+  // non-decreasing in j), computed by the whole warp.
+  __device__ __forceinline__ int2 count2(long long X1, long long X2, int lane) const {
+    if constexpr (V != VAR_IID) {
+      // theta_j lies in [floor(j Z / S), floor((j + 1) Z / S)]: a count is
+      // within 2 of e = trunc(X S / Z).  Lanes 0..7 test the window
+      // [e1 - 4, e1 + 4) of X1, lanes 8..15 that of X2, in one ballot.
+      const long long X = (lane & 8) ? X2 : X1;
+      int e = 0;
+      if (X >= tc.Z) e = S;
+      else if (X > 0) {
+        const int sh = max(0, 40 - __clzll(tc.Z));
+        e = (int)(__fdividef((float)(uint32_t)(X >> sh), (float)(uint32_t)(tc.Z >> sh)) * (float)S);
+        e = min(max(e, 0), S);
+      }
+      const int j = e - 4 + (lane & 7);
+      const bool below = X > 0 && (j < 0 || (j < S && (X >= tc.Z || theta(j) < X)));
+      const unsigned bal = __ballot_sync(FULL, below);
+      int c[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const unsigned w = (bal >> (8 * q)) & 0xffu;
+        const int eq = __shfl_sync(FULL, e, 8 * q);
+        const long long Xq = q ? X2 : X1;
+        if (Xq <= 0) c[q] = 0;
+        else if (Xq >= tc.Z) c[q] = S;
+        else if ((w & 1u) && !(w & 0x80u)) c[q] = eq - 4 + __popc(w);
+        else c[q] = count_serial(Xq, eq);   // the window missed (never expected)
+      }
+      return make_int2(c[0], c[1]);
+    } else {
+      return make_int2(count_sorted(X1, lane), count_sorted(X2, lane));
+    }
+  }
+  // sorted keys: 32-way search, one probe per lane and round
+  __device__ __forceinline__ int count_sorted(long long X, int lane) const {
+    if (X <= 0) return 0;
+    if (X >= tc.Z) return S;
+    int lo = 0, n = S;   // the count lies in [lo, lo + n]
+    while (n > 0) {
+      const int step = (n + 31) >> 5;
+      const int p = lo + lane * step;
+      const bool below = p < lo + n && theta(p) < X;
+      const int c = __popc(__ballot_sync(FULL, below));
+      if (c == 0) break;
+      const int end = lo + n;
+      lo = lo + (c - 1) * step + 1;
+      n = min(step - 1, end - lo);
+    }
+    return lo;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Per-CTA aggregate of one head over the CTA's keys of a shared piece.
+// Masses are taken relative to a power of two so that every reader rescales
+// them exactly by a shift:
+//   m  max score over the keys
+//   e  ceil(m log2(e)), an integer
+//   F  sum_n 2^(s_n log2(e) - e) in units of 2^-40 (rounded toward zero)
+// With E* the largest e over the CTAs of a head, CTA k's mass relative to
+// 2^E* is F_k >> (E* - e_k): the same integer in every CTA that computes it.
+// ---------------------------------------------------------------------------
+constexpr int AGG_EMPTY = -(1 << 30);   // e of a range with no finite score
+struct __align__(16) Agg {
+  float m;
+  int e;
+  long long F;
+};
+// from the max m and the natural-base sum l = sum_n exp(s_n - m)
+__device__ __forceinline__ Agg make_agg(float m, float l) {
+  Agg x;
+  x.m = m;
+  x.e = AGG_EMPTY;
+  x.F = 0;
+  if (m > -INFINITY) {
+    const float t = m * LOG2E;
+    x.e = (int)ceilf(t);
+    x.F = mass_fixed(l * fast_exp2(t - (float)x.e));
+  }
+  return x;
+}
+
+// ---------------------------------------------------------------------------
+// Grid-wide barrier (all CTAs are resident: cooperative launch).  A counter
+// and a generation word in the workspace; each CTA reads the generation
+// before it arrives, the last CTA to arrive resets the counter and advances
+// the generation.  Waits are bounded; on expiry ERR_TIMEOUT is flagged and
+// the CTA proceeds.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+  unsigned r;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(r) : "l"(p), "r"(v) : "memory");
+  return r;
+}
+__device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Arrival of this CTA (one thread, after the CTA's writes are ordered by a
+// CTA barrier); g is the generation read before arriving.
+__device__ __forceinline__ void grid_arrive(unsigned* count, unsigned* gen, unsigned g) {
+  if (atom_add_acq_rel(count, 1u) == gridDim.x - 1u) {   // the last to arrive
+    atomicExch(count, 0u);
+    st_release(gen, g + 1u);
+  }
+}
+// Waiting half: thread 0 spins until the generation moves past g (bounded),
+// then the CTA proceeds together.
+__device__ __forceinline__ void grid_wait(const unsigned* gen, unsigned g, int* err,
+                                          unsigned long long limit_ns = GRID_WAIT_NS) {
+  if (threadIdx.x == 0) {
+    const unsigned long long t0 = global_ns();
+    while (ld_acquire(gen) == g) {
+      if (global_ns() - t0 > limit_ns) {
+        flag_error(err, ERR_TIMEOUT);
+        break;
+      }
+      __nanosleep(32);
+    }
+    __threadfence();
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Block enumeration over the actual sequence lengths
+// ---------------------------------------------------------------------------
+struct SeqGeo {
+  int64_t row0, nk;
+  int nblk;
+};
+// Rows of sequence b; lengths outside [1, nk_max] are clamped here (the
+// metadata check reports them).
+__device__ __forceinline__ SeqGeo seq_geo(const LaunchArgs& a, int b) {
+  SeqGeo g;
+  if (a.kv_offsets) {
+    g.row0 = a.kv_offsets[b];
+    g.nk = a.kv_offsets[b + 1] - g.row0;
+  } else {
+    g.row0 = (int64_t)b * a.nk_max;
+    g.nk = a.nk_max;
+  }
+  if (g.nk < 1 || g.row0 < 0) g.nk = 0;
+  if (g.nk > a.nk_max) g.nk = a.nk_max;
+  g.nblk = (int)((g.nk + BK - 1) / BK);
+  return g;
+}
+
+// Position of one block: sequence b, KV head kvh, key block kblk of the
+// sequence; pb_lo is the global index of block 0 of piece (b, kvh).
+struct Cur {
+  int b, kvh, kblk, nblk;
+  int64_t row0, nk;
+  long long pb_lo;
+};
+// Moves kblk past the end of its piece into the following pieces (b = B: end).
+__device__ __forceinline__ void cur_norm(Cur& c, const LaunchArgs& a) {
+  while (c.kblk >= c.nblk) {
+    c.kblk -= c.nblk;
+    c.pb_lo += c.nblk;
+    if (++c.kvh == a.Hkv) {
+      c.kvh = 0;
+      if (++c.b >= a.B) {
+        c.b = a.B;
+        c.nblk = INT_MAX;
+        return;
+      }
+      const SeqGeo g = seq_geo(a, c.b);
+      c.row0 = g.row0;
+      c.nk = g.nk;
+      c.nblk = g.nblk;
+    }
+  }
+}
+__device__ __forceinline__ void cur_advance(Cur& c, const LaunchArgs& a, int n) {
+  c.kblk += n;
+  cur_norm(c, a);
+}
+
+// The cursors of blocks x0 and x1 (x0 <= x1 < T) and the total T, computed by
+// one warp.  Uniform batches are closed form; ragged ones scan the lengths.
+__device__ __forceinline__ long long total_blocks(const LaunchArgs& a, int lane) {
+  if (!a.kv_offsets) return (long long)a.B * a.Hkv * ((a.nk_max + BK - 1) / BK);
+  long long total = 0;
+  for (int b0 = 0; b0 < a.B; b0 += 32) {
+    long long s = (b0 + lane < a.B) ? (long long)seq_geo(a, b0 + lane).nblk : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(FULL, s, o);
+    total += s;
+  }
+  return total * a.Hkv;
+}
+__device__ __forceinline__ Cur locate_block(const LaunchArgs& a, long long x, int lane) {
+  Cur c;
+  if (!a.kv_offsets) {
+    const int nblk = (int)((a.nk_max + BK - 1) / BK);
+    const long long per_b = (long long)a.Hkv * nblk;
+    c.b = (int)(x / per_b);
+    const long long r = x - (long long)c.b * per_b;
+    c.kvh = (int)(r / nblk);
+    c.kblk = (int)(r - (long long)c.kvh * nblk);
+    c.nblk = nblk;
+    c.row0 = (int64_t)c.b * a.nk_max;
+    c.nk = a.nk_max;
+    c.pb_lo = x - c.kblk;
+    return c;
+  }
+  long long base = 0;
+  c.b = a.B;
+  for (int b0 = 0; b0 < a.B; b0 += 32) {
+    const int nb = (b0 + lane < a.B) ? seq_geo(a, b0 + lane).nblk : 0;
+    long long incl = (long long)nb * a.Hkv;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long t = __shfl_up_sync(FULL, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const unsigned hit = __ballot_sync(FULL, base + incl > x);
+    if (hit) {
+      const int l = __ffs(hit) - 1;
+      const int nbl = __shfl_sync(FULL, nb, l);
+      const long long excl = base + __shfl_sync(FULL, incl, l) - (long long)nbl * a.Hkv;
+      c.b = b0 + l;
+      const long long r = x - excl;
+      c.kvh = (int)(r / nbl);
+      c.kblk = (int)(r - (long long)c.kvh * nbl);
+      c.nblk = nbl;
+      const SeqGeo g = seq_geo(a, c.b);
+      c.row0 = g.row0;
+      c.nk = g.nk;
+      c.pb_lo = x - c.kblk;
+      break;
+    }
+    base += __shfl_sync(FULL, incl, 31);
+  }
+  return c;
+}
+
+// One piece as seen by one CTA.
+struct Piece {
+  int b, kvh, nblk;
+  int64_t row0, nk;
+  long long pb_lo;
+  int c_lo, c_hi;          // this CTA's key blocks (= statistics chunks) of the piece
+  int i_first, i_last;     // CTAs covering the piece
+};
+
+// Per-head state of phase B (shared memory).  "Own units": relative to the
+// CTA's power 2^e_own; "head units": relative to 2^E*.  A threshold theta in
+// [pown, pown + town) maps to the own-unit offset (theta - pown) << d, d =
+// E* - e_own, exactly.
+struct HeadState {
+  long long Z, pown, town;  // head units: total mass, prefix and mass of this range
+  long long carry, seg_end; // own units: prefix at the start / end of the current segment
+  unsigned long long rcp;   // ceil(2^64 / S_b) (S_b > 1), for the thresholds
+  uint32_t ksys;            // systematic: the head's uniform key
+  float ref;                // e_own: masses are 2^(s log2(e) - e_own)
+  float mstar;              // max score (the piece, when it is this CTA's alone)
+  int d;                    // E* - e_own
+  int jcur, jend;           // next threshold of the range; end of the range's thresholds
+  int jseg_lo, jseg_hi;     // thresholds of the current segment
+  int lastnz;               // last chunk of the segment with nonzero mass (-1: none)
+};
+
+// Shared-memory layout of a piece inside a phase-B region: one segment's
+// exact own-unit chunk masses and prefixes per head (a segment: as many
+// chunks as fit; one segment holds the CTA's whole range at a 32K context)
+// and, when they fit too, the range's scores.
+struct SegLayout {
+  long long* w;             // [G][segc] own-unit chunk masses
+  long long* pref;          // [G][segc + 1] exclusive own-unit chunk prefixes from the segment's carry
+  float* st;                // [G][capk] the range's scores (staged from the 16-byte boundary below), or NULL
+  int segc, nseg, capk;
+};
+
+// The single-launch partition: CTA i of P takes blocks [lo(i), lo(i + 1)),
+// lo(i) = floor(T i / P) = q i + floor(r i / P) with T = q P + r.
+struct Part {
+  long long T, q;
+  int r, P;
+  __device__ __forceinline__ long long lo(int i) const { return q * i + (r * i) / P; }
+  // the CTA whose range holds block x (0 <= x < T): the largest i with lo(i) <= x
+  __device__ __forceinline__ int cta_of(long long x) const {
+    int c = (int)(((float)x + 0.5f) / (float)T * (float)P);
+    c = min(max(c, 0), P - 1);
+    while (c + 1 < P && lo(c + 1) <= x) ++c;
+    while (c > 0 && lo(c) > x) --c;
+    return c;
+  }
+  __device__ __forceinline__ bool nonempty(int i) const { return T >= P || lo(i) < lo(i + 1); }
+};
+
+// Cursor of block x of a uniform batch (every sequence nk_max keys).
+__device__ __forceinline__ Cur locate_uniform(const LaunchArgs& a, long long x) {
+  Cur c;
+  const int nblk = (int)((a.nk_max + BK - 1) / BK);
+  const long long per_b = (long long)a.Hkv * nblk;
+  long long r;
+  if (x < (1ll << 32) && per_b < (1ll << 32)) {   // 32-bit division
+    c.b = (int)((uint32_t)x / (uint32_t)per_b);
+    r = (long long)((uint32_t)x - (uint32_t)c.b * (uint32_t)per_b);
+  } else {
+    c.b = (int)(x / per_b);
+    r = x - (long long)c.b * per_b;
+  }
+  c.kvh = (int)((uint32_t)r / (uint32_t)nblk);
+  c.kblk = (int)(r - (long long)c.kvh * nblk);
+  c.nblk = nblk;
+  c.row0 = (int64_t)c.b * a.nk_max;
+  c.nk = a.nk_max;
+  c.pb_lo = x - c.kblk;
+  return c;
+}
+
+// ---------------------------------------------------------------------------
+// i.i.d.: sorted 24-bit uniform keys of one head into ukeys (all threads of
+// the CTA).  Up to 1024 keys are placed by rank (each thread counts the keys
+// below its own: one barrier), more by a bitonic network in `keys`.
+// ---------------------------------------------------------------------------
+static __device__ __noinline__ void sort_head_keys(int b, int h, int S_b, uint32_t step, uint32_t k0, uint32_t k1,
+                                                  uint32_t* dst, uint32_t* keys) {
+  const int tid = threadIdx.x;
+  int S2 = 1;
+  while (S2 < S_b) S2 <<= 1;
+  for (int i = tid; i < S2; i += FT) {
+    uint32_t k = 0xffffffffu;
+    if (i < S_b) {
+      const uint4 w = philox4x32_10(make_uint4((uint32_t)(i >> 2), (uint32_t)h, (uint32_t)b, step), k0, k1);
+      const uint32_t x = (i & 3) == 0 ? w.x : (i & 3) == 1 ? w.y : (i & 3) == 2 ? w.z : w.w;
+      k = x >> 8;
+    }
+    keys[i] = k;
+  }
+  __syncthreads();
+  if (S_b <= 1024) {
+    for (int i = tid; i < S_b; i += FT) {
+      const uint32_t ki = keys[i];
+      int rank = 0;
+      for (int u = 0; u < S_b; ++u) {
+        const uint32_t ku = keys[u];
+        rank += (ku < ki || (ku == ki && u < i)) ? 1 : 0;
+      }
+      dst[rank] = ki;
+    }
+  } else {
+    for (int kk = 2; kk <= S2; kk <<= 1) {
+      for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+        for (int i = tid; i < S2; i += FT) {
+          const int ixj = i ^ jj;
+          if (ixj > i) {
+            const uint32_t x = keys[i], y = keys[ixj];
+            if ((x > y) == ((i & kk) == 0)) {
+              keys[i] = y;
+              keys[ixj] = x;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+    for (int i = tid; i < S_b; i += FT) dst[i] = keys[i];
+  }
+  __syncthreads();   // keys is rewritten for the next head
+}
+
+// ---------------------------------------------------------------------------
+// The kernel.  V: the sampling variant.  TMA_K: K is read by TMA boxes
+// through `tmap`; otherwise by per-lane 16-byte cp.async into the same
+// swizzled stage layout (K in host memory read in place).
+// ---------------------------------------------------------------------------
+template <typename T, int D, int V, bool TMA_K>
+__global__ void __launch_bounds__(FT, 1)
+fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsigned* bar_count, unsigned* bar_gen) {
+  using Gm = FGeom<D>;
+  constexpr int NS = Gm::NSTAGE, STG = Gm::STAGE, CPL = Gm::CPL;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ __align__(8) unsigned long long s_bar[FW * NS];
+  __shared__ float s_rm[2][FW][8], s_rl[2][FW][8];   // per-warp running statistics of the first / last piece
+  __shared__ int s_eown[2][8];                        // exponent of each published aggregate
+  __shared__ uint32_t s_keys[V == VAR_IID ? MAX_S : 1];   // i.i.d. key sort
+  __shared__ Cur s_cur[2];                            // blocks lo and hi - 1 (ragged batches)
+  __shared__ long long s_part[2];                     // T, q (ragged batches)
+  __shared__ HeadState s_hs[3][8];                    // per phase-B group and head
+  __shared__ unsigned s_gen;
+
+  SANTA_STAMP(0);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int P = gridDim.x, cta = blockIdx.x;
+  const int G = a.H / a.Hkv;
+  const uint32_t k0 = (uint32_t)a.seed, k1 = (uint32_t)(a.seed >> 32);
+  unsigned char* const ring = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const uint32_t ring_u32 = smem_addr(ring);
+  if constexpr (TMA_K)
+    if (tid == 0) prefetch_tensormap(&tmap);
+
+  // ---- the CTA's block range: closed form for uniform batches (every thread,
+  //      no wait), a scan of the lengths by one warp for ragged ones
+  Part pt;
+  pt.P = P;
+  Cur cA, cB;
+  if (!a.kv_offsets) {
+    pt.T = a.blk_total;
+    pt.q = a.blk_q;
+    pt.r = a.blk_r;
+  } else {
+    if (warp == 0) {
+      const long long Tb = total_blocks(a, lane);
+      if (lane == 0) {
+        s_part[0] = Tb;
+        s_part[1] = Tb / P;
+      }
+    }
+    __syncthreads();
+    pt.T = s_part[0];
+    pt.q = s_part[1];
+    pt.r = (int)(pt.T - pt.q * P);
+  }
+  const long long lo = pt.lo(cta), hi = pt.lo(cta + 1);
+  const bool has_range = hi > lo;
+  if (!a.kv_offsets) {
+    if (has_range) {
+      cA = locate_uniform(a, lo);
+      cB = locate_uniform(a, hi - 1);
+    }
+  } else {
+    if (warp == 0 && has_range) {
+      const Cur c0 = locate_block(a, lo, lane), c1 = locate_block(a, hi - 1, lane);
+      if (lane == 0) {
+        s_cur[0] = c0;
+        s_cur[1] = c1;
+      }
+    }
+    __syncthreads();
+    cA = s_cur[0];
+    cB = s_cur[1];
+  }
+  if (!has_range) {
+    cA.b = cB.b = a.B;
+    cA.pb_lo = cB.pb_lo = LLONG_MAX;
+    cA.nblk = cB.nblk = INT_MAX;
+  }
+  auto piece_at = [&](const Cur& c) {
+    Piece p;
+    p.b = c.b;
+    p.kvh = c.kvh;
+    p.nblk = c.nblk;
+    p.row0 = c.row0;
+    p.nk = c.nk;
+    p.pb_lo = c.pb_lo;
+    p.c_lo = (int)(max(lo, c.pb_lo) - c.pb_lo);
+    p.c_hi = (int)(min(hi, c.pb_lo + c.nblk) - c.pb_lo);
+    p.i_first = pt.cta_of(c.pb_lo);
+    p.i_last = pt.cta_of(c.pb_lo + c.nblk - 1);
+    return p;
+  };
+  // shared pieces: slot 0 = the first piece of the range, slot 1 = the last
+  // (when it is another piece); a piece is shared when it crosses the range
+  const bool first_shared = has_range && (cA.pb_lo < lo || cA.pb_lo + cA.nblk > hi);
+  const bool two_pieces = has_range && cB.pb_lo != cA.pb_lo;
+  const bool last_shared = two_pieces && cB.pb_lo + cB.nblk > hi;
+  SANTA_STAMP(1);
+
+  // ---- phase A: per-warp rings; the first NS blocks are requested first
+  const int n_mine = has_range && hi - lo > warp ? (int)((hi - lo - warp + FW - 1) / FW) : 0;
+  const uint32_t wring = ring_u32 + (uint32_t)(warp * NS * STG);
+  const uint32_t wbar = smem_addr(&s_bar[warp * NS]);
+  const unsigned long long pol = evict_first_policy();   // K is read once per step
+  if (TMA_K) {
+    if (lane == 0)
+      for (int s = 0; s < NS; ++s) mbar_init(wbar + 8 * s, 1);
+    mbar_fence_init();
+    __syncwarp();
+  }
+  Cur cur = cA;   // block being scored
+  if (n_mine > 0) cur_advance(cur, a, warp);
+  Cur prod = cur;   // block being requested
+  const T* Kp = static_cast<const T*>(a.K);
+  auto issue = [&](int k) {
+    const int s = k % NS;
+    const uint32_t dst = wring + (uint32_t)(s * STG);
+    if (k < n_mine) {
+      const int z = (int)(prod.row0 + (int64_t)prod.kblk * BK);
+      if constexpr (TMA_K) {
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          mbar_expect_tx(wbar + 8 * s, STG);
+#pragma unroll
+          for (int x = 0; x < D / 64; ++x) tma_load_3d(dst + x * 2048, &tmap, x * 64, prod.kvh, z, wbar + 8 * s, pol);
+        }
+      } else {
+        const int rows = (int)min((int64_t)BK, prod.nk - (int64_t)prod.kblk * BK);
+        const T* src = Kp + ((int64_t)z * a.Hkv + prod.kvh) * D;
+#pragma unroll
+        for (int j = 0; j < Gm::CPB; ++j) {
+          const int q = lane + 32 * j, r = q / (D / 8), c = q % (D / 8);
+          if (r < rows) cp_async16_hint(dst + swz128_offset(r, c), src + (int64_t)r * a.Hkv * D + c * 8, pol);
+        }
+      }
+      cur_advance(prod, a, FW);
+    }
+    if constexpr (!TMA_K) cp_async_commit();
+  };
+#pragma unroll 1
+  for (int k = 0; k < NS; ++k) issue(k);
+
+  // ---- prologue work while the first blocks are in flight
+  // the barrier generation before this launch's arrivals (no CTA of this
+  // launch can advance it before this one has arrived)
+  if (tid == 32) s_gen = ld_acquire(bar_gen);
+  if (lane < 16) {   // each warp clears its own running-statistics slots
+    s_rm[lane >> 3][warp][lane & 7] = -INFINITY;
+    s_rl[lane >> 3][warp][lane & 7] = 0.f;
+  }
+  // sequence metadata (sequence b checked by CTA b mod P): a sequence the
+  // device rejects gets zero outputs and -1 sample slots
+  for (int b = cta; b < a.B; b += P) {
+    int S_b;
+    const int e = seq_error(a, b, S_b);
+    if (e) {
+      if (tid == 0) flag_error(a.err, e);
+      float4* o = reinterpret_cast<float4*>(a.out + (int64_t)b * a.H * D);
+      for (int i = tid; i < a.H * D / 4; i += FT) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (a.sample_idx)
+        for (int i = tid; i < a.H * a.S_max; i += FT) a.sample_idx[(int64_t)b * a.H * a.S_max + i] = -1;
+    }
+  }
+  // pieces that start in this range: outputs of shared pieces to zero (their
+  // CTAs add into them after the barrier), unused sample slots to -1, and the
+  // i.i.d. keys this CTA sorts (head g of a piece: covering CTA i_first + g)
+  if (has_range) {
+    Cur pc = cA;
+    while (pc.b < a.B && pc.pb_lo < hi) {
+      int S_b;
+      const bool needed = (pc.pb_lo >= lo || V == VAR_IID) && !seq_error(a, pc.b, S_b);
+      if (needed) {
+        const Piece p = piece_at(pc);
+        const int64_t bh0 = (int64_t)p.b * a.H + (int64_t)p.kvh * G;
+        if (p.pb_lo >= lo) {
+          if (p.i_first != p.i_last) {
+            float4* o = reinterpret_cast<float4*>(a.out + bh0 * D);
+            for (int i = tid; i < G * D / 4; i += FT) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          if (a.sample_idx && S_b < a.S_max)
+            for (int i = tid; i < G * (a.S_max - S_b); i += FT)
+              a.sample_idx[(bh0 + i / (a.S_max - S_b)) * a.S_max + S_b + i % (a.S_max - S_b)] = -1;
+        }
+        if constexpr (V == VAR_IID)
+          for (int g = 0; g < G; ++g) {
+            int sorter = p.i_first + g;
+            if (sorter > p.i_last || !pt.nonempty(sorter)) sorter = p.i_first;
+            if (sorter == cta)
+              sort_head_keys(p.b, p.kvh * G + g, S_b, a.step, k0, k1, a.ukeys + (bh0 + g) * a.S_max, s_keys);
+          }
+      }
+      pc.kblk = pc.nblk;
+      cur_norm(pc, a);
+    }
+  }
+
+  // ---- phase A: the stream
+  SANTA_STAMP(2);
+  {
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;   // ldmatrix row of this lane
+    const int lhalf = lane >> 4;                           // ldmatrix 8-column half of this lane
+    float rm[2] = {-INFINITY, -INFINITY}, rl[2] = {0.f, 0.f};   // running statistics, heads 2*t4 + hh
+    long long run_piece = cur.pb_lo;
+    auto flush = [&]() {   // running statistics of run_piece into its slot (first / last piece only)
+      const int slot = run_piece == cA.pb_lo ? 0 : (run_piece == cB.pb_lo ? 1 : -1);
+      if (slot >= 0 && lane < 4) {
+        s_rm[slot][warp][2 * lane] = rm[0];
+        s_rm[slot][warp][2 * lane + 1] = rm[1];
+        s_rl[slot][warp][2 * lane] = rl[0];
+        s_rl[slot][warp][2 * lane + 1] = rl[1];
+      }
+      rm[0] = rm[1] = -INFINITY;
+      rl[0] = rl[1] = 0.f;
+    };
+    const T* qp = static_cast<const T*>(a.q);
+    bool ring_dead = false;
+    uint32_t bq[D / 16][2];
+    int bq_b = -1, bq_kvh = -1;
+    for (int k = 0; k < n_mine; ++k) {
+      const int s = k % NS;
+      if constexpr (TMA_K) {
+        // after one expired wait the warp stops waiting (its results are void, the error word says so)
+        if (!ring_dead && !mbar_wait(wbar + 8 * s, (unsigned)((k / NS) & 1), a.err)) ring_dead = true;
+      } else {
+        cp_async_wait<NS - 1>();
+      }
+      __syncwarp();
+      if (cur.pb_lo != run_piece) {
+        flush();
+        run_piece = cur.pb_lo;
+      }
+      const int64_t bh0 = (int64_t)cur.b * a.H + (int64_t)cur.kvh * G;
+      if (cur.b != bq_b || cur.kvh != bq_kvh) {   // q fragments change only with the piece
+        const T* qg = qp + bh0 * D;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const T* q2 = qg + g8 * D + ks * 16 + t4 * 2;
+          bq[ks][0] = (g8 < G) ? *reinterpret_cast<const uint32_t*>(q2) : 0u;
+          bq[ks][1] = (g8 < G) ? *reinterpret_cast<const uint32_t*>(q2 + 8) : 0u;
+        }
+        bq_b = cur.b;
+        bq_kvh = cur.kvh;
+      }
+      // A fragments of the whole block (16 keys x D) into registers; the stage is then free
+      uint32_t af[D / 16][4];
+      const uint32_t sbase = wring + (uint32_t)(s * STG);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) ldmatrix_x4(sbase + swz128_offset(lrow, ks * 2 + lhalf), af[ks]);
+      __syncwarp();
+      issue(k + NS);
+      // 16 keys x 8 heads on the tensor cores, two independent accumulators
+      float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ks += 2) {
+        Mma<T>::run(acc0, af[ks], bq[ks][0], bq[ks][1]);
+        Mma<T>::run(acc1, af[ks + 1], bq[ks + 1][0], bq[ks + 1][1]);
+      }
+      // lane holds keys g8 and g8 + 8 of the block for heads 2*t4 and 2*t4 + 1
+      const int64_t key0 = (int64_t)cur.kblk * BK;
+      const bool ok0 = key0 + g8 < cur.nk, ok1 = key0 + g8 + 8 < cur.nk;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int head = 2 * t4 + hh;
+        const float s0 = (acc0[hh] + acc1[hh]) * a.scale, s1 = (acc0[2 + hh] + acc1[2 + hh]) * a.scale;
+        if (head < G) {
+          float* sp = a.stash + (bh0 + head) * a.nk_max + key0 + g8;
+          if (ok0) sp[0] = s0;
+          if (ok1) sp[8] = s1;
+        }
+        float m = fmaxf(ok0 ? s0 : -INFINITY, ok1 ? s1 : -INFINITY);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
+        float l = (ok0 ? fast_exp(s0 - m) : 0.f) + (ok1 ? fast_exp(s1 - m) : 0.f);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) l += __shfl_xor_sync(FULL, l, o);
+        if (g8 == 0 && head < G) {
+          a.tile_max[(bh0 + head) * a.chunks_max + cur.kblk] = m;
+          a.tile_sum[(bh0 + head) * a.chunks_max + cur.kblk] = l;
+        }
+        const float nm = fmaxf(rm[hh], m);
+        rl[hh] = rl[hh] * fast_exp(rm[hh] - nm) + l * fast_exp(m - nm);
+        rm[hh] = nm;
+      }
+      cur_advance(cur, a, FW);
+    }
+    if constexpr (!TMA_K) cp_async_wait_all();
+    if (n_mine > 0) flush();
+  }
+  __syncthreads();   // statistics of the range written; the ring is free
+  SANTA_STAMP(3);
+
+  // ---- aggregates of the shared pieces (16 lanes per head combine the 16
+  //      warps' running statistics), then arrival at the grid barrier
+  if (tid < 256) {
+    const int slot = tid >> 7, g = (tid >> 4) & 7, w = tid & 15;
+    const float m = s_rm[slot][w][g], l = s_rl[slot][w][g];
+    float mm = m;
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(FULL, mm, o, 16));
+    float ll = m > -INFINITY ? l * expf(m - mm) : 0.f;
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) ll += __shfl_xor_sync(FULL, ll, o, 16);
+    const bool pub = (slot == 0 ? first_shared : last_shared) && g < G;
+    if (pub && w == 0) {
+      const Cur& c = slot == 0 ? cA : cB;
+      const int64_t bh = (int64_t)c.b * a.H + (int64_t)c.kvh * G + g;
+      const Agg x = make_agg(mm, ll);
+      reinterpret_cast<Agg*>(a.agg)[bh * MAX_CTAS + cta] = x;
+      s_eown[slot][g] = x.e;
+    }
+  }
+  __syncthreads();
+  SANTA_STAMP(4);
+  if (tid == 0) grid_arrive(bar_count, bar_gen, s_gen);
+  SANTA_STAMP(5);
+
+  // =====================================================================
+  // phase B
+  // =====================================================================
+  const int n_shared = (first_shared ? 1 : 0) + (last_shared ? 1 : 0);
+  unsigned char* const regions = ring;   // 0 and 1: the shared pieces (one group of 16 warps uses both); 2: the rest
+  auto seg_layout = [&](unsigned char* reg, int reg_bytes, int nch_part) {
+    SegLayout L;
+    // per head and chunk: the chunk mass and the exclusive prefix, 16 bytes
+    const int cap = ((int)((float)(reg_bytes - 64) / (float)(16 * G)) - 1) & ~3;
+    L.segc = min(cap, (nch_part + 3) & ~3);
+    L.nseg = (int)(((float)nch_part + (float)(L.segc - 1)) / (float)L.segc);
+    L.w = reinterpret_cast<long long*>(reg);
+    L.pref = L.w + (size_t)G * L.segc;
+    const int used = G * L.segc * 8 + G * (L.segc + 1) * 8;
+    L.capk = BK * L.segc + 8;
+    L.st = L.nseg == 1 && used + 16 + G * L.capk * 4 <= reg_bytes
+               ? reinterpret_cast<float*>(reg + ((used + 15) & ~15))
+               : nullptr;
+    return L;
+  };
+  // One warp (head wl): exact exclusive prefixes of the own-unit chunk masses
+  // w[0, nch) of its head from `carry` (each lane a run of consecutive chunks,
+  // one 64-bit warp scan); returns the segment's end and its last chunk with
+  // nonzero mass.
+  auto scan_head = [&](const SegLayout& L, int wl, int nch, long long carry, int& lastnz) {
+    const long long* w = L.w + wl * L.segc;
+    long long* pr = L.pref + wl * (L.segc + 1);
+    const int run = (nch + 31) >> 5;   // chunks per lane
+    const int ca = min(nch, lane * run), cb = min(nch, ca + run);
+    long long s = 0;
+    int nz = -1;
+    for (int c = ca; c < cb; ++c) {
+      s += w[c];
+      if (w[c] > 0) nz = c;
+    }
+    long long x = carry + warp_inclusive_scan(s, lane) - s;
+    for (int c = ca; c < cb; ++c) {
+      pr[c] = x;
+      x += w[c];
+    }
+    lastnz = __reduce_max_sync(FULL, nz);
+    return __shfl_sync(FULL, x, 31);
+  };
+  // Own-unit chunk mass of chunk c0 + c of head bh relative to 2^ref.
+  auto chunk_mass = [&](int64_t bh, int c, float ref) {
+    const int64_t gi2 = bh * a.chunks_max + c;
+    return mass_fixed(fast_exp2(fmaf(a.tile_max[gi2], LOG2E, -ref)) * a.tile_sum[gi2]);
+  };
+
+  // Preparation of one piece by one group of nw warps (warps w0 .. w0 + nw -
+  // 1; named barrier bar_id) in region reg, needing nothing from other CTAs:
+  // per head (warp w0 + g) the own power e_own, the threshold constants
+  // (budget reciprocal, systematic key), the own-unit chunk prefixes of the
+  // first segment (masses by the whole group) and, for a piece wholly inside
+  // this range, Z; and the range's scores staged when they fit.  Not
+  // synchronised at the end.
+  auto prep_piece = [&](const Piece& p, const SegLayout& L, bool shared, int slot, int gid, int bar_id, int w0,
+                        int nw) {
+    const int wl = warp - w0, tg = tid - w0 * 32, nthr = nw * 32;
+    int S_b;
+    if (seq_error(a, p.b, S_b)) return;
+    const int64_t bh0 = (int64_t)p.b * a.H + (int64_t)p.kvh * G;
+    const int nch_part = p.c_hi - p.c_lo;
+    const int nch0 = min(L.segc, nch_part);
+    if (L.st) {
+      // the range's scores, copied while the rest is prepared (waited for
+      // before the grid wait, or by the piece's finish); rows start at the
+      // 16-byte boundary at or below their first element
+      const int64_t key0 = (int64_t)p.c_lo * BK;
+      const int nkeys = (int)(min((int64_t)p.c_hi * BK, p.nk) - key0);
+      for (int h = 0; h < G; ++h) {
+        const int64_t g0 = (bh0 + h) * a.nk_max + key0, a0 = g0 & ~(int64_t)3;
+        const int n16 = (int)((g0 + nkeys - a0 + 3) >> 2);
+        float* row = L.st + h * L.capk;
+        for (int j = tg; j < n16; j += nthr) cp_async16(smem_addr(row + 4 * j), a.stash + a0 + 4 * j);
+      }
+      cp_async_commit();
+    }
+    // threshold constants of head g by warp w0 + (G + g) % nw (lane 0)
+    for (int g = 0; g < G; ++g)
+      if (wl == (G + g) % nw && lane == 0) {
+        HeadState& H = s_hs[gid][g];
+        H.rcp = (V != VAR_IID && S_b > 1) ? ~0ull / (unsigned)S_b + 1ull : 0ull;
+        H.ksys = V == VAR_SYS ? philox4x32_10(make_uint4(0u, (uint32_t)(p.kvh * G + g), (uint32_t)p.b, a.step), k0,
+                                              k1).x >> 8
+                              : 0u;
+      }
+    if (!shared && wl < G) {
+      // the whole piece is this CTA's: e_own from the chunk maxima (and Z,
+      // when the chunks do not fit one segment, their exact sum)
+      const int64_t bh = bh0 + wl;
+      HeadState& H = s_hs[gid][wl];
+      const float* mx = a.tile_max + bh * a.chunks_max;
+      float mstar = -INFINITY;
+      for (int c = lane; c < p.nblk; c += 32) mstar = fmaxf(mstar, mx[c]);
+      mstar = warp_max(mstar);
+      const int e_own = mstar > -INFINITY ? (int)ceilf(mstar * LOG2E) : AGG_EMPTY;
+      long long Z = 0;
+      if (nch0 < nch_part) {
+        for (int c = lane; c < p.nblk; c += 32) Z += chunk_mass(bh, c, (float)e_own);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(FULL, Z, o);
+      }
+      if (lane == 0) {
+        H.ref = (float)e_own;
+        H.mstar = mstar;
+        H.Z = Z;
+      }
+    }
+    if (shared && tg < G) s_hs[gid][tg].ref = (float)s_eown[slot][tg];
+    group_sync(bar_id, nthr);   // own powers visible
+    // the first segment's chunk masses by the whole group, then one warp per head scans them
+    for (int it = tg; it < G * nch0; it += nthr) {
+      const int h = it / nch0, c = it - h * nch0;
+      L.w[h * L.segc + c] = chunk_mass(bh0 + h, p.c_lo + c, s_hs[gid][h].ref);
+    }
+    group_sync(bar_id, nthr);
+    if (wl < G) {
+      HeadState& H = s_hs[gid][wl];
+      int lastnz;
+      const long long end = scan_head(L, wl, nch0, 0, lastnz);
+      __syncwarp();
+      if (lane == 0) {
+        H.seg_end = end;
+        H.lastnz = lastnz;
+        if (!shared) {
+          if (nch0 == nch_part) H.Z = end;
+          H.pown = 0;
+          H.town = H.Z;
+          H.d = 0;
+        }
+      }
+    }
+  };
+
+  // The rest of one piece (same group, region and layout as its
+  // preparation), one warp per head with no further synchronisation: Z, the
+  // range's prefix pown and mass town and d (from the other CTAs' aggregates
+  // when shared); the range's thresholds, resolved one per lane (chunk by a
+  // search of the prefixes, key by the chunk's 16 key masses); the drawn V
+  // rows, each distinct key of the head once with its count, gathered four
+  // at a time; the sums, times 1/S_b, into out.  The G head warps of a piece
+  // gather at the same time, so a row drawn by several heads of the KV group
+  // is fetched from memory once and served to the others from L2.
+  auto finish_piece = [&](const Piece& p, const SegLayout& L, bool shared, int gid, int bar_id, int w0, int nw) {
+    const int wl = warp - w0, nthr = nw * 32;
+    int S_b;
+    if (seq_error(a, p.b, S_b)) return;   // the same in every thread of the group
+    if (!shared) {   // the preparation's state and staged scores visible (a shared piece: by the grid wait)
+      cp_async_wait_all();
+      group_sync(bar_id, nthr);
+    }
+    SANTA_STAMP(20);
+    if (wl < G) {
+      const int64_t bh0 = (int64_t)p.b * a.H + (int64_t)p.kvh * G, bh = bh0 + wl;
+      const HeadState& H = s_hs[gid][wl];
+      Draws<V> dr;
+      dr.S = S_b;
+      dr.b = p.b;
+      dr.h = p.kvh * G + wl;
+      dr.step = a.step;
+      dr.k0 = k0;
+      dr.k1 = k1;
+      dr.sorted = a.ukeys + bh * a.S_max;
+      dr.ksys = H.ksys;
+      const float ref = H.ref;
+      long long Z, pown, town;
+      int d = 0;
+      if (shared) {
+        // the covering CTAs' aggregates (one per lane): E* by a max, then the
+        // masses relative to it, their prefix, this range's prefix and mass
+        const Agg* ag = reinterpret_cast<const Agg*>(a.agg) + bh * MAX_CTAS;
+        const int ncov = p.i_last - p.i_first + 1;
+        Agg x0;
+        x0.m = -INFINITY;
+        x0.e = AGG_EMPTY;
+        x0.F = 0;
+        if (lane < ncov && pt.nonempty(p.i_first + lane)) x0 = ag[p.i_first + lane];
+        int emax = __reduce_max_sync(FULL, x0.e);
+        float mstar = x0.m;
+        for (int i = p.i_first + 32 + lane; i - lane <= p.i_last; i += 32) {   // more than 32 covering CTAs
+          int e = AGG_EMPTY;
+          if (i <= p.i_last && pt.nonempty(i)) {
+            e = ag[i].e;
+            mstar = fmaxf(mstar, ag[i].m);
+          }
+          emax = max(emax, __reduce_max_sync(FULL, e));
+        }
+        SANTA_STAMP(21);
+        long long carry = 0;
+        pown = town = 0;
+        for (int base = 0; base < ncov; base += 32) {
+          Agg x = x0;
+          if (base > 0) {
+            x.e = AGG_EMPTY;
+            x.F = 0;
+            const int i = p.i_first + base + lane;
+            if (base + lane < ncov && pt.nonempty(i)) x = ag[i];
+          }
+          const int dd = emax - x.e;
+          const long long Ti = dd < 63 ? (x.F >> dd) : 0;
+          const long long incl = warp_inclusive_scan(Ti, lane) + carry;
+          if (p.i_first + base + lane == cta) {
+            pown = incl - Ti;
+            town = Ti;
+          }
+          carry = __shfl_sync(FULL, incl, 31);
+        }
+        Z = carry;
+        const int own = (cta - p.i_first) & 31;   // the lane that held this CTA
+        pown = __shfl_sync(FULL, pown, own);
+        town = __shfl_sync(FULL, town, own);
+        d = emax - (int)ref;
+        if (cta == p.i_first) {
+          mstar = warp_max(mstar);
+          if (lane == 0) a.head_max[bh] = mstar;
+        }
+      } else {
+        Z = H.Z;
+        pown = H.pown;
+        town = H.town;
+        if (lane == 0) a.head_max[bh] = H.mstar;
+      }
+      dr.tc = theta_ctx_rcp(Z, V == VAR_IID ? 1u : (unsigned)S_b, H.rcp);
+      const bool none = town == 0 || d > 61;   // no threshold falls in this range
+      const int2 jr = dr.count2(pown, none ? pown : pown + town, lane);
+      SANTA_STAMP(9);
+      const T* Vb = static_cast<const T*>(a.V) + (p.row0 * a.Hkv + p.kvh) * (int64_t)D + lane * CPL;
+      const long long* pr = L.pref + wl * (L.segc + 1);
+      float acc[CPL];
+#pragma unroll
+      for (int k = 0; k < CPL; ++k) acc[k] = 0.f;
+      long long seg_end = H.seg_end;
+      int lastnz = H.lastnz;
+      int j = jr.x;
+      for (int sg = 0; sg < L.nseg && j < jr.y; ++sg) {
+        const int c0 = p.c_lo + sg * L.segc, nch = min(L.segc, p.c_hi - c0);
+        if (sg > 0) {   // this segment's chunk prefixes, by this warp alone
+          for (int c = lane; c < nch; c += 32) L.w[wl * L.segc + c] = chunk_mass(bh, c0 + c, ref);
+          __syncwarp();
+          seg_end = scan_head(L, wl, nch, seg_end, lastnz);
+          __syncwarp();
+        }
+        // own-unit offset x >= seg_end  <=>  theta >= pown + ceil(seg_end / 2^d)
+        int jhi = jr.y;
+        if (sg + 1 < L.nseg) {
+          const long long X = pown + (long long)(((unsigned long long)seg_end + (1ull << d) - 1ull) >> d);
+          jhi = max(j, min(jr.y, dr.count2(min(X, pown + town), 0, lane).x));
+        }
+        SANTA_STAMP(10);
+        for (int jb = j; jb < jhi; jb += 32) {
+          // ---- thresholds jb .. jb + 31, one per lane
+          const int jj = jb + lane;
+          const bool valid = jj < jhi;
+          int key = -1;
+          if (valid) {
+            const long long x = (dr.theta(jj) - pown) << d;   // own-unit offset in this range
+            int c;
+            const bool gap = x >= seg_end;   // rounding gap at the range's end: the last nonzero chunk
+            if (gap) {
+              c = lastnz;
+            } else {
+              int lo2 = 0, hi2 = nch - 1;   // the last chunk with pref <= x
+              while (lo2 < hi2) {
+                const int mid = (lo2 + hi2 + 1) >> 1;
+                if (pr[mid] <= x) lo2 = mid;
+                else hi2 = mid - 1;
+              }
+              c = lo2;
+            }
+            if (c < 0) {
+              key = c0 * BK;   // no mass in the range at all (never expected)
+            } else {
+              // the first key of the chunk whose inclusive key-mass prefix
+              // exceeds x - pref[c]; past the chunk's key total, its last
+              // nonzero key
+              const long long xc = gap ? LLONG_MAX : x - pr[c];
+              const int64_t kc = (int64_t)(c0 + c) * BK;
+              const int64_t kr0 = (int64_t)p.c_lo * BK;   // the range's first key
+              const float* sc = L.st ? L.st + wl * L.capk + (int)((bh * a.nk_max + kr0) & 3) + (int)(kc - kr0)
+                                     : a.stash + bh * a.nk_max + kc;
+              float s[BK];
+#pragma unroll
+              for (int kk = 0; kk < BK; ++kk) s[kk] = kc + kk < p.nk ? sc[kk] : -INFINITY;
+              long long F = 0;
+              int found = -1, lastk = 0;
+#pragma unroll
+              for (int kk = 0; kk < BK; ++kk) {
+                const long long w = mass_fixed(fast_exp2(fmaf(s[kk], LOG2E, -ref)));
+                F += w;
+                lastk = w > 0 ? kk : lastk;
+                found = (found < 0 && F > xc) ? kk : found;
+              }
+              key = (int)(kc + (found >= 0 ? found : lastk));
+            }
+            if (a.sample_idx) a.sample_idx[bh * a.S_max + jj] = key;
+          }
+          SANTA_STAMP(12);
+          // ---- the distinct keys (keys are non-decreasing along the lanes)
+          //      with their counts, gathered four at a time
+          const int kprev = __shfl_up_sync(FULL, key, 1);
+          unsigned starts = __ballot_sync(FULL, valid && (lane == 0 || kprev != key));
+          const int nval = __popc(__ballot_sync(FULL, valid));
+          const unsigned later = starts & ~((2u << lane) - 1u);
+          const float cnt = (float)((later ? __ffs(later) - 1 : nval) - lane);   // meaningful at run starts
+          while (starts) {   // warp-uniform
+            int src[4];
+            uint2 raw[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              src[u] = starts ? __ffs(starts) - 1 : -1;
+              starts &= starts ? starts - 1 : 0u;
+              const int kk = __shfl_sync(FULL, key, src[u] < 0 ? 0 : src[u]);
+              raw[u] = make_uint2(0u, 0u);
+              if (src[u] >= 0) {
+                const T* row = Vb + (int64_t)kk * a.Hkv * D;
+                if constexpr (CPL == 4) raw[u] = *reinterpret_cast<const uint2*>(row);
+                else raw[u].x = *reinterpret_cast<const uint32_t*>(row);
+              }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float c = __shfl_sync(FULL, cnt, src[u] < 0 ? 0 : src[u]);
+              f2x pr2[4];
+              Pairs<T>::get(make_uint4(raw[u].x, raw[u].y, 0u, 0u), pr2);
+              const float2 p0 = unpack2(pr2[0]), p1 = unpack2(pr2[1]);
+              const float vf[4] = {p0.x, p0.y, p1.x, p1.y};
+#pragma unroll
+              for (int k = 0; k < CPL; ++k) acc[k] = src[u] >= 0 ? fmaf(c, vf[k], acc[k]) : acc[k];
+            }
+          }
+          SANTA_STAMP(13);
+        }
+        j = jhi;   // the next segment's first threshold
+      }
+      // ---- the head's sums, times 1/S_b, into out
+      const float inv_S = 1.0f / (float)S_b;
+      float* o = a.out + bh * D + lane * CPL;
+      if constexpr (CPL == 4) {
+        const float4 v4 = make_float4(acc[0] * inv_S, acc[1] * inv_S, acc[2] * inv_S, acc[3] * inv_S);
+        if (!shared) *reinterpret_cast<float4*>(o) = v4;
+        else if (__any_sync(FULL, acc[0] != 0.f || acc[1] != 0.f || acc[2] != 0.f || acc[3] != 0.f)) red_add_v4(o, v4);
+      } else {
+        const float2 v2 = make_float2(acc[0] * inv_S, acc[1] * inv_S);
+        if (!shared) *reinterpret_cast<float2*>(o) = v2;
+        else if (__any_sync(FULL, acc[0] != 0.f || acc[1] != 0.f)) red_add_v2(o, v2);
+      }
+      SANTA_STAMP(14);
+    }
+    if (!shared) group_sync(bar_id, nthr);   // the region is free for the next piece
+  };
+
+  // ---- work items, in order: preparation of the shared pieces (their
+  //      groups), the pieces inside the range (all warps), the grid wait, the
+  //      rest of the shared pieces.  One call site each.
+  const int gi = n_shared == 2 ? warp / (FW / 2) : 0;             // this warp's group for the shared pieces
+  const int sh_slot = n_shared == 2 ? gi : (first_shared ? 0 : 1);
+  const int sh_bar = gi == 0 ? BAR_G0 : BAR_G1;
+  const int sh_w0 = n_shared == 2 ? gi * (FW / 2) : 0, sh_nw = n_shared == 2 ? FW / 2 : FW;
+  unsigned char* const sh_reg = regions + gi * REG;
+  const int sh_bytes = n_shared == 2 ? REG : 2 * REG;
+  Piece psh;
+  SegLayout Lsh;
+  if (n_shared > 0) {
+    psh = piece_at(sh_slot == 0 ? cA : cB);
+    Lsh = seg_layout(sh_reg, sh_bytes, psh.c_hi - psh.c_lo);
+  }
+  Cur pc = cA;
+  int stage = n_shared > 0 ? 0 : 1;
+  for (;;) {
+    Piece p;
+    bool shared = false, do_prep = false, do_finish = false;
+    int slot = 0, gid = 2, bar_id = BAR_INT, w0 = 0, nw = FW, reg_bytes = REG;
+    unsigned char* reg = regions + 2 * REG;
+    if (stage == 0) {            // preparation of this warp's shared piece
+      stage = 1;
+      p = psh;
+      shared = true;
+      do_prep = true;
+      slot = sh_slot;
+      gid = gi;
+      bar_id = sh_bar;
+      w0 = sh_w0;
+      nw = sh_nw;
+      reg = sh_reg;
+      reg_bytes = sh_bytes;
+    } else if (stage == 1) {     // next piece wholly inside the range
+      bool found = false;
+      while (has_range && pc.b < a.B && pc.pb_lo < hi) {
+        const bool inside = pc.pb_lo >= lo && pc.pb_lo + pc.nblk <= hi;
+        if (inside) p = piece_at(pc);
+        pc.kblk = pc.nblk;
+        cur_norm(pc, a);
+        if (inside) {
+          found = true;
+          break;
+        }
+      }
+      if (!found) {
+        SANTA_STAMP(7);
+        stage = 2;
+        if (n_shared == 0) break;
+        cp_async_wait_all();   // the shared pieces' staged scores, visible after the wait's barrier
+        grid_wait(bar_gen, s_gen, a.err);
+        SANTA_STAMP(8);
+        continue;
+      }
+      do_prep = do_finish = true;
+    } else if (stage == 2) {     // the rest of this warp's shared piece
+      stage = 3;
+      p = psh;
+      shared = true;
+      do_finish = true;
+      gid = gi;
+      bar_id = sh_bar;
+      w0 = sh_w0;
+      nw = sh_nw;
+      reg = sh_reg;
+      reg_bytes = sh_bytes;
+    } else {
+      break;
+    }
+    const SegLayout L = shared ? Lsh : seg_layout(reg, reg_bytes, p.c_hi - p.c_lo);
+    if (do_prep) prep_piece(p, L, shared, slot, gid, bar_id, w0, nw);
+    if (do_finish) finish_piece(p, L, shared, gid, bar_id, w0, nw);
+    if (stage == 1 && shared) SANTA_STAMP(6);
+  }
+  cp_async_wait_all();   // no copy outlives the CTA
+  SANTA_STAMP(15);
+}
+
+// Launch of one instantiation: one CTA per SM (at most MAX_CTAS), cooperative.
+template <typename T, int D, int V, bool TMA_K>
+inline cudaError_t launch_fused_inst(const LaunchArgs& a, const CUtensorMap& tm, unsigned* bar_count,
+                                     unsigned* bar_gen, int grid) {
+  using Gm = FGeom<D>;
+  auto kern = fused_decode_kernel<T, D, V, TMA_K>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Gm::SMEM);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(FT);
+  cfg.dynamicSmemBytes = Gm::SMEM;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tm, a, bar_count, bar_gen);
+}
+
+// Every instantiation for one cache dtype: head_dim x variant x K access.
+template <typename T>
+inline cudaError_t launch_fused_dtype(const LaunchArgs& a, const CUtensorMap& tm, bool tma, unsigned* bar_count,
+                                      unsigned* bar_gen, int grid) {
+#define SANTA_FUSED_CASE(DD, VV)                                                                 \
+  if (a.D == DD && a.variant == VV)                                                              \
+    return tma ? launch_fused_inst<T, DD, VV, true>(a, tm, bar_count, bar_gen, grid)           \
+               : launch_fused_inst<T, DD, VV, false>(a, tm, bar_count, bar_gen, grid);
+  SANTA_FUSED_CASE(128, VAR_SYS)
+  SANTA_FUSED_CASE(128, VAR_STRAT)
+  SANTA_FUSED_CASE(128, VAR_IID)
+  SANTA_FUSED_CASE(64, VAR_SYS)
+  SANTA_FUSED_CASE(64, VAR_STRAT)
+  SANTA_FUSED_CASE(64, VAR_IID)
+#undef SANTA_FUSED_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace santa

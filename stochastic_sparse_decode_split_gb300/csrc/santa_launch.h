@@ -9,6 +9,7 @@
 namespace santa {
 
 constexpr int MAX_CTAS = 160;   // bound on the single-launch grid (aggregate slots per head)
+constexpr int MAX_S = 4096;     // largest sample budget (SANTA_MAX_S)
 
 // Everything one decode call needs, already validated and carved out of the workspace.
 struct LaunchArgs {
@@ -21,6 +22,12 @@ struct LaunchArgs {
   int groups_max;  // santa: ceil(ceil(nk_max / WIN) / SPC) sampler CTAs per (b, kv head)
   int tiles_max;   // ceil(nk_max / TILE) score-pass tiles per (b, kv head)
   int num_sms;     // streaming multiprocessors of the device (persistent grid size)
+  int k_host;      // K is page-locked host memory read in place (no TMA on it)
+  // single-launch partition of uniform batches, computed by the launcher
+  // (blk_total = 0: ragged, the kernel computes it): total 16-key blocks and
+  // blk_total = blk_q * grid + blk_r
+  long long blk_total, blk_q;
+  int blk_r;
   int S_max;
   int variant;
   float scale;

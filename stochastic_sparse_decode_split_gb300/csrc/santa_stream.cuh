@@ -31,11 +31,6 @@ constexpr int SB_UNIT_ROWS_X_W = SB_TASKS * 32; // K rows (key, KV head) per uni
 // microseconds; on expiry the kernel flags ERR_TIMEOUT and stops waiting.
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
 
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
 
 // Width of a score-pass unit in KV heads: the largest power of two <= 8 dividing H_kv.
 __host__ __device__ inline int unit_heads(int Hkv) {
