@@ -20,8 +20,10 @@ static_assert(SANTA_DEVERR_NK_BOUND == santa::ERR_NK_BOUND && SANTA_DEVERR_S_RAN
 namespace {
 
 constexpr size_t ALIGN = 256;
-constexpr size_t HEADER = 256;  // error word, grid-barrier counter and generation, padding
-constexpr size_t BAR_COUNT = 64, BAR_GEN = 128;  // header offsets of the grid-barrier words
+constexpr size_t HEADER = 256;  // error word, grid-barrier arrival counters and generation, padding
+// header offsets of the grid-barrier words: arrival counters at 64 and 192
+// (the second at the first + 32 words), generation at 128
+constexpr size_t BAR_COUNT = 64, BAR_GEN = 128;
 
 size_t up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
 

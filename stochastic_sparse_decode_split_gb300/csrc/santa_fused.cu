@@ -75,6 +75,10 @@ cudaError_t launch_fused(const LaunchArgs& a_in, unsigned* bar_count, unsigned* 
     a.blk_q = blocks / grid;
     a.blk_r = (int)(blocks % grid);
   }
+  const long long nblk = (a.nk_max + BK - 1) / BK;
+  a.rdiv_perb = div_reciprocal((unsigned long long)(a.Hkv * nblk));
+  a.rdiv_nblk = div_reciprocal((unsigned long long)nblk);
+  a.rdiv_grid = div_reciprocal((unsigned long long)grid);
   // TMA boxes address cache rows with 32-bit coordinates; K in host memory is
   // read by cp.async
   const long long rows = (long long)a.B * a.nk_max;

@@ -71,6 +71,7 @@ constexpr int BK = SUB;             // keys per block (== statistics chunk)
 constexpr int REG = 64 * 1024;      // phase-B shared-memory region
 constexpr int BAR_G0 = 1, BAR_G1 = 2, BAR_INT = 3;   // named barriers of the phase-B groups
 constexpr unsigned long long GRID_WAIT_NS = 2000000000ull;
+constexpr int STATS_CAP = 1024;     // (block, head) statistics a CTA keeps in shared memory
 
 template <int D>
 struct FGeom {
@@ -82,6 +83,15 @@ struct FGeom {
   static constexpr int CPB = BK * D / 8 / 32;            // 16-byte copies per lane per block (cp.async path)
   static_assert(RING >= 3 * REG, "phase-B regions fit the ring");
 };
+
+// x / d for 32-bit x by a precomputed reciprocal r = floor(2^64 / d) + 1
+// (r = 0 stands for d = 1): the 64-bit multiply-high is exact for x < 2^32.
+__host__ __device__ inline unsigned long long div_reciprocal(unsigned long long d) {
+  return d <= 1 ? 0ull : ~0ull / d + 1ull;
+}
+__device__ __forceinline__ uint32_t div_by(uint32_t x, unsigned long long r) {
+  return r ? (uint32_t)__umul64hi((unsigned long long)x, r) : x;
+}
 
 // ---------------------------------------------------------------------------
 // Exact thresholds.  A threshold is theta = floor(N * Z / (div * 2^24)) for an
@@ -234,32 +244,39 @@ __device__ __forceinline__ Agg make_agg(float m, float l) {
 }
 
 // ---------------------------------------------------------------------------
-// Grid-wide barrier (all CTAs are resident: cooperative launch).  A counter
-// and a generation word in the workspace; each CTA reads the generation
-// before it arrives, the last CTA to arrive resets the counter and advances
-// the generation.  Waits are bounded; on expiry ERR_TIMEOUT is flagged and
-// the CTA proceeds.
+// Grid-wide barrier (all CTAs are resident: cooperative launch).  Two
+// arrival counters and a generation word in the workspace: a launch uses
+// counter (generation & 1), which every CTA increments once without waiting;
+// a CTA that needs the others spins until it reaches the grid size.  The
+// launch's first CTA clears the other counter for the next launch and, once
+// all have arrived, advances the generation.  Waits are bounded; on expiry
+// ERR_TIMEOUT is flagged and the CTA proceeds.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
-  unsigned r;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(r) : "l"(p), "r"(v) : "memory");
-  return r;
-}
 __device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-// Arrival of this CTA (one thread, after the CTA's writes are ordered by a
-// CTA barrier); g is the generation read before arriving.
-__device__ __forceinline__ void grid_arrive(unsigned* count, unsigned* gen, unsigned g) {
-  if (atom_add_acq_rel(count, 1u) == gridDim.x - 1u) {   // the last to arrive
-    atomicExch(count, 0u);
-    st_release(gen, g + 1u);
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Waiting for every CTA's arrival: thread 0 spins until the counter reaches
+// n (bounded), then the CTA proceeds together.
+__device__ __forceinline__ void arrivals_wait(const unsigned* count, unsigned n, int* err,
+                                             unsigned long long limit_ns = GRID_WAIT_NS) {
+  if (threadIdx.x == 0) {
+    const unsigned long long t0 = global_ns();
+    while (ld_acquire(count) < n) {
+      if (global_ns() - t0 > limit_ns) {
+        flag_error(err, ERR_TIMEOUT);
+        break;
+      }
+    }
   }
+  __syncthreads();
 }
 // Waiting half: thread 0 spins until the generation moves past g (bounded),
 // then the CTA proceeds together.
@@ -435,7 +452,8 @@ struct SegLayout {
 struct Part {
   long long T, q;
   int r, P;
-  __device__ __forceinline__ long long lo(int i) const { return q * i + (r * i) / P; }
+  unsigned long long rP;   // reciprocal of P (div_reciprocal)
+  __device__ __forceinline__ long long lo(int i) const { return q * i + div_by((uint32_t)(r * i), rP); }
   // the CTA whose range holds block x (0 <= x < T): the largest i with lo(i) <= x
   __device__ __forceinline__ int cta_of(long long x) const {
     int c = (int)(((float)x + 0.5f) / (float)T * (float)P);
@@ -453,14 +471,14 @@ __device__ __forceinline__ Cur locate_uniform(const LaunchArgs& a, long long x) 
   const int nblk = (int)((a.nk_max + BK - 1) / BK);
   const long long per_b = (long long)a.Hkv * nblk;
   long long r;
-  if (x < (1ll << 32) && per_b < (1ll << 32)) {   // 32-bit division
-    c.b = (int)((uint32_t)x / (uint32_t)per_b);
+  if (x < (1ll << 32) && per_b < (1ll << 32)) {   // 32-bit dividends: multiply-high reciprocals
+    c.b = (int)div_by((uint32_t)x, a.rdiv_perb);
     r = (long long)((uint32_t)x - (uint32_t)c.b * (uint32_t)per_b);
   } else {
     c.b = (int)(x / per_b);
     r = x - (long long)c.b * per_b;
   }
-  c.kvh = (int)((uint32_t)r / (uint32_t)nblk);
+  c.kvh = (int)div_by((uint32_t)r, a.rdiv_nblk);
   c.kblk = (int)(r - (long long)c.kvh * nblk);
   c.nblk = nblk;
   c.row0 = (int64_t)c.b * a.nk_max;
@@ -538,6 +556,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
   __shared__ Cur s_cur[2];                            // blocks lo and hi - 1 (ragged batches)
   __shared__ long long s_part[2];                     // T, q (ragged batches)
   __shared__ HeadState s_hs[3][8];                    // per phase-B group and head
+  __shared__ float2 s_stats[STATS_CAP];               // the range's 16-key (max, exp-sum), when they fit
   __shared__ unsigned s_gen;
 
   SANTA_STAMP(0);
@@ -554,6 +573,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
   //      no wait), a scan of the lengths by one warp for ragged ones
   Part pt;
   pt.P = P;
+  pt.rP = a.rdiv_grid;
   Cur cA, cB;
   if (!a.kv_offsets) {
     pt.T = a.blk_total;
@@ -615,6 +635,10 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
   const bool first_shared = has_range && (cA.pb_lo < lo || cA.pb_lo + cA.nblk > hi);
   const bool two_pieces = has_range && cB.pb_lo != cA.pb_lo;
   const bool last_shared = two_pieces && cB.pb_lo + cB.nblk > hi;
+  // a piece wholly inside the range: the first or last one unshared, or one between them
+  const bool has_interior = has_range && (!first_shared || (two_pieces && !last_shared) ||
+                                          cB.pb_lo > cA.pb_lo + cA.nblk);
+  const bool use_ss = (hi - lo) * G <= STATS_CAP;   // the range's chunk statistics kept in shared memory
   SANTA_STAMP(1);
 
   // ---- phase A: per-warp rings; the first NS blocks are requested first
@@ -663,7 +687,13 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
   // ---- prologue work while the first blocks are in flight
   // the barrier generation before this launch's arrivals (no CTA of this
   // launch can advance it before this one has arrived)
-  if (tid == 32) s_gen = ld_acquire(bar_gen);
+  if (tid == 32) {
+    s_gen = ld_acquire(bar_gen);
+    // launches alternate between two arrival counters; this launch's first
+    // CTA clears the other one for the next launch (the previous launch,
+    // which used it, has completed)
+    if (cta == 0) bar_count[((s_gen & 1u) ^ 1u) * 32] = 0u;
+  }
   if (lane < 16) {   // each warp clears its own running-statistics slots
     s_rm[lane >> 3][warp][lane & 7] = -INFINITY;
     s_rl[lane >> 3][warp][lane & 7] = 0.f;
@@ -797,6 +827,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
         if (g8 == 0 && head < G) {
           a.tile_max[(bh0 + head) * a.chunks_max + cur.kblk] = m;
           a.tile_sum[(bh0 + head) * a.chunks_max + cur.kblk] = l;
+          if (use_ss) s_stats[(warp + FW * k) * G + head] = make_float2(m, l);
         }
         const float nm = fmaxf(rm[hh], m);
         rl[hh] = rl[hh] * fast_exp(rm[hh] - nm) + l * fast_exp(m - nm);
@@ -832,7 +863,11 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
   }
   __syncthreads();
   SANTA_STAMP(4);
-  if (tid == 0) grid_arrive(bar_count, bar_gen, s_gen);
+  unsigned* const arrivals = bar_count + (s_gen & 1u) * 32;   // this launch's arrival counter
+  // arrival: nothing to wait for, but its release holds the issuing warp for
+  // a memory round trip, so it comes from the last warp (no head's warp
+  // unless two shared pieces of 8 heads use every warp)
+  if (tid == FT - 32) red_release_add(arrivals, 1u);
   SANTA_STAMP(5);
 
   // =====================================================================
@@ -878,10 +913,23 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
     lastnz = __reduce_max_sync(FULL, nz);
     return __shfl_sync(FULL, x, 31);
   };
-  // Own-unit chunk mass of chunk c0 + c of head bh relative to 2^ref.
-  auto chunk_mass = [&](int64_t bh, int c, float ref) {
-    const int64_t gi2 = bh * a.chunks_max + c;
-    return mass_fixed(fast_exp2(fmaf(a.tile_max[gi2], LOG2E, -ref)) * a.tile_sum[gi2]);
+  // Chunk c of head g of piece p (a chunk of this range) as an aggregate:
+  // exponent e_c and mass relative to 2^e_c, from its 16-key statistics
+  // (kept in shared memory during the stream when the range's chunks fit)
+  auto chunk_agg = [&](const Piece& p, int g, int c) {
+    if (use_ss) {
+      const float2 st = s_stats[(int)(p.pb_lo + c - lo) * G + g];
+      return make_agg(st.x, st.y);
+    }
+    const int64_t gi2 = ((int64_t)p.b * a.H + (int64_t)p.kvh * G + g) * a.chunks_max + c;
+    return make_agg(a.tile_max[gi2], a.tile_sum[gi2]);
+  };
+  // Own-unit mass of chunk c of head g of piece p: its mass relative to
+  // 2^e_c shifted to the CTA's power 2^e_own (e_own >= e_c), as T_k of an aggregate.
+  auto chunk_mass = [&](const Piece& p, int g, int c, int e_own) {
+    const Agg x = chunk_agg(p, g, c);
+    const int dd = e_own - x.e;
+    return dd < 63 ? (x.F >> dd) : 0ll;
   };
 
   // Preparation of one piece by one group of nw warps (warps w0 .. w0 + nw -
@@ -925,16 +973,19 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
     if (!shared && wl < G) {
       // the whole piece is this CTA's: e_own from the chunk maxima (and Z,
       // when the chunks do not fit one segment, their exact sum)
-      const int64_t bh = bh0 + wl;
       HeadState& H = s_hs[gid][wl];
-      const float* mx = a.tile_max + bh * a.chunks_max;
       float mstar = -INFINITY;
-      for (int c = lane; c < p.nblk; c += 32) mstar = fmaxf(mstar, mx[c]);
+      int e_own = AGG_EMPTY;
+      const int64_t bh = bh0 + wl;
+      for (int c = lane; c < p.nblk; c += 32) {
+        mstar = fmaxf(mstar, a.tile_max[bh * a.chunks_max + c]);
+        e_own = max(e_own, chunk_agg(p, wl, c).e);
+      }
       mstar = warp_max(mstar);
-      const int e_own = mstar > -INFINITY ? (int)ceilf(mstar * LOG2E) : AGG_EMPTY;
+      e_own = __reduce_max_sync(FULL, e_own);
       long long Z = 0;
       if (nch0 < nch_part) {
-        for (int c = lane; c < p.nblk; c += 32) Z += chunk_mass(bh, c, (float)e_own);
+        for (int c = lane; c < p.nblk; c += 32) Z += chunk_mass(p, wl, c, e_own);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(FULL, Z, o);
       }
@@ -945,11 +996,12 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
       }
     }
     if (shared && tg < G) s_hs[gid][tg].ref = (float)s_eown[slot][tg];
-    group_sync(bar_id, nthr);   // own powers visible
+    if (!shared) group_sync(bar_id, nthr);   // own powers visible (a shared piece's are in s_eown)
     // the first segment's chunk masses by the whole group, then one warp per head scans them
+    const float inv_nch0 = 1.0f / (float)nch0;
     for (int it = tg; it < G * nch0; it += nthr) {
-      const int h = it / nch0, c = it - h * nch0;
-      L.w[h * L.segc + c] = chunk_mass(bh0 + h, p.c_lo + c, s_hs[gid][h].ref);
+      const int h = (int)(((float)it + 0.5f) * inv_nch0), c = it - h * nch0;   // it / nch0 (exact: it < 2^13)
+      L.w[h * L.segc + c] = chunk_mass(p, h, p.c_lo + c, shared ? s_eown[slot][h] : (int)s_hs[gid][h].ref);
     }
     group_sync(bar_id, nthr);
     if (wl < G) {
@@ -1073,7 +1125,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
       for (int sg = 0; sg < L.nseg && j < jr.y; ++sg) {
         const int c0 = p.c_lo + sg * L.segc, nch = min(L.segc, p.c_hi - c0);
         if (sg > 0) {   // this segment's chunk prefixes, by this warp alone
-          for (int c = lane; c < nch; c += 32) L.w[wl * L.segc + c] = chunk_mass(bh, c0 + c, ref);
+          for (int c = lane; c < nch; c += 32) L.w[wl * L.segc + c] = chunk_mass(p, wl, c0 + c, (int)ref);
           __syncwarp();
           seg_end = scan_head(L, wl, nch, seg_end, lastnz);
           __syncwarp();
@@ -1096,14 +1148,13 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
             const bool gap = x >= seg_end;   // rounding gap at the range's end: the last nonzero chunk
             if (gap) {
               c = lastnz;
-            } else {
-              int lo2 = 0, hi2 = nch - 1;   // the last chunk with pref <= x
-              while (lo2 < hi2) {
-                const int mid = (lo2 + hi2 + 1) >> 1;
-                if (pr[mid] <= x) lo2 = mid;
-                else hi2 = mid - 1;
+            } else {   // the last chunk with pref <= x (pref[0] <= x), by halving steps
+              c = 0;
+#pragma unroll
+              for (int sh = 12; sh >= 0; --sh) {
+                const int t = c + (1 << sh);
+                if (t < nch && pr[t] <= x) c = t;
               }
-              c = lo2;
             }
             if (c < 0) {
               key = c0 * BK;   // no mass in the range at all (never expected)
@@ -1223,7 +1274,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
       reg_bytes = sh_bytes;
     } else if (stage == 1) {     // next piece wholly inside the range
       bool found = false;
-      while (has_range && pc.b < a.B && pc.pb_lo < hi) {
+      while (has_interior && pc.b < a.B && pc.pb_lo < hi) {
         const bool inside = pc.pb_lo >= lo && pc.pb_lo + pc.nblk <= hi;
         if (inside) p = piece_at(pc);
         pc.kblk = pc.nblk;
@@ -1238,7 +1289,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
         stage = 2;
         if (n_shared == 0) break;
         cp_async_wait_all();   // the shared pieces' staged scores, visible after the wait's barrier
-        grid_wait(bar_gen, s_gen, a.err);
+        arrivals_wait(arrivals, (unsigned)P, a.err);
         SANTA_STAMP(8);
         continue;
       }
@@ -1263,6 +1314,12 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
     if (stage == 1 && shared) SANTA_STAMP(6);
   }
   cp_async_wait_all();   // no copy outlives the CTA
+  // the first CTA, once every CTA has arrived (each read the generation
+  // before arriving), advances the generation for the next launch
+  if (cta == 0) {
+    if (n_shared == 0) arrivals_wait(arrivals, (unsigned)P, a.err);
+    if (tid == 0) st_release(bar_gen, s_gen + 1u);
+  }
   SANTA_STAMP(15);
 }
 

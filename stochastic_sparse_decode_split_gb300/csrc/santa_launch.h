@@ -28,6 +28,10 @@ struct LaunchArgs {
   // blk_total = blk_q * grid + blk_r
   long long blk_total, blk_q;
   int blk_r;
+  // uniform batch: multiply-high reciprocals of H_kv * blocks per sequence,
+  // blocks per sequence and the grid (division by invariant integers, for
+  // 32-bit dividends; 0 for a divisor of 1)
+  unsigned long long rdiv_perb, rdiv_nblk, rdiv_grid;
   int S_max;
   int variant;
   float scale;
