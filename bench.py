@@ -38,6 +38,7 @@ FLUSH_BYTES = 512 * 1024 * 1024
 KERNEL_SOURCES = ["stochastic_sparse_decode_split_gb300/csrc/santa_fused.cuh",
                   "stochastic_sparse_decode_split_gb300/csrc/santa_fused.cu",
                   "stochastic_sparse_decode_split_gb300/csrc/santa_tma.cuh",
+                  "stochastic_sparse_decode_split_gb300/csrc/santa_part.cuh",
                   "stochastic_sparse_decode_split_gb300/csrc/santa_window.cuh",
                   "stochastic_sparse_decode_split_gb300/csrc/santa_common.cuh",
                   "stochastic_sparse_decode_split_gb300/csrc/santa_seq.cuh"]

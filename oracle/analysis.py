@@ -10,11 +10,14 @@ Attention for Memory-Bound Inference":
 * independent stratified variance trace (1/S^2) sum_m tr(Sigma_m), Sigma_m
   the value covariance of the within-stratum distribution (App. A.5,
   Thm. A.6; App. M);
-* systematic variance by replicates (App. M) -- no closed form exists;
+* systematic variance by replicates (App. M), and exactly as the integral
+  over the shared offset u of the squared deviation of the estimate, which is
+  constant between the offsets where a threshold (j + u)/S crosses a CDF edge
+  (Sec. 2.1 systematic sampling; the paper gives no closed form);
 * vector Bernstein tail for i.i.d. SANTA (App. B, Thm. B.1);
-* expected number of distinct keys drawn (App. L, App. M.1 item 1) and the
-  expected share of V rows a causal prefill pass reads (App. F, Table 9),
-  both for i.i.d. SANTA, where draws are independent.
+* expected number of distinct keys drawn (App. L, App. M.1 item 1) for the
+  i.i.d., stratified and systematic samplers, and the expected share of V
+  rows a causal prefill pass of i.i.d. SANTA reads (App. F, Table 9).
 
 Strata follow Sec. 2.1: I_m = [m/S, (m+1)/S), with the inverse CDF of App. A.4.
 """
@@ -100,6 +103,57 @@ def expectation_over_offset(estimator, breakpoints: np.ndarray) -> np.ndarray:
         val = np.asarray(estimator(0.5 * (a + b)), np.float64) * (b - a)
         total = val if total is None else total + val
     return total
+
+
+def systematic_estimates(p: np.ndarray, V: np.ndarray, S: int, u: np.ndarray) -> np.ndarray:
+    """The systematic estimate (1/S) sum_j V[F^-1((j + u)/S)] for each offset
+    in u (shape [M]); F^-1(t) is the first key n with F(n) > t (App. A.4)."""
+    F = cdf(p)
+    V = np.asarray(V, np.float64)
+    t = (np.arange(S, dtype=np.float64)[None, :] + np.asarray(u, np.float64)[:, None]) / S
+    keys = np.minimum(np.searchsorted(F, t, side="right"), len(F) - 1)
+    return V[keys].mean(axis=1)
+
+
+def systematic_coordinate_variance(p: np.ndarray, V: np.ndarray, S: int) -> np.ndarray:
+    """Per output coordinate, the exact variance of the systematic estimate
+    over u ~ U[0, 1): the integral of (estimate(u) - mu)^2.
+
+    As u grows each CDF edge F(n) < 1 is passed by exactly one threshold
+    (j + u)/S, at u = S F(n) - floor(S F(n)), and that threshold's key moves
+    from n to n + 1, changing the estimate by (V[n+1] - V[n]) / S.  So the
+    estimate is the u = 0 estimate plus a running sum of these steps in the
+    order of their offsets, constant in between: O(nk d) in all."""
+    V = np.asarray(V, np.float64)
+    F = cdf(p)
+    mu = exact_mean(p, V)
+    x = S * F[:-1]
+    jn = np.floor(x)
+    ue = x - jn
+    ev = np.nonzero((ue > 0.0) & (jn < S))[0]          # edges passed for some u in (0, 1)
+    order = np.argsort(ue[ev], kind="stable")
+    ev = ev[order]
+    steps = (V[ev + 1] - V[ev]) / S
+    states = np.concatenate([systematic_estimates(p, V, S, np.zeros(1)),
+                             systematic_estimates(p, V, S, np.zeros(1)) + np.cumsum(steps, axis=0)])
+    cuts = np.concatenate([[0.0], ue[ev], [1.0]])
+    dev = states - mu
+    return np.diff(cuts) @ (dev * dev)
+
+
+def expected_unique_keys_systematic(p: np.ndarray, S: int) -> float:
+    """E|U| for systematic sampling: key n is drawn as often as the lattice
+    {(j + u)/S} meets [F(n-1), F(n)), an interval of length p_n, so at least
+    once with probability min(1, S p_n)."""
+    return float(np.minimum(1.0, S * np.asarray(p, np.float64)).sum())
+
+
+def expected_unique_keys_stratified(p: np.ndarray, S: int) -> float:
+    """E|U| for independent stratified sampling: stratum m draws key n with
+    probability w[m, n] (stratum_weights), independently of the other
+    strata, so key n is missed with probability prod_m (1 - w[m, n])."""
+    w = stratum_weights(p, S)
+    return float((1.0 - np.prod(1.0 - w, axis=0)).sum())
 
 
 def replicate_variance_trace(estimates: np.ndarray) -> float:

@@ -54,6 +54,7 @@
 #include "santa_common.cuh"
 #include "santa_launch.h"
 #include "santa_seq.cuh"
+#include "santa_part.cuh"
 #include "santa_tma.cuh"
 #include "santa_window.cuh"
 
@@ -67,7 +68,6 @@ namespace santa {
 
 constexpr int FW = 16;              // warps per CTA
 constexpr int FT = FW * 32;         // threads per CTA
-constexpr int BK = SUB;             // keys per block (== statistics chunk)
 constexpr int REG = 64 * 1024;      // phase-B shared-memory region
 constexpr int BAR_G0 = 1, BAR_G1 = 2, BAR_INT = 3;   // named barriers of the phase-B groups
 constexpr unsigned long long GRID_WAIT_NS = 2000000000ull;
@@ -83,15 +83,6 @@ struct FGeom {
   static constexpr int CPB = BK * D / 8 / 32;            // 16-byte copies per lane per block (cp.async path)
   static_assert(RING >= 3 * REG, "phase-B regions fit the ring");
 };
-
-// x / d for 32-bit x by a precomputed reciprocal r = floor(2^64 / d) + 1
-// (r = 0 stands for d = 1): the 64-bit multiply-high is exact for x < 2^32.
-__host__ __device__ inline unsigned long long div_reciprocal(unsigned long long d) {
-  return d <= 1 ? 0ull : ~0ull / d + 1ull;
-}
-__device__ __forceinline__ uint32_t div_by(uint32_t x, unsigned long long r) {
-  return r ? (uint32_t)__umul64hi((unsigned long long)x, r) : x;
-}
 
 // ---------------------------------------------------------------------------
 // Exact thresholds.  A threshold is theta = floor(N * Z / (div * 2^24)) for an
@@ -296,119 +287,13 @@ __device__ __forceinline__ void grid_wait(const unsigned* gen, unsigned g, int* 
   __syncthreads();
 }
 
-// ---------------------------------------------------------------------------
-// Block enumeration over the actual sequence lengths
-// ---------------------------------------------------------------------------
-struct SeqGeo {
-  int64_t row0, nk;
-  int nblk;
+// The CTA's share of the partition, as phase B reads it (shared memory).
+struct CtaRange {
+  Part pt;
+  long long lo, hi;        // blocks [lo, hi)
+  Cur cA, cB;              // blocks lo and hi - 1
+  int has_range, first_shared, last_shared, has_interior, use_ss;
 };
-// Rows of sequence b; lengths outside [1, nk_max] are clamped here (the
-// metadata check reports them).
-__device__ __forceinline__ SeqGeo seq_geo(const LaunchArgs& a, int b) {
-  SeqGeo g;
-  if (a.kv_offsets) {
-    g.row0 = a.kv_offsets[b];
-    g.nk = a.kv_offsets[b + 1] - g.row0;
-  } else {
-    g.row0 = (int64_t)b * a.nk_max;
-    g.nk = a.nk_max;
-  }
-  if (g.nk < 1 || g.row0 < 0) g.nk = 0;
-  if (g.nk > a.nk_max) g.nk = a.nk_max;
-  g.nblk = (int)((g.nk + BK - 1) / BK);
-  return g;
-}
-
-// Position of one block: sequence b, KV head kvh, key block kblk of the
-// sequence; pb_lo is the global index of block 0 of piece (b, kvh).
-struct Cur {
-  int b, kvh, kblk, nblk;
-  int64_t row0, nk;
-  long long pb_lo;
-};
-// Moves kblk past the end of its piece into the following pieces (b = B: end).
-__device__ __forceinline__ void cur_norm(Cur& c, const LaunchArgs& a) {
-  while (c.kblk >= c.nblk) {
-    c.kblk -= c.nblk;
-    c.pb_lo += c.nblk;
-    if (++c.kvh == a.Hkv) {
-      c.kvh = 0;
-      if (++c.b >= a.B) {
-        c.b = a.B;
-        c.nblk = INT_MAX;
-        return;
-      }
-      const SeqGeo g = seq_geo(a, c.b);
-      c.row0 = g.row0;
-      c.nk = g.nk;
-      c.nblk = g.nblk;
-    }
-  }
-}
-__device__ __forceinline__ void cur_advance(Cur& c, const LaunchArgs& a, int n) {
-  c.kblk += n;
-  cur_norm(c, a);
-}
-
-// The cursors of blocks x0 and x1 (x0 <= x1 < T) and the total T, computed by
-// one warp.  Uniform batches are closed form; ragged ones scan the lengths.
-__device__ __forceinline__ long long total_blocks(const LaunchArgs& a, int lane) {
-  if (!a.kv_offsets) return (long long)a.B * a.Hkv * ((a.nk_max + BK - 1) / BK);
-  long long total = 0;
-  for (int b0 = 0; b0 < a.B; b0 += 32) {
-    long long s = (b0 + lane < a.B) ? (long long)seq_geo(a, b0 + lane).nblk : 0;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(FULL, s, o);
-    total += s;
-  }
-  return total * a.Hkv;
-}
-__device__ __forceinline__ Cur locate_block(const LaunchArgs& a, long long x, int lane) {
-  Cur c;
-  if (!a.kv_offsets) {
-    const int nblk = (int)((a.nk_max + BK - 1) / BK);
-    const long long per_b = (long long)a.Hkv * nblk;
-    c.b = (int)(x / per_b);
-    const long long r = x - (long long)c.b * per_b;
-    c.kvh = (int)(r / nblk);
-    c.kblk = (int)(r - (long long)c.kvh * nblk);
-    c.nblk = nblk;
-    c.row0 = (int64_t)c.b * a.nk_max;
-    c.nk = a.nk_max;
-    c.pb_lo = x - c.kblk;
-    return c;
-  }
-  long long base = 0;
-  c.b = a.B;
-  for (int b0 = 0; b0 < a.B; b0 += 32) {
-    const int nb = (b0 + lane < a.B) ? seq_geo(a, b0 + lane).nblk : 0;
-    long long incl = (long long)nb * a.Hkv;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long t = __shfl_up_sync(FULL, incl, o);
-      if (lane >= o) incl += t;
-    }
-    const unsigned hit = __ballot_sync(FULL, base + incl > x);
-    if (hit) {
-      const int l = __ffs(hit) - 1;
-      const int nbl = __shfl_sync(FULL, nb, l);
-      const long long excl = base + __shfl_sync(FULL, incl, l) - (long long)nbl * a.Hkv;
-      c.b = b0 + l;
-      const long long r = x - excl;
-      c.kvh = (int)(r / nbl);
-      c.kblk = (int)(r - (long long)c.kvh * nbl);
-      c.nblk = nbl;
-      const SeqGeo g = seq_geo(a, c.b);
-      c.row0 = g.row0;
-      c.nk = g.nk;
-      c.pb_lo = x - c.kblk;
-      break;
-    }
-    base += __shfl_sync(FULL, incl, 31);
-  }
-  return c;
-}
 
 // One piece as seen by one CTA.
 struct Piece {
@@ -446,46 +331,6 @@ struct SegLayout {
   float* st;                // [G][capk] the range's scores (staged from the 16-byte boundary below), or NULL
   int segc, nseg, capk;
 };
-
-// The single-launch partition: CTA i of P takes blocks [lo(i), lo(i + 1)),
-// lo(i) = floor(T i / P) = q i + floor(r i / P) with T = q P + r.
-struct Part {
-  long long T, q;
-  int r, P;
-  unsigned long long rP;   // reciprocal of P (div_reciprocal)
-  __device__ __forceinline__ long long lo(int i) const { return q * i + div_by((uint32_t)(r * i), rP); }
-  // the CTA whose range holds block x (0 <= x < T): the largest i with lo(i) <= x
-  __device__ __forceinline__ int cta_of(long long x) const {
-    int c = (int)(((float)x + 0.5f) / (float)T * (float)P);
-    c = min(max(c, 0), P - 1);
-    while (c + 1 < P && lo(c + 1) <= x) ++c;
-    while (c > 0 && lo(c) > x) --c;
-    return c;
-  }
-  __device__ __forceinline__ bool nonempty(int i) const { return T >= P || lo(i) < lo(i + 1); }
-};
-
-// Cursor of block x of a uniform batch (every sequence nk_max keys).
-__device__ __forceinline__ Cur locate_uniform(const LaunchArgs& a, long long x) {
-  Cur c;
-  const int nblk = (int)((a.nk_max + BK - 1) / BK);
-  const long long per_b = (long long)a.Hkv * nblk;
-  long long r;
-  if (x < (1ll << 32) && per_b < (1ll << 32)) {   // 32-bit dividends: multiply-high reciprocals
-    c.b = (int)div_by((uint32_t)x, a.rdiv_perb);
-    r = (long long)((uint32_t)x - (uint32_t)c.b * (uint32_t)per_b);
-  } else {
-    c.b = (int)(x / per_b);
-    r = x - (long long)c.b * per_b;
-  }
-  c.kvh = (int)div_by((uint32_t)r, a.rdiv_nblk);
-  c.kblk = (int)(r - (long long)c.kvh * nblk);
-  c.nblk = nblk;
-  c.row0 = (int64_t)c.b * a.nk_max;
-  c.nk = a.nk_max;
-  c.pb_lo = x - c.kblk;
-  return c;
-}
 
 // ---------------------------------------------------------------------------
 // i.i.d.: sorted 24-bit uniform keys of one head into ukeys (all threads of
@@ -558,6 +403,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
   __shared__ HeadState s_hs[3][8];                    // per phase-B group and head
   __shared__ float2 s_stats[STATS_CAP];               // the range's 16-key (max, exp-sum), when they fit
   __shared__ unsigned s_gen;
+  __shared__ CtaRange s_rg;
 
   SANTA_STAMP(0);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -570,52 +416,83 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
     if (tid == 0) prefetch_tensormap(&tmap);
 
   // ---- the CTA's block range: closed form for uniform batches (every thread,
-  //      no wait), a scan of the lengths by one warp for ragged ones
-  Part pt;
-  pt.P = P;
-  pt.rP = a.rdiv_grid;
-  Cur cA, cB;
-  if (!a.kv_offsets) {
-    pt.T = a.blk_total;
-    pt.q = a.blk_q;
-    pt.r = a.blk_r;
-  } else {
-    if (warp == 0) {
-      const long long Tb = total_blocks(a, lane);
-      if (lane == 0) {
-        s_part[0] = Tb;
-        s_part[1] = Tb / P;
+  //      no wait), a scan of the lengths by one warp for ragged ones.  Kept in
+  //      shared memory (s_rg) and read from there: no register holds it
+  //      across the stream.
+  {
+    Part pt;
+    pt.P = P;
+    pt.rP = a.rdiv_grid;
+    Cur cA, cB;
+    if (!a.kv_offsets) {
+      pt.T = a.blk_total;
+      pt.q = a.blk_q;
+      pt.r = a.blk_r;
+    } else {
+      if (warp == 0) {
+        const long long Tb = total_blocks(a, lane);
+        if (lane == 0) {
+          s_part[0] = Tb;
+          s_part[1] = Tb / P;
+        }
       }
+      __syncthreads();
+      pt.T = s_part[0];
+      pt.q = s_part[1];
+      pt.r = (int)(pt.T - pt.q * P);
     }
-    __syncthreads();
-    pt.T = s_part[0];
-    pt.q = s_part[1];
-    pt.r = (int)(pt.T - pt.q * P);
-  }
-  const long long lo = pt.lo(cta), hi = pt.lo(cta + 1);
-  const bool has_range = hi > lo;
-  if (!a.kv_offsets) {
-    if (has_range) {
-      cA = locate_uniform(a, lo);
-      cB = locate_uniform(a, hi - 1);
-    }
-  } else {
-    if (warp == 0 && has_range) {
-      const Cur c0 = locate_block(a, lo, lane), c1 = locate_block(a, hi - 1, lane);
-      if (lane == 0) {
-        s_cur[0] = c0;
-        s_cur[1] = c1;
+    const long long lo = pt.lo(cta), hi = pt.lo(cta + 1);
+    const bool has_range = hi > lo;
+    if (!a.kv_offsets) {
+      if (has_range) {
+        cA = locate_uniform(a, lo);
+        cB = locate_uniform(a, hi - 1);
       }
+    } else {
+      if (warp == 0 && has_range) {
+        const Cur c0 = locate_block(a, lo, lane), c1 = locate_block(a, hi - 1, lane);
+        if (lane == 0) {
+          s_cur[0] = c0;
+          s_cur[1] = c1;
+        }
+      }
+      __syncthreads();
+      cA = s_cur[0];
+      cB = s_cur[1];
     }
-    __syncthreads();
-    cA = s_cur[0];
-    cB = s_cur[1];
+    if (!has_range) {
+      cA.b = cB.b = a.B;
+      cA.pb_lo = cB.pb_lo = LLONG_MAX;
+      cA.nblk = cB.nblk = INT_MAX;
+    }
+    // shared pieces: slot 0 = the first piece of the range, slot 1 = the last
+    // (when it is another piece); a piece is shared when it crosses the range
+    const bool first_shared = has_range && (cA.pb_lo < lo || cA.pb_lo + cA.nblk > hi);
+    const bool two_pieces = has_range && cB.pb_lo != cA.pb_lo;
+    const bool last_shared = two_pieces && cB.pb_lo + cB.nblk > hi;
+    // a piece wholly inside the range: the first or last one unshared, or one between them
+    const bool has_interior = has_range && (!first_shared || (two_pieces && !last_shared) ||
+                                            cB.pb_lo > cA.pb_lo + cA.nblk);
+    const bool use_ss = (hi - lo) * G <= STATS_CAP;   // the range's chunk statistics kept in shared memory
+    if (tid == 0) {
+      s_rg.pt = pt;
+      s_rg.lo = lo;
+      s_rg.hi = hi;
+      s_rg.cA = cA;
+      s_rg.cB = cB;
+      s_rg.has_range = has_range;
+      s_rg.first_shared = first_shared;
+      s_rg.last_shared = last_shared;
+      s_rg.has_interior = has_interior;
+      s_rg.use_ss = use_ss;
+    }
   }
-  if (!has_range) {
-    cA.b = cB.b = a.B;
-    cA.pb_lo = cB.pb_lo = LLONG_MAX;
-    cA.nblk = cB.nblk = INT_MAX;
-  }
+  __syncthreads();
+  const Part& pt = s_rg.pt;
+  const long long &lo = s_rg.lo, &hi = s_rg.hi;
+  const Cur &cA = s_rg.cA, &cB = s_rg.cB;
+  const int &has_range = s_rg.has_range, &first_shared = s_rg.first_shared, &last_shared = s_rg.last_shared;
+  const int &has_interior = s_rg.has_interior, &use_ss = s_rg.use_ss;
   auto piece_at = [&](const Cur& c) {
     Piece p;
     p.b = c.b;
@@ -630,15 +507,6 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
     p.i_last = pt.cta_of(c.pb_lo + c.nblk - 1);
     return p;
   };
-  // shared pieces: slot 0 = the first piece of the range, slot 1 = the last
-  // (when it is another piece); a piece is shared when it crosses the range
-  const bool first_shared = has_range && (cA.pb_lo < lo || cA.pb_lo + cA.nblk > hi);
-  const bool two_pieces = has_range && cB.pb_lo != cA.pb_lo;
-  const bool last_shared = two_pieces && cB.pb_lo + cB.nblk > hi;
-  // a piece wholly inside the range: the first or last one unshared, or one between them
-  const bool has_interior = has_range && (!first_shared || (two_pieces && !last_shared) ||
-                                          cB.pb_lo > cA.pb_lo + cA.nblk);
-  const bool use_ss = (hi - lo) * G <= STATS_CAP;   // the range's chunk statistics kept in shared memory
   SANTA_STAMP(1);
 
   // ---- phase A: per-warp rings; the first NS blocks are requested first
@@ -944,6 +812,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
     const int wl = warp - w0, tg = tid - w0 * 32, nthr = nw * 32;
     int S_b;
     if (seq_error(a, p.b, S_b)) return;
+    SANTA_STAMP(16);
     const int64_t bh0 = (int64_t)p.b * a.H + (int64_t)p.kvh * G;
     const int nch_part = p.c_hi - p.c_lo;
     const int nch0 = min(L.segc, nch_part);
@@ -961,6 +830,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
       }
       cp_async_commit();
     }
+    SANTA_STAMP(17);
     // threshold constants of head g by warp w0 + (G + g) % nw (lane 0)
     for (int g = 0; g < G; ++g)
       if (wl == (G + g) % nw && lane == 0) {
@@ -995,6 +865,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
         H.Z = Z;
       }
     }
+    SANTA_STAMP(18);
     if (shared && tg < G) s_hs[gid][tg].ref = (float)s_eown[slot][tg];
     if (!shared) group_sync(bar_id, nthr);   // own powers visible (a shared piece's are in s_eown)
     // the first segment's chunk masses by the whole group, then one warp per head scans them
@@ -1004,6 +875,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
       L.w[h * L.segc + c] = chunk_mass(p, h, p.c_lo + c, shared ? s_eown[slot][h] : (int)s_hs[gid][h].ref);
     }
     group_sync(bar_id, nthr);
+    SANTA_STAMP(19);
     if (wl < G) {
       HeadState& H = s_hs[gid][wl];
       int lastnz;
@@ -1020,6 +892,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
         }
       }
     }
+    SANTA_STAMP(22);
   };
 
   // The rest of one piece (same group, region and layout as its

@@ -17,15 +17,18 @@ namespace santa {
 // truncates; masses below 2^-40 of the max key count as zero.
 constexpr int MASS_SHIFT = 40;
 
-// w * 2^40 rounded toward zero, for finite w in [0, 2^22), by integer operations.
+// w * 2^40 rounded toward zero, for finite w in [0, 2^22), by integer
+// operations without branches (both shifts computed, one selected): zero,
+// subnormal, non-finite and negative w give 0.
 __device__ __forceinline__ long long mass_fixed(float w) {
   const uint32_t bits = __float_as_uint(w);
   const int e = (int)((bits >> 23) & 0xffu);
-  if (e == 0 || e == 0xff || (bits >> 31)) return 0;          // zero, subnormal, non-finite, negative
-  const long long m = (long long)((bits & 0x7fffffu) | 0x800000u);
+  const unsigned long long m = (unsigned long long)((bits & 0x7fffffu) | 0x800000u);
   const int sh = e - 127 - 23 + MASS_SHIFT;                  // w * 2^40 = m * 2^sh
-  if (sh >= 0) return m << min(sh, 39);
-  return sh > -64 ? (m >> -sh) : 0;
+  const unsigned long long up = m << (unsigned)min(max(sh, 0), 39);
+  const unsigned long long dn = m >> (unsigned)min(max(-sh, 0), 63);
+  const bool ok = e != 0 && e != 0xff && !(bits >> 31);
+  return ok ? (long long)(sh >= 0 ? up : dn) : 0ll;
 }
 
 // Inclusive warp scan of one int64 per lane.

@@ -379,7 +379,8 @@ def test_mean_over_10k_seeds_within_4_sigma(variant, which):
     P = oracle.Problem.from_inputs(inp)
     mu = oracle.dense(P)
     B, H, _ = inp.q.shape
-    zs = []
+    zs, vars_ = [], []
+    vmax = 0.0
     for b in range(B):
         for h in range(H):
             _, p = oracle.scores(P, b, h)
@@ -390,20 +391,39 @@ def test_mean_over_10k_seeds_within_4_sigma(variant, which):
                 var = analysis.iid_coordinate_variance(p, V, S)
             elif variant == "stratified":
                 var = analysis.stratified_coordinate_variance(p, V, S)
-            else:
-                var = var_emp[b, h]   # replicate estimate (no closed form for systematic)
+            else:   # exact integral over the shared offset u
+                var = analysis.systematic_coordinate_variance(p, V, S)
+            vars_.append(var)
             # standard error of the mean, floored by fp32 rounding of one estimate
+            vmax = max(vmax, float(np.abs(V).max()))
             se = np.sqrt(var / R + (2e-6 * np.abs(V).max()) ** 2)
             zs.append(np.abs(mean[b, h] - mu[b, h]) / se)
-    # Every coordinate within 4 sigma, with the bound widened to the family-wise
-    # (Bonferroni, two-sided 1e-3) level when many coordinates are tested at
-    # once; and no bias inflating the mean squared z-score.
-    from scipy.stats import norm
+    # Each coordinate is held to 4 sigma.  Among n coordinates some may pass
+    # 4 sigma by chance (two-sided rate 6.3e-5 each): the number that do is
+    # Binomial(n, 6.3e-5) and must stay within its 1 - 1e-6 quantile, and no
+    # coordinate may pass 6 sigma.  No bias may inflate the mean squared z.
+    from scipy.stats import binom, norm
     z = np.concatenate(zs)
     n = z.size
-    z_allowed = max(4.0, float(norm.isf(0.5e-3 / n)))
-    assert z.max() <= z_allowed, f"max z {z.max():.2f} over {n} coordinates (allowed {z_allowed:.2f})"
+    k_allowed = int(binom.isf(1e-6, n, 2.0 * norm.sf(4.0)))
+    over = int((z > 4.0).sum())
+    assert over <= k_allowed, f"{over} of {n} coordinates beyond 4 sigma (allowed {k_allowed}); max z {z.max():.2f}"
+    assert z.max() <= 6.0, f"max z {z.max():.2f}"
     assert np.mean(z * z) <= 1.0 + 5.0 * np.sqrt(2.0 / n), f"mean z^2 {np.mean(z * z):.3f}"
+    # the GPU's replicate variance (App. M) agrees with the exact one: per
+    # head its trace within 10 %, per coordinate within 5 % at the median;
+    # a head whose exact variance is below the fp32 rounding of one estimate
+    # (nearly deterministic draws) only has to stay that small
+    v = np.stack(vars_).reshape(B, H, -1)
+    floor = v.shape[-1] * (2e-6 * vmax) ** 2
+    tv, te = v.sum(-1), var_emp.sum(-1)
+    live = tv > 100.0 * floor
+    assert np.all(te[~live] <= 1000.0 * floor), (te[~live], floor)
+    if live.any():
+        tr_rel = np.abs(te[live] - tv[live]) / tv[live]
+        assert tr_rel.max() < 0.10, tr_rel.max()
+        big = (v > 1e-3 * v.max()) & live[..., None]
+        assert np.median(np.abs(var_emp[big] - v[big]) / v[big]) < 0.05
 
 
 def test_bounded_wait_times_out():

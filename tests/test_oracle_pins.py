@@ -328,9 +328,50 @@ def test_mean_over_seeds_within_4_sigma(oracle_lib, variant):
     elif variant == "stratified":
         var = analysis.stratified_coordinate_variance(p, V, S)
     else:
-        var = E.var(axis=0, ddof=1)
+        var = analysis.systematic_coordinate_variance(p, V, S)
+        # the exact integral agrees with the replicate estimate (App. M)
+        np.testing.assert_allclose(E.var(axis=0, ddof=1), var, rtol=0.15)
     sigma = np.sqrt(np.maximum(var, 1e-14) / R)
     assert np.all(np.abs(E.mean(axis=0) - mu) <= 4.0 * sigma)
+
+
+@pytest.mark.parametrize("S", [1, 2, 5, 16])
+def test_systematic_variance_is_the_integral_over_the_oracle_sampler(oracle_lib, S):
+    """The exact systematic variance (float CDF, vectorised) equals the
+    integral over u of the squared deviation of the oracle's own sampler
+    (fixed-point thresholds, Sec. 2.1 / App. A.4), piece by piece."""
+    rng = np.random.default_rng(60 + S)
+    P = random_problem(oracle_lib, rng, 23, 5, spread=1.5)
+    _, p = oracle_lib.scores(P, 0, 0)
+    V = values_of(P, 0, 0)
+    mu = oracle_lib.dense(P)[0, 0]
+
+    def sq_dev(u):
+        est = oracle_lib.sample_head(P, 0, 0, (np.arange(S) + u) / S)[0]
+        return (est - mu) ** 2
+
+    want = analysis.expectation_over_offset(sq_dev, analysis.systematic_breakpoints(p, S))
+    np.testing.assert_allclose(analysis.systematic_coordinate_variance(p, V, S), want, rtol=1e-8, atol=1e-14)
+
+
+def test_systematic_variance_special_cases():
+    """S = 1 is one inverse-CDF draw from a uniform: the single-draw variance
+    sum_n p_n V_n^2 - mu^2.  When every S p_n is an integer each key is drawn
+    exactly S p_n times whatever u: variance zero.  Equal V rows: zero."""
+    rng = np.random.default_rng(61)
+    p = rng.dirichlet(np.ones(40))
+    V = rng.standard_normal((40, 7)) * 2.0 + 1.0
+    np.testing.assert_allclose(analysis.systematic_coordinate_variance(p, V, 1),
+                               analysis.iid_coordinate_variance(p, V, 1), rtol=1e-10)
+    q = np.array([2, 1, 0, 5, 3, 5], np.float64) / 16.0
+    Vq = rng.standard_normal((6, 4))
+    assert np.abs(analysis.systematic_coordinate_variance(q, Vq, 16)).max() < 1e-20
+    assert np.abs(analysis.systematic_coordinate_variance(p, np.tile(V[3], (40, 1)), 9)).max() < 1e-20
+    # an average of S draws whose thresholds are uniform on the strata: by
+    # Cauchy-Schwarz and the law of total variance it varies no more than a
+    # single draw (and, for generic p, more than not at all)
+    v_sys = analysis.systematic_coordinate_variance(p, V, 8)
+    assert np.all(v_sys > 0) and np.all(v_sys <= analysis.iid_coordinate_variance(p, V, 1))
 
 
 def test_closed_form_variances_special_cases():
@@ -722,6 +763,40 @@ def test_unique_keys_iid_closed_form_matches_the_sampler(oracle_lib):
         want = analysis.expected_unique_keys_iid(p, S)
         got = [np.unique(oracle_lib.decode(P, "iid", S, seed=s)[1][0, 0]).size for s in range(200)]
         assert abs(np.mean(got) - want) < 4 * np.std(got) / np.sqrt(len(got)) + 1e-9, (S, np.mean(got), want)
+
+
+@pytest.mark.parametrize("variant", ["stratified", "systematic"])
+def test_unique_keys_closed_forms_match_the_sampler(oracle_lib, variant):
+    """E|U| for the stratified sampler, sum_n 1 - prod_m (1 - w[m, n]), and
+    for the systematic one, sum_n min(1, S p_n), against the oracle's own
+    sampler averaged over Philox seeds."""
+    rng = np.random.default_rng(7)
+    P = random_problem(oracle_lib, rng, 300, 16, spread=2.0)
+    _, p = oracle_lib.scores(P, 0, 0)
+    f = analysis.expected_unique_keys_stratified if variant == "stratified" else analysis.expected_unique_keys_systematic
+    for S in (8, 64):
+        want = f(p, S)
+        got = [np.unique(oracle_lib.decode(P, variant, S, seed=s)[1][0, 0]).size for s in range(300)]
+        assert abs(np.mean(got) - want) < 4 * np.std(got) / np.sqrt(len(got)) + 0.02, (S, np.mean(got), want)
+
+
+def test_unique_keys_closed_forms_special_cases():
+    """S = 1: one key, whatever the sampler.  S p_n integers: the stratified
+    and systematic samplers draw every key of positive mass (S p_n times).
+    Uniform p over nk = S keys: every key exactly once for both, while S
+    i.i.d. draws miss a share (1 - 1/S)^S of them."""
+    rng = np.random.default_rng(8)
+    p = rng.dirichlet(np.ones(50))
+    for f in (analysis.expected_unique_keys_iid, analysis.expected_unique_keys_stratified,
+              analysis.expected_unique_keys_systematic):
+        assert abs(f(p, 1) - 1.0) < 1e-12
+    q = np.array([2, 1, 0, 5, 3, 5], np.float64) / 16.0
+    assert abs(analysis.expected_unique_keys_systematic(q, 16) - 5.0) < 1e-12
+    assert abs(analysis.expected_unique_keys_stratified(q, 16) - 5.0) < 1e-12
+    u = np.full(32, 1.0 / 32)
+    assert abs(analysis.expected_unique_keys_systematic(u, 32) - 32.0) < 1e-9
+    assert abs(analysis.expected_unique_keys_stratified(u, 32) - 32.0) < 1e-9
+    assert abs(analysis.expected_unique_keys_iid(u, 32) - 32.0 * (1.0 - (31.0 / 32.0) ** 32)) < 1e-9
 
 
 def _decode_head_8k():
