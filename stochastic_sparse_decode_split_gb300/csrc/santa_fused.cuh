@@ -72,6 +72,7 @@ constexpr int REG = 64 * 1024;      // phase-B shared-memory region
 constexpr int BAR_G0 = 1, BAR_G1 = 2, BAR_INT = 3;   // named barriers of the phase-B groups
 constexpr unsigned long long GRID_WAIT_NS = 2000000000ull;
 constexpr int STATS_CAP = 1024;     // (block, head) statistics a CTA keeps in shared memory
+constexpr int STG_ROW = 20;         // floats per head row of a warp's score staging (16 keys, padded)
 
 template <int D>
 struct FGeom {
@@ -397,13 +398,20 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
   __shared__ __align__(8) unsigned long long s_bar[FW * NS];
   __shared__ float s_rm[2][FW][8], s_rl[2][FW][8];   // per-warp running statistics of the first / last piece
   __shared__ int s_eown[2][8];                        // exponent of each published aggregate
-  __shared__ uint32_t s_keys[V == VAR_IID ? MAX_S : 1];   // i.i.d. key sort
+  // i.i.d. key sort (prologue), then each warp's score staging for the bulk
+  // stores of the stream ([8 heads][STG_ROW] floats per warp)
+  constexpr int AUX = (V == VAR_IID && MAX_S * 4 > FW * 8 * STG_ROW * 4) ? MAX_S * 4 : FW * 8 * STG_ROW * 4;
+  __shared__ __align__(16) unsigned char s_aux[AUX];
+  uint32_t* const s_keys = reinterpret_cast<uint32_t*>(s_aux);
   __shared__ Cur s_cur[2];                            // blocks lo and hi - 1 (ragged batches)
   __shared__ long long s_part[2];                     // T, q (ragged batches)
   __shared__ HeadState s_hs[3][8];                    // per phase-B group and head
   __shared__ float2 s_stats[STATS_CAP];               // the range's 16-key (max, exp-sum), when they fit
   __shared__ unsigned s_gen;
   __shared__ CtaRange s_rg;
+  __shared__ Piece s_psh[2];                          // the range's first / last piece (phase B's shared pieces)
+  __shared__ uint32_t s_ksys[2][8];                   // their heads' systematic keys
+  __shared__ unsigned long long s_rcp[2];             // their sequences' ceil(2^64 / S_b)
 
   SANTA_STAMP(0);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -414,6 +422,68 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
   const uint32_t ring_u32 = smem_addr(ring);
   if constexpr (TMA_K)
     if (tid == 0) prefetch_tensormap(&tmap);
+
+  // ---- phase A: per-warp rings.  Warp w scores blocks lo + w + FW k,
+  //      k < n_mine; the first NS are requested first, at once for uniform
+  //      batches (their partition is closed form), after the scan of the
+  //      lengths for ragged ones.
+  const uint32_t wring = ring_u32 + (uint32_t)(warp * NS * STG);
+  const uint32_t wbar = smem_addr(&s_bar[warp * NS]);
+  const unsigned long long pol = evict_first_policy();   // K is read once per step
+  if (TMA_K) {
+    if (lane == 0)
+      for (int s = 0; s < NS; ++s) mbar_init(wbar + 8 * s, 1);
+    mbar_fence_init();
+    __syncwarp();
+  }
+  int n_mine = 0;
+  Cur cur;    // block being scored
+  cur.b = a.B;
+  cur.kvh = cur.kblk = cur.nblk = 0;
+  cur.row0 = cur.nk = 0;
+  cur.pb_lo = LLONG_MAX;
+  Cur prod = cur;   // block being requested
+  const T* Kp = static_cast<const T*>(a.K);
+  auto issue = [&](int k) {
+    const int s = k % NS;
+    const uint32_t dst = wring + (uint32_t)(s * STG);
+    if (k < n_mine) {
+      const int z = (int)(prod.row0 + (int64_t)prod.kblk * BK);
+      if constexpr (TMA_K) {
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          mbar_expect_tx(wbar + 8 * s, STG);
+#pragma unroll
+          for (int x = 0; x < D / 64; ++x) tma_load_3d(dst + x * 2048, &tmap, x * 64, prod.kvh, z, wbar + 8 * s, pol);
+        }
+      } else {
+        const int rows = (int)min((int64_t)BK, prod.nk - (int64_t)prod.kblk * BK);
+        const T* src = Kp + ((int64_t)z * a.Hkv + prod.kvh) * D;
+#pragma unroll
+        for (int j = 0; j < Gm::CPB; ++j) {
+          const int q = lane + 32 * j, r = q / (D / 8), c = q % (D / 8);
+          if (r < rows) cp_async16_hint(dst + swz128_offset(r, c), src + (int64_t)r * a.Hkv * D + c * 8, pol);
+        }
+      }
+      cur_advance(prod, a, FW);
+    }
+    if constexpr (!TMA_K) cp_async_commit();
+  };
+  if (!a.kv_offsets) {
+    Part p0;
+    p0.T = a.blk_total;
+    p0.q = a.blk_q;
+    p0.r = a.blk_r;
+    p0.P = P;
+    p0.rP = a.rdiv_grid;
+    const long long l0 = p0.lo(cta), h0 = p0.lo(cta + 1);
+    n_mine = h0 - l0 > warp ? (int)((h0 - l0 - warp + FW - 1) / FW) : 0;
+    if (n_mine > 0) cur = locate_uniform(a, l0 + warp);
+    prod = cur;
+#pragma unroll 1
+    for (int k = 0; k < NS; ++k) issue(k);
+  }
+
 
   // ---- the CTA's block range: closed form for uniform batches (every thread,
   //      no wait), a scan of the lengths by one warp for ragged ones.  Kept in
@@ -507,50 +577,33 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
     p.i_last = pt.cta_of(c.pb_lo + c.nblk - 1);
     return p;
   };
+  // the pieces phase B may share with other CTAs, and their threshold
+  // constants, while the first blocks are in flight (read after the stream)
+  if (has_range && warp == FW - 1) {
+    if (lane < 2) {
+      const Cur& c = lane == 0 ? cA : cB;
+      s_psh[lane] = piece_at(c);
+      const int S_b = a.S_per_seq ? a.S_per_seq[c.b] : a.S_max;
+      s_rcp[lane] = (V != VAR_IID && S_b > 1) ? ~0ull / (unsigned)S_b + 1ull : 0ull;
+    } else if (V == VAR_SYS && lane >= 16) {
+      const int slot = (lane >> 3) & 1, g = lane & 7;
+      const Cur& c = slot == 0 ? cA : cB;
+      if (g < G)
+        s_ksys[slot][g] =
+            philox4x32_10(make_uint4(0u, (uint32_t)(c.kvh * G + g), (uint32_t)c.b, a.step), k0, k1).x >> 8;
+    }
+  }
   SANTA_STAMP(1);
 
-  // ---- phase A: per-warp rings; the first NS blocks are requested first
-  const int n_mine = has_range && hi - lo > warp ? (int)((hi - lo - warp + FW - 1) / FW) : 0;
-  const uint32_t wring = ring_u32 + (uint32_t)(warp * NS * STG);
-  const uint32_t wbar = smem_addr(&s_bar[warp * NS]);
-  const unsigned long long pol = evict_first_policy();   // K is read once per step
-  if (TMA_K) {
-    if (lane == 0)
-      for (int s = 0; s < NS; ++s) mbar_init(wbar + 8 * s, 1);
-    mbar_fence_init();
-    __syncwarp();
-  }
-  Cur cur = cA;   // block being scored
-  if (n_mine > 0) cur_advance(cur, a, warp);
-  Cur prod = cur;   // block being requested
-  const T* Kp = static_cast<const T*>(a.K);
-  auto issue = [&](int k) {
-    const int s = k % NS;
-    const uint32_t dst = wring + (uint32_t)(s * STG);
-    if (k < n_mine) {
-      const int z = (int)(prod.row0 + (int64_t)prod.kblk * BK);
-      if constexpr (TMA_K) {
-        if (lane == 0) {
-          fence_proxy_async_smem();
-          mbar_expect_tx(wbar + 8 * s, STG);
-#pragma unroll
-          for (int x = 0; x < D / 64; ++x) tma_load_3d(dst + x * 2048, &tmap, x * 64, prod.kvh, z, wbar + 8 * s, pol);
-        }
-      } else {
-        const int rows = (int)min((int64_t)BK, prod.nk - (int64_t)prod.kblk * BK);
-        const T* src = Kp + ((int64_t)z * a.Hkv + prod.kvh) * D;
-#pragma unroll
-        for (int j = 0; j < Gm::CPB; ++j) {
-          const int q = lane + 32 * j, r = q / (D / 8), c = q % (D / 8);
-          if (r < rows) cp_async16_hint(dst + swz128_offset(r, c), src + (int64_t)r * a.Hkv * D + c * 8, pol);
-        }
-      }
-      cur_advance(prod, a, FW);
-    }
-    if constexpr (!TMA_K) cp_async_commit();
-  };
+  // ragged batches: the ring starts once the partition is known
+  if (a.kv_offsets) {
+    n_mine = has_range && hi - lo > warp ? (int)((hi - lo - warp + FW - 1) / FW) : 0;
+    cur = cA;
+    if (n_mine > 0) cur_advance(cur, a, warp);
+    prod = cur;
 #pragma unroll 1
-  for (int k = 0; k < NS; ++k) issue(k);
+    for (int k = 0; k < NS; ++k) issue(k);
+  }
 
   // ---- prologue work while the first blocks are in flight
   // the barrier generation before this launch's arrivals (no CTA of this
@@ -632,6 +685,11 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
       rl[0] = rl[1] = 0.f;
     };
     const T* qp = static_cast<const T*>(a.q);
+    // scores of full blocks go out through this warp's staging rows as one
+    // 16-byte store per lane (4 keys of one head; rows start 16-byte aligned
+    // when nk_max is a multiple of 4), the rest as plain stores
+    float* const stg = reinterpret_cast<float*>(s_aux) + warp * (8 * STG_ROW);
+    const bool vec_ok = (a.nk_max & 3) == 0;
     bool ring_dead = false;
     uint32_t bq[D / 16][2];
     int bq_b = -1, bq_kvh = -1;
@@ -660,31 +718,38 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
         bq_b = cur.b;
         bq_kvh = cur.kvh;
       }
-      // A fragments of the whole block (16 keys x D) into registers; the stage is then free
-      uint32_t af[D / 16][4];
+      // 16 keys x 8 heads on the tensor cores, two independent accumulators,
+      // the A fragments (16 keys x 16 dims) read from the stage two at a time;
+      // then the stage is free for the block NS ahead
       const uint32_t sbase = wring + (uint32_t)(s * STG);
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) ldmatrix_x4(sbase + swz128_offset(lrow, ks * 2 + lhalf), af[ks]);
-      __syncwarp();
-      issue(k + NS);
-      // 16 keys x 8 heads on the tensor cores, two independent accumulators
       float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int ks = 0; ks < D / 16; ks += 2) {
-        Mma<T>::run(acc0, af[ks], bq[ks][0], bq[ks][1]);
-        Mma<T>::run(acc1, af[ks + 1], bq[ks + 1][0], bq[ks + 1][1]);
+        uint32_t f0[4], f1[4];
+        ldmatrix_x4(sbase + swz128_offset(lrow, ks * 2 + lhalf), f0);
+        ldmatrix_x4(sbase + swz128_offset(lrow, ks * 2 + 2 + lhalf), f1);
+        Mma<T>::run(acc0, f0, bq[ks][0], bq[ks][1]);
+        Mma<T>::run(acc1, f1, bq[ks + 1][0], bq[ks + 1][1]);
       }
+      __syncwarp();
+      issue(k + NS);
       // lane holds keys g8 and g8 + 8 of the block for heads 2*t4 and 2*t4 + 1
       const int64_t key0 = (int64_t)cur.kblk * BK;
       const bool ok0 = key0 + g8 < cur.nk, ok1 = key0 + g8 + 8 < cur.nk;
+      const bool vec = vec_ok && key0 + BK <= cur.nk;   // warp-uniform
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int head = 2 * t4 + hh;
         const float s0 = (acc0[hh] + acc1[hh]) * a.scale, s1 = (acc0[2 + hh] + acc1[2 + hh]) * a.scale;
         if (head < G) {
-          float* sp = a.stash + (bh0 + head) * a.nk_max + key0 + g8;
-          if (ok0) sp[0] = s0;
-          if (ok1) sp[8] = s1;
+          if (vec) {
+            stg[head * STG_ROW + g8] = s0;
+            stg[head * STG_ROW + g8 + 8] = s1;
+          } else {
+            float* sp = a.stash + (bh0 + head) * a.nk_max + key0 + g8;
+            if (ok0) sp[0] = s0;
+            if (ok1) sp[8] = s1;
+          }
         }
         float m = fmaxf(ok0 ? s0 : -INFINITY, ok1 ? s1 : -INFINITY);
 #pragma unroll
@@ -693,13 +758,23 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) l += __shfl_xor_sync(FULL, l, o);
         if (g8 == 0 && head < G) {
-          a.tile_max[(bh0 + head) * a.chunks_max + cur.kblk] = m;
-          a.tile_sum[(bh0 + head) * a.chunks_max + cur.kblk] = l;
-          if (use_ss) s_stats[(warp + FW * k) * G + head] = make_float2(m, l);
+          if (use_ss) {   // written out after the stream
+            s_stats[(warp + FW * k) * G + head] = make_float2(m, l);
+          } else {
+            a.tile_max[(bh0 + head) * a.chunks_max + cur.kblk] = m;
+            a.tile_sum[(bh0 + head) * a.chunks_max + cur.kblk] = l;
+          }
         }
         const float nm = fmaxf(rm[hh], m);
         rl[hh] = rl[hh] * fast_exp(rm[hh] - nm) + l * fast_exp(m - nm);
         rm[hh] = nm;
+      }
+      if (vec) {
+        __syncwarp();
+        if (lane < 4 * G) {
+          const float4 v = *reinterpret_cast<const float4*>(stg + (lane >> 2) * STG_ROW + (lane & 3) * 4);
+          *reinterpret_cast<float4*>(a.stash + (bh0 + (lane >> 2)) * a.nk_max + key0 + (lane & 3) * 4) = v;
+        }
       }
       cur_advance(cur, a, FW);
     }
@@ -709,9 +784,54 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
   __syncthreads();   // statistics of the range written; the ring is free
   SANTA_STAMP(3);
 
+  // phase-B regions of the ring: 0 and 1 for the shared pieces (one piece
+  // alone takes both), 2 for the pieces inside the range
+  const int n_shared = (first_shared ? 1 : 0) + (last_shared ? 1 : 0);
+  unsigned char* const regions = ring;
+  auto seg_layout = [&](unsigned char* reg, int reg_bytes, int nch_part) {
+    SegLayout L;
+    // per head and chunk: the chunk mass and the exclusive prefix, 16 bytes
+    const int cap = ((int)((float)(reg_bytes - 64) / (float)(16 * G)) - 1) & ~3;
+    L.segc = min(cap, (nch_part + 3) & ~3);
+    L.nseg = (int)(((float)nch_part + (float)(L.segc - 1)) / (float)L.segc);
+    L.w = reinterpret_cast<long long*>(reg);
+    L.pref = L.w + (size_t)G * L.segc;
+    const int used = G * L.segc * 8 + G * (L.segc + 1) * 8;
+    L.capk = BK * L.segc + 8;
+    L.st = L.nseg == 1 && used + 16 + G * L.capk * 4 <= reg_bytes
+               ? reinterpret_cast<float*>(reg + ((used + 15) & ~15))
+               : nullptr;
+    return L;
+  };
+  // Copies the range's scores of piece p (rows from the 16-byte boundary at
+  // or below their first element) into L.st: threads tg of nthr, one commit
+  // group per thread.
+  auto stage_scores = [&](const Piece& p, const SegLayout& L, int tg, int nthr) {
+    const int64_t bh0 = (int64_t)p.b * a.H + (int64_t)p.kvh * G;
+    const int64_t key0 = (int64_t)p.c_lo * BK;
+    const int nkeys = (int)(min((int64_t)p.c_hi * BK, p.nk) - key0);
+    for (int h = 0; h < G; ++h) {
+      const int64_t g0 = (bh0 + h) * a.nk_max + key0, a0 = g0 & ~(int64_t)3;
+      const int n16 = (int)((g0 + nkeys - a0 + 3) >> 2);
+      float* row = L.st + h * L.capk;
+      for (int j = tg; j < n16; j += nthr) cp_async16(smem_addr(row + 4 * j), a.stash + a0 + 4 * j);
+    }
+    cp_async_commit();
+  };
+
   // ---- aggregates of the shared pieces (16 lanes per head combine the 16
-  //      warps' running statistics), then arrival at the grid barrier
-  if (tid < 256) {
+  //      warps' running statistics), then arrival at the grid barrier; the
+  //      other 8 warps meanwhile copy the shared pieces' scores into their
+  //      regions (waited for before the grid wait)
+  if (tid >= 256) {
+    for (int slot = 0; slot < 2; ++slot) {
+      if (!(slot == 0 ? first_shared : last_shared)) continue;
+      const Piece p = s_psh[slot];
+      const SegLayout L = seg_layout(regions + (n_shared == 2 ? slot * REG : 0), n_shared == 2 ? REG : 2 * REG,
+                                     p.c_hi - p.c_lo);
+      if (L.st) stage_scores(p, L, tid - 256, FT - 256);
+    }
+  } else {
     const int slot = tid >> 7, g = (tid >> 4) & 7, w = tid & 15;
     const float m = s_rm[slot][w][g], l = s_rl[slot][w][g];
     float mm = m;
@@ -737,27 +857,30 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
   // unless two shared pieces of 8 heads use every warp)
   if (tid == FT - 32) red_release_add(arrivals, 1u);
   SANTA_STAMP(5);
+  // The range's 16-key statistics, kept in shared memory during the stream,
+  // out to the workspace (all threads; while the grid barrier is pending).
+  auto write_tile_stats = [&]() {
+    if (!use_ss || !has_range) return;
+    Cur pc = cA;
+    while (pc.b < a.B && pc.pb_lo < hi) {
+      const long long x0 = max(lo, pc.pb_lo), x1 = min(hi, pc.pb_lo + pc.nblk);
+      const int n = (int)(x1 - x0) * G, kb0 = (int)(x0 - pc.pb_lo), j0 = (int)(x0 - lo);
+      const int64_t bh0 = (int64_t)pc.b * a.H + (int64_t)pc.kvh * G;
+      for (int i = tid; i < n; i += FT) {
+        const int jb = i / G, hd = i - jb * G;
+        const float2 st = s_stats[(j0 + jb) * G + hd];
+        const int64_t o = (bh0 + hd) * a.chunks_max + kb0 + jb;
+        a.tile_max[o] = st.x;
+        a.tile_sum[o] = st.y;
+      }
+      pc.kblk = pc.nblk;
+      cur_norm(pc, a);
+    }
+  };
 
   // =====================================================================
   // phase B
   // =====================================================================
-  const int n_shared = (first_shared ? 1 : 0) + (last_shared ? 1 : 0);
-  unsigned char* const regions = ring;   // 0 and 1: the shared pieces (one group of 16 warps uses both); 2: the rest
-  auto seg_layout = [&](unsigned char* reg, int reg_bytes, int nch_part) {
-    SegLayout L;
-    // per head and chunk: the chunk mass and the exclusive prefix, 16 bytes
-    const int cap = ((int)((float)(reg_bytes - 64) / (float)(16 * G)) - 1) & ~3;
-    L.segc = min(cap, (nch_part + 3) & ~3);
-    L.nseg = (int)(((float)nch_part + (float)(L.segc - 1)) / (float)L.segc);
-    L.w = reinterpret_cast<long long*>(reg);
-    L.pref = L.w + (size_t)G * L.segc;
-    const int used = G * L.segc * 8 + G * (L.segc + 1) * 8;
-    L.capk = BK * L.segc + 8;
-    L.st = L.nseg == 1 && used + 16 + G * L.capk * 4 <= reg_bytes
-               ? reinterpret_cast<float*>(reg + ((used + 15) & ~15))
-               : nullptr;
-    return L;
-  };
   // One warp (head wl): exact exclusive prefixes of the own-unit chunk masses
   // w[0, nch) of its head from `carry` (each lane a run of consecutive chunks,
   // one 64-bit warp scan); returns the segment's end and its last chunk with
@@ -816,24 +939,14 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
     const int64_t bh0 = (int64_t)p.b * a.H + (int64_t)p.kvh * G;
     const int nch_part = p.c_hi - p.c_lo;
     const int nch0 = min(L.segc, nch_part);
-    if (L.st) {
-      // the range's scores, copied while the rest is prepared (waited for
-      // before the grid wait, or by the piece's finish); rows start at the
-      // 16-byte boundary at or below their first element
-      const int64_t key0 = (int64_t)p.c_lo * BK;
-      const int nkeys = (int)(min((int64_t)p.c_hi * BK, p.nk) - key0);
-      for (int h = 0; h < G; ++h) {
-        const int64_t g0 = (bh0 + h) * a.nk_max + key0, a0 = g0 & ~(int64_t)3;
-        const int n16 = (int)((g0 + nkeys - a0 + 3) >> 2);
-        float* row = L.st + h * L.capk;
-        for (int j = tg; j < n16; j += nthr) cp_async16(smem_addr(row + 4 * j), a.stash + a0 + 4 * j);
-      }
-      cp_async_commit();
-    }
+    // the range's scores, copied while the rest is prepared (a shared
+    // piece's were copied after the stream)
+    if (L.st && !shared) stage_scores(p, L, tg, nthr);
     SANTA_STAMP(17);
-    // threshold constants of head g by warp w0 + (G + g) % nw (lane 0)
+    // threshold constants of head g by warp w0 + (G + g) % nw (lane 0); a
+    // shared piece's were computed at the start
     for (int g = 0; g < G; ++g)
-      if (wl == (G + g) % nw && lane == 0) {
+      if (!shared && wl == (G + g) % nw && lane == 0) {
         HeadState& H = s_hs[gid][g];
         H.rcp = (V != VAR_IID && S_b > 1) ? ~0ull / (unsigned)S_b + 1ull : 0ull;
         H.ksys = V == VAR_SYS ? philox4x32_10(make_uint4(0u, (uint32_t)(p.kvh * G + g), (uint32_t)p.b, a.step), k0,
@@ -848,7 +961,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
       int e_own = AGG_EMPTY;
       const int64_t bh = bh0 + wl;
       for (int c = lane; c < p.nblk; c += 32) {
-        mstar = fmaxf(mstar, a.tile_max[bh * a.chunks_max + c]);
+        mstar = fmaxf(mstar, use_ss ? s_stats[(int)(p.pb_lo + c - lo) * G + wl].x : a.tile_max[bh * a.chunks_max + c]);
         e_own = max(e_own, chunk_agg(p, wl, c).e);
       }
       mstar = warp_max(mstar);
@@ -866,7 +979,12 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
       }
     }
     SANTA_STAMP(18);
-    if (shared && tg < G) s_hs[gid][tg].ref = (float)s_eown[slot][tg];
+    if (shared && tg < G) {
+      HeadState& H = s_hs[gid][tg];
+      H.ref = (float)s_eown[slot][tg];
+      H.rcp = s_rcp[slot];
+      if constexpr (V == VAR_SYS) H.ksys = s_ksys[slot][tg];
+    }
     if (!shared) group_sync(bar_id, nthr);   // own powers visible (a shared piece's are in s_eown)
     // the first segment's chunk masses by the whole group, then one warp per head scans them
     const float inv_nch0 = 1.0f / (float)nch0;
@@ -1041,8 +1159,19 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
               const float* sc = L.st ? L.st + wl * L.capk + (int)((bh * a.nk_max + kr0) & 3) + (int)(kc - kr0)
                                      : a.stash + bh * a.nk_max + kc;
               float s[BK];
+              if (((reinterpret_cast<uintptr_t>(sc) & 15) == 0) && kc + BK <= p.nk) {   // four 16-byte loads
 #pragma unroll
-              for (int kk = 0; kk < BK; ++kk) s[kk] = kc + kk < p.nk ? sc[kk] : -INFINITY;
+                for (int q4 = 0; q4 < BK / 4; ++q4) {
+                  const float4 v = reinterpret_cast<const float4*>(sc)[q4];
+                  s[4 * q4] = v.x;
+                  s[4 * q4 + 1] = v.y;
+                  s[4 * q4 + 2] = v.z;
+                  s[4 * q4 + 3] = v.w;
+                }
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < BK; ++kk) s[kk] = kc + kk < p.nk ? sc[kk] : -INFINITY;
+              }
               long long F = 0;
               int found = -1, lastk = 0;
 #pragma unroll
@@ -1060,7 +1189,13 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
           // ---- the distinct keys (keys are non-decreasing along the lanes)
           //      with their counts, gathered four at a time
           const int kprev = __shfl_up_sync(FULL, key, 1);
-          unsigned starts = __ballot_sync(FULL, valid && (lane == 0 || kprev != key));
+          const bool start = valid && (lane == 0 || kprev != key);
+          if (start) {   // every distinct row of this pass requested at once, into L2
+            const char* row = reinterpret_cast<const char*>(Vb - lane * CPL + (int64_t)key * a.Hkv * D);
+#pragma unroll
+            for (int o = 0; o < D * 2; o += 128) prefetch_l2(row + o);
+          }
+          unsigned starts = __ballot_sync(FULL, start);
           const int nval = __popc(__ballot_sync(FULL, valid));
           const unsigned later = starts & ~((2u << lane) - 1u);
           const float cnt = (float)((later ? __ffs(later) - 1 : nval) - lane);   // meaningful at run starts
@@ -1123,7 +1258,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
   Piece psh;
   SegLayout Lsh;
   if (n_shared > 0) {
-    psh = piece_at(sh_slot == 0 ? cA : cB);
+    psh = s_psh[sh_slot];
     Lsh = seg_layout(sh_reg, sh_bytes, psh.c_hi - psh.c_lo);
   }
   Cur pc = cA;
@@ -1160,6 +1295,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
       if (!found) {
         SANTA_STAMP(7);
         stage = 2;
+        write_tile_stats();
         if (n_shared == 0) break;
         cp_async_wait_all();   // the shared pieces' staged scores, visible after the wait's barrier
         arrivals_wait(arrivals, (unsigned)P, a.err);
