@@ -400,14 +400,44 @@ def run_ours(args):
             torch.distributed.barrier()
         return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
+    # The timed region: W plain warm-up steps, then the K steps captured once
+    # as a CUDA graph (one kernel node per step over the rotating replicas,
+    # plus the flush where one is used) and replayed between two events on
+    # the launching stream.  The replay removes the host's launch overhead,
+    # not any device work.
+    def graph_timed(fn, n, warm):
+        for i in range(warm):
+            between_steps()
+            fn(i)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n):
+                between_steps()
+                fn(i)
+        g.replay()   # graph upload, untimed
+        torch.cuda.synchronize()
+        s = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0.record(s)
+        g.replay()
+        e1.record(s)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        del g
+        return e0.elapsed_time(e1)
+
     sampler = ClockSampler(local_rank).start()
     time.sleep(0.3)
-    ms = timed_loop(lambda i: decs[i % R](step=0), args.steps, args.warmup)
+    region_ms = graph_timed(lambda i: decs[i % R](step=0), args.steps, args.warmup)
     clocks = sampler.stop()
 
-    total_ms = max_over_ranks(sum(ms), dev)
+    total_ms = max_over_ranks(region_ms, dev)
     mean_ms = total_ms / args.steps
-    med_ms = statistics.median(ms)
 
     # per-stage times (events recorded between the stages, same stream)
     n_prof = min(args.steps, 1000)
@@ -466,7 +496,7 @@ def run_ours(args):
     # dense comparator, same protocol
     denses = [santa.Decoder(t["q"], Kr, Vr, S=1, variant=wl.variant, dense=True, **kw) for (Kr, Vr) in reps]
     n_dense = min(args.steps, 1000)
-    dms = timed_loop(lambda i: denses[i % R](), n_dense, args.warmup)
+    dense_ms = graph_timed(lambda i: denses[i % R](), n_dense, args.warmup) / n_dense
 
     # end to end through the public API with host buffers, the D2H of the
     # output inside the timed region, the cache's host copy in pinned memory
@@ -527,7 +557,7 @@ def run_ours(args):
     sb = score_pass_bytes(inp)
     stb = step_bytes(inp, unique_rows)
     single = wl.dtype != "fp32"          # 16-bit caches: the whole step is one launch
-    kernel_ms = launch_ms if launch_ms is not None else mean_ms
+    kernel_ms = mean_ms   # the timed region holds only the step's launches, one after another
     achieved = stb / (kernel_ms * 1e-3) / 1e9
     step_achieved = stb / (mean_ms * 1e-3) / 1e9
     value_us = mean_ms * 1e3 / world   # whole job: time per decode step over all ranks' steps
@@ -549,14 +579,14 @@ def run_ours(args):
                    "n_q_heads": H, "n_kv_heads": wl.n_kv_heads, "head_dim": d,
                    "l2": l2_note,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "median_us": med_ms * 1e3,
+        "plain_launch_us": launch_ms * 1e3 if launch_ms is not None else None,
         "roofline": {"bound": "hbm", "kernel": "fused_decode_kernel" if single else "staged path",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": recorded_traffic(wl.name) if single else None,
                      "peak_kind": f"of {peak_kind}", "alg_bytes_per_launch": stb,
                      "us_per_launch": kernel_ms * 1e3,
-                     "timing": ("back-to-back launches over rotating replicas" if launch_ms is not None
-                                else "events around each step")},
+                     "timing": "graph replay of the K timed steps over rotating replicas, events on the "
+                               "launching stream"},
         "step": {"alg_bytes": stb, "unique_v_rows": unique_rows, "achieved_GBps": step_achieved,
                  "frac": step_achieved / peak},
         "read_probe": (dict(read_probe, frac_of_peak=read_probe["GBps"] / peak) if read_probe else None),
@@ -564,9 +594,11 @@ def run_ours(args):
                                      "sample_gather": stage_ms[2] * 1e3},
                         "score_pass_us_per_launch": score_launch_ms * 1e3 if score_launch_ms else None,
                         "score_pass_GBps": sb / (score_launch_ms * 1e-3) / 1e9 if score_launch_ms else None},
-        "dense": {"us_per_step": statistics.mean(dms) * 1e3, "alg_bytes": dense_bytes(inp),
-                  "achieved_GBps": dense_bytes(inp) / (statistics.mean(dms) * 1e-3) / 1e9,
-                  "speedup_santa_vs_dense": statistics.mean(dms) / mean_ms},
+        "dense": {"us_per_step": dense_ms * 1e3, "alg_bytes": dense_bytes(inp),
+                  "achieved_GBps": dense_bytes(inp) / (dense_ms * 1e-3) / 1e9,
+                  "frac": dense_bytes(inp) / (dense_ms * 1e-3) / 1e9 / peak,
+                  "timing": "graph replay, as the main line",
+                  "speedup_santa_vs_dense": dense_ms / mean_ms},
         "cpu_baseline": cpu_baseline,
         "e2e": e2e,
         "e2e_in_place": e2e_in_place,

@@ -20,9 +20,9 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libsanta.so")
 SOURCES = ["santa_api.cu", "santa_score.cu", "santa_sample.cu", "santa_fused.cu", "santa_fused_bf16.cu", "santa_fused_fp16.cu",
-           "santa_static.cu", "santa_tiled.cu", "santa_bernoulli.cu", "santa_probe.cu"]
-HEADERS = ["santa_common.cuh", "santa_fused.cuh", "santa_launch.h", "santa_part.cuh", "santa_seq.cuh", "santa_stream.cuh",
-           "santa_tma.cuh", "santa_window.cuh"]
+           "santa_flash.cu", "santa_static.cu", "santa_tiled.cu", "santa_bernoulli.cu", "santa_probe.cu"]
+HEADERS = ["santa_common.cuh", "santa_flash.cuh", "santa_fused.cuh", "santa_grid.cuh", "santa_launch.h", "santa_part.cuh",
+           "santa_seq.cuh", "santa_stream.cuh", "santa_tma.cuh", "santa_window.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

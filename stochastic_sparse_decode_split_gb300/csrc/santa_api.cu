@@ -28,7 +28,7 @@ constexpr size_t BAR_COUNT = 64, BAR_GEN = 128;
 size_t up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
 
 struct Layout {
-  size_t stash, tile_max, tile_sum, prefix, thresh, jstart, head_max, part_o, agg, ukeys, rcp_S, total;
+  size_t stash, tile_max, tile_sum, prefix, thresh, jstart, head_max, part_o, fpart, agg, ukeys, rcp_S, total;
   size_t tl_pre, tl_w, tl_o;
   int64_t tl_T;
   int64_t chunks, groups;
@@ -123,6 +123,7 @@ Layout dense_layout(const santa_params_t* p) {
   L.tile_max = off; off += up(B * H * (size_t)L.chunks * sizeof(float));
   L.tile_sum = off; off += up(B * H * (size_t)L.chunks * sizeof(float));
   L.part_o = off;   off += up(B * H * (size_t)L.chunks * D * sizeof(float));
+  L.fpart = off;    off += up(santa::flash_part_bytes((int)D));
   L.total = off;
   return L;
 }
@@ -389,7 +390,17 @@ santa_status_t santa_dense_decode(const santa_params_t* p, const void* q, const 
   st = check_buffers(q, K, V, out, workspace, ws_bytes, L.total);
   if (st != SANTA_OK) return st;
   santa::LaunchArgs a = base_args(p, L, q, K, V, out, workspace, (cudaStream_t)stream);
-  return santa::launch_dense(a) == cudaSuccess ? SANTA_OK : SANTA_ERR_CUDA;
+  a.fpart = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + L.fpart);
+  // 16-bit caches: one cooperative launch (santa_flash.cuh); the rest, or a
+  // shape it does not cover, the two-kernel split (santa_score.cu)
+  unsigned char* w = static_cast<unsigned char*>(workspace);
+  const cudaError_t e =
+      santa::launch_flash(a, reinterpret_cast<unsigned*>(w + BAR_COUNT), reinterpret_cast<unsigned*>(w + BAR_GEN));
+  if (e == cudaErrorNotSupported) {
+    (void)cudaGetLastError();
+    return santa::launch_dense(a) == cudaSuccess ? SANTA_OK : SANTA_ERR_CUDA;
+  }
+  return e == cudaSuccess ? SANTA_OK : SANTA_ERR_CUDA;
 }
 
 int32_t santa_workspace_layout(const santa_params_t* p, santa_ws_layout_t* layout) {

@@ -54,6 +54,7 @@
 #include "santa_common.cuh"
 #include "santa_launch.h"
 #include "santa_seq.cuh"
+#include "santa_grid.cuh"
 #include "santa_part.cuh"
 #include "santa_tma.cuh"
 #include "santa_window.cuh"
@@ -70,7 +71,6 @@ constexpr int FW = 16;              // warps per CTA
 constexpr int FT = FW * 32;         // threads per CTA
 constexpr int REG = 64 * 1024;      // phase-B shared-memory region
 constexpr int BAR_G0 = 1, BAR_G1 = 2, BAR_INT = 3;   // named barriers of the phase-B groups
-constexpr unsigned long long GRID_WAIT_NS = 2000000000ull;
 constexpr int STATS_CAP = 1024;     // (block, head) statistics a CTA keeps in shared memory
 constexpr int STG_ROW = 20;         // floats per head row of a warp's score staging (16 keys, padded)
 
@@ -235,58 +235,6 @@ __device__ __forceinline__ Agg make_agg(float m, float l) {
   return x;
 }
 
-// ---------------------------------------------------------------------------
-// Grid-wide barrier (all CTAs are resident: cooperative launch).  Two
-// arrival counters and a generation word in the workspace: a launch uses
-// counter (generation & 1), which every CTA increments once without waiting;
-// a CTA that needs the others spins until it reaches the grid size.  The
-// launch's first CTA clears the other counter for the next launch and, once
-// all have arrived, advances the generation.  Waits are bounded; on expiry
-// ERR_TIMEOUT is flagged and the CTA proceeds.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-// Waiting for every CTA's arrival: thread 0 spins until the counter reaches
-// n (bounded), then the CTA proceeds together.
-__device__ __forceinline__ void arrivals_wait(const unsigned* count, unsigned n, int* err,
-                                             unsigned long long limit_ns = GRID_WAIT_NS) {
-  if (threadIdx.x == 0) {
-    const unsigned long long t0 = global_ns();
-    while (ld_acquire(count) < n) {
-      if (global_ns() - t0 > limit_ns) {
-        flag_error(err, ERR_TIMEOUT);
-        break;
-      }
-    }
-  }
-  __syncthreads();
-}
-// Waiting half: thread 0 spins until the generation moves past g (bounded),
-// then the CTA proceeds together.
-__device__ __forceinline__ void grid_wait(const unsigned* gen, unsigned g, int* err,
-                                          unsigned long long limit_ns = GRID_WAIT_NS) {
-  if (threadIdx.x == 0) {
-    const unsigned long long t0 = global_ns();
-    while (ld_acquire(gen) == g) {
-      if (global_ns() - t0 > limit_ns) {
-        flag_error(err, ERR_TIMEOUT);
-        break;
-      }
-      __nanosleep(32);
-    }
-    __threadfence();
-  }
-  __syncthreads();
-}
 
 // The CTA's share of the partition, as phase B reads it (shared memory).
 struct CtaRange {
@@ -436,6 +384,9 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
     mbar_fence_init();
     __syncwarp();
   }
+  // the end of the K buffer: B nk_max rows, or kv_offsets[B] for a ragged
+  // batch (a box of the last sequence's last block may not reach past it)
+  const int64_t row_end = a.kv_offsets ? a.kv_offsets[a.B] : (int64_t)a.B * a.nk_max;
   int n_mine = 0;
   Cur cur;    // block being scored
   cur.b = a.B;
@@ -450,11 +401,18 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
     if (k < n_mine) {
       const int z = (int)(prod.row0 + (int64_t)prod.kblk * BK);
       if constexpr (TMA_K) {
-        if (lane == 0) {
-          fence_proxy_async_smem();
-          mbar_expect_tx(wbar + 8 * s, STG);
+        if (z + BK <= row_end) {
+          if (lane == 0) {
+            fence_proxy_async_smem();
+            mbar_expect_tx(wbar + 8 * s, STG);
 #pragma unroll
-          for (int x = 0; x < D / 64; ++x) tma_load_3d(dst + x * 2048, &tmap, x * 64, prod.kvh, z, wbar + 8 * s, pol);
+            for (int x = 0; x < D / 64; ++x)
+              tma_load_3d(dst + x * 2048, &tmap, x * 64, prod.kvh, z, wbar + 8 * s, pol);
+          }
+        } else {   // a box would reach past the end of a ragged cache buffer
+          fill_stage_plain<D>(dst, static_cast<const uint16_t*>(a.K), z, prod.kvh, a.Hkv, row_end, lane);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(wbar + 8 * s);
         }
       } else {
         const int rows = (int)min((int64_t)BK, prod.nk - (int64_t)prod.kblk * BK);

@@ -55,6 +55,7 @@ struct LaunchArgs {
   int32_t* jstart;         // [B, H, chunks_max + 1]
   float* head_max;         // [B, H]
   float* part_o;           // dense: [B, H, chunks_max, D] chunk partial outputs
+  float* fpart;            // dense, one launch: [MAX_CTAS][2] partials of shared pieces (santa_flash.cuh)
   // single-launch decode
   void* agg;               // [B, H, MAX_CTAS] per-CTA aggregates (16 bytes each, see santa_fused.cu)
   uint32_t* ukeys;         // [B, H, S_max] sorted 24-bit uniform keys (i.i.d.)
@@ -74,6 +75,10 @@ cudaError_t launch_score(const LaunchArgs& a);
 cudaError_t launch_combine(const LaunchArgs& a);
 cudaError_t launch_sample_gather(const LaunchArgs& a);
 cudaError_t launch_dense(const LaunchArgs& a);
+// Dense decode in one cooperative launch (16-bit caches, group <= 8);
+// cudaErrorNotSupported for the shapes it does not cover.
+cudaError_t launch_flash(const LaunchArgs& a, unsigned* bar_count, unsigned* bar_gen);
+size_t flash_part_bytes(int D);   // workspace bytes of its shared-piece partials
 // The whole decode step in one cooperative launch (16-bit caches, Philox uniforms).
 cudaError_t launch_fused(const LaunchArgs& a, unsigned* bar_count, unsigned* bar_gen);
 constexpr int TL_MAX_LEN = 1024;   // longest tile of the tile samplers

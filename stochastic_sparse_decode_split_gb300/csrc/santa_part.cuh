@@ -7,6 +7,8 @@
 // divisions the partition uses.
 #pragma once
 
+#include <climits>
+
 #include "santa_common.cuh"
 #include "santa_launch.h"
 
@@ -175,6 +177,59 @@ __device__ __forceinline__ Cur locate_uniform(const LaunchArgs& a, long long x) 
   c.nk = a.nk_max;
   c.pb_lo = x - c.kblk;
   return c;
+}
+
+// The range [lo, hi) of CTA `cta` of P and the cursors of blocks lo and
+// hi - 1 (b = B when the range is empty), for uniform batches in closed form,
+// for ragged ones by a scan of the lengths in warp 0.  Called by every thread
+// of the CTA (ragged batches synchronise it through s_part and s_cur).
+__device__ __forceinline__ void cta_range(const LaunchArgs& a, int P, int cta, int warp, int lane,
+                                          long long* s_part, Cur* s_cur, Part& pt, long long& lo, long long& hi,
+                                          Cur& cA, Cur& cB) {
+  pt.P = P;
+  pt.rP = a.rdiv_grid;
+  if (!a.kv_offsets) {
+    pt.T = a.blk_total;
+    pt.q = a.blk_q;
+    pt.r = a.blk_r;
+  } else {
+    if (warp == 0) {
+      const long long Tb = total_blocks(a, lane);
+      if (lane == 0) {
+        s_part[0] = Tb;
+        s_part[1] = Tb / P;
+      }
+    }
+    __syncthreads();
+    pt.T = s_part[0];
+    pt.q = s_part[1];
+    pt.r = (int)(pt.T - pt.q * P);
+  }
+  lo = pt.lo(cta);
+  hi = pt.lo(cta + 1);
+  const bool has_range = hi > lo;
+  if (!a.kv_offsets) {
+    if (has_range) {
+      cA = locate_uniform(a, lo);
+      cB = locate_uniform(a, hi - 1);
+    }
+  } else {
+    if (warp == 0 && has_range) {
+      const Cur c0 = locate_block(a, lo, lane), c1 = locate_block(a, hi - 1, lane);
+      if (lane == 0) {
+        s_cur[0] = c0;
+        s_cur[1] = c1;
+      }
+    }
+    __syncthreads();
+    cA = s_cur[0];
+    cB = s_cur[1];
+  }
+  if (!has_range) {
+    cA.b = cB.b = a.B;
+    cA.pb_lo = cB.pb_lo = LLONG_MAX;
+    cA.nblk = cB.nblk = INT_MAX;
+  }
 }
 
 }  // namespace santa

@@ -23,6 +23,27 @@ __device__ __forceinline__ void mbar_fence_init() { asm volatile("fence.mbarrier
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, unsigned bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
+// One plain arrival (the stage was filled by ordinary shared-memory stores).
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// Rows [z, z + 16) of a (row, KV head kvh, d) cache into a 16-row stage in
+// the TMA's 128-byte swizzled layout by ordinary loads and stores (one warp),
+// rows at or past `row_end` as zeros: for the blocks whose box would reach
+// past the end of a ragged cache buffer.
+template <int D>
+__device__ __forceinline__ void fill_stage_plain(uint32_t dst, const uint16_t* base, int64_t z, int kvh, int Hkv,
+                                                 int64_t row_end, int lane) {
+#pragma unroll
+  for (int j = 0; j < 16 * D / 8 / 32; ++j) {
+    const int q = lane + 32 * j, r = q / (D / 8), c = q % (D / 8);
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (z + r < row_end) v = *reinterpret_cast<const uint4*>(base + ((z + r) * Hkv + kvh) * D + c * 8);
+    const uint32_t a = (uint32_t)((c >> 3) * 2048 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst + a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+  }
+}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, unsigned parity) {
   uint32_t ok;
   asm volatile(

@@ -43,6 +43,9 @@ def check(inp, tol=TOL):
     (1, 16, 2, 64, 1, "bf16"),
     (1, 6, 2, 128, 2049, "fp32"),
     (2, 10, 2, 64, 777, "bf16"),
+    (64, 8, 2, 128, 40, "bf16"),      # many short pieces in every CTA's range
+    (3, 32, 8, 128, 16, "fp16"),      # one block per piece
+    (1, 8, 1, 128, 20000, "bf16"),    # one piece across many CTAs
 ])
 def test_dense_grid(B, H, Hkv, d, nk, dtype):
     check(synth.generate(synth.Workload("dense", B, H, Hkv, d, nk, dtype, 1, "systematic"), 3))
@@ -51,6 +54,8 @@ def test_dense_grid(B, H, Hkv, d, nk, dtype):
 def test_dense_ragged():
     wl = synth.Workload("dense_ragged", 5, 8, 2, 128, 2000, "bf16", 1, "systematic", ragged=(1, 2000))
     check(synth.generate(wl, 8))
+    wl = synth.Workload("dense_ragged_short", 33, 16, 4, 64, 300, "fp16", 1, "systematic", ragged=(1, 300))
+    check(synth.generate(wl, 9))
 
 
 def test_dense_full_size_llama32k():
