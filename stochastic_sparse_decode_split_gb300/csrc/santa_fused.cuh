@@ -354,6 +354,8 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
   __shared__ Cur s_cur[2];                            // blocks lo and hi - 1 (ragged batches)
   __shared__ long long s_part[2];                     // T, q (ragged batches)
   __shared__ HeadState s_hs[3][8];                    // per phase-B group and head
+  __shared__ long long s_wtot[2][8][FW];              // shared pieces: chunk-mass totals of each head's warps
+  __shared__ int s_wnz[2][8][FW];                     // and their last chunks with nonzero mass
   __shared__ float2 s_stats[STATS_CAP];               // the range's 16-key (max, exp-sum), when they fit
   __shared__ unsigned s_gen;
   __shared__ CtaRange s_rg;
@@ -881,6 +883,37 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
     return dd < 63 ? (x.F >> dd) : 0ll;
   };
 
+  // As scan_head, with the masses computed on the way (chunk c0 + c of head
+  // wl of piece p at the power 2^e_own) and left in w.
+  auto scan_masses = [&](const Piece& p, const SegLayout& L, int wl, int nch, int c0, int e_own, long long carry,
+                         int& lastnz) {
+    long long* w = L.w + wl * L.segc;
+    long long* pr = L.pref + wl * (L.segc + 1);
+    const int run = (nch + 31) >> 5;   // chunks per lane
+    const int ca = min(nch, lane * run), cb = min(nch, ca + run);
+    long long s = 0;
+    int nz = -1;
+    for (int c = ca; c < cb; c += 4) {   // four independent chunks at a time
+      long long m4[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) m4[u] = c + u < cb ? chunk_mass(p, wl, c0 + c + u, e_own) : 0ll;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (c + u < cb) {
+          w[c + u] = m4[u];
+          s += m4[u];
+          if (m4[u] > 0) nz = c + u;
+        }
+    }
+    long long x = carry + warp_inclusive_scan(s, lane) - s;
+    for (int c = ca; c < cb; ++c) {
+      pr[c] = x;
+      x += w[c];
+    }
+    lastnz = __reduce_max_sync(FULL, nz);
+    return __shfl_sync(FULL, x, 31);
+  };
+
   // Preparation of one piece by one group of nw warps (warps w0 .. w0 + nw -
   // 1; named barrier bar_id) in region reg, needing nothing from other CTAs:
   // per head (warp w0 + g) the own power e_own, the threshold constants
@@ -937,11 +970,66 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
       }
     }
     SANTA_STAMP(18);
-    if (shared && tg < G) {
-      HeadState& H = s_hs[gid][tg];
-      H.ref = (float)s_eown[slot][tg];
-      H.rcp = s_rcp[slot];
-      if constexpr (V == VAR_SYS) H.ksys = s_ksys[slot][tg];
+    if (shared) {
+      // the range's part of a shared piece: each head's warp alone, its chunk
+      // masses at the published power and their prefixes (no group barrier)
+      if (tg < G) {
+        HeadState& H = s_hs[gid][tg];
+        H.ref = (float)s_eown[slot][tg];
+        H.rcp = s_rcp[slot];
+        if constexpr (V == VAR_SYS) H.ksys = s_ksys[slot][tg];
+      }
+      // wph warps per head, each a contiguous share of the chunks (one
+      // 64-bit warp scan each), their totals combined through shared memory
+      const int wph = max(1, nw / G);
+      const int hw = wl / wph, kw = wl - hw * wph;
+      long long* const w = L.w + hw * L.segc;
+      long long* const pr = L.pref + hw * (L.segc + 1);
+      int la = 0, lb = 0;
+      long long excl = 0, tot = 0;
+      if (hw < G) {
+        const int cpw = (nch0 + wph - 1) / wph;
+        const int c_a = min(nch0, kw * cpw), n = min(nch0, c_a + cpw) - c_a, run = (n + 31) >> 5;
+        la = c_a + min(n, lane * run);
+        lb = c_a + min(n, lane * run + run);
+        const int e_own = s_eown[slot][hw];
+        long long sm = 0;
+        int nz = -1;
+        for (int c = la; c < lb; ++c) {
+          const long long m = chunk_mass(p, hw, p.c_lo + c, e_own);
+          w[c] = m;
+          sm += m;
+          if (m > 0) nz = c;
+        }
+        const long long incl = warp_inclusive_scan(sm, lane);
+        excl = incl - sm;
+        tot = __shfl_sync(FULL, incl, 31);
+        nz = __reduce_max_sync(FULL, nz);
+        if (lane == 0) {
+          s_wtot[gid][hw][kw] = tot;
+          s_wnz[gid][hw][kw] = nz;
+        }
+      }
+      if (wph > 1) group_sync(bar_id, nthr);
+      if (hw < G) {
+        long long base = 0;
+        int lastnz = -1;
+        for (int k = 0; k < wph; ++k) {
+          if (k < kw) base += s_wtot[gid][hw][k];
+          lastnz = max(lastnz, s_wnz[gid][hw][k]);
+        }
+        long long x = base + excl;
+        for (int c = la; c < lb; ++c) {
+          pr[c] = x;
+          x += w[c];
+        }
+        if (kw == wph - 1 && lane == 0) {
+          s_hs[gid][hw].seg_end = base + tot;
+          s_hs[gid][hw].lastnz = lastnz;
+        }
+      }
+      SANTA_STAMP(22);
+      return;
     }
     if (!shared) group_sync(bar_id, nthr);   // own powers visible (a shared piece's are in s_eown)
     // the first segment's chunk masses by the whole group, then one warp per head scans them
