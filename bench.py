@@ -39,6 +39,8 @@ KERNEL_SOURCES = ["stochastic_sparse_decode_split_gb300/csrc/santa_fused.cuh",
                   "stochastic_sparse_decode_split_gb300/csrc/santa_fused.cu",
                   "stochastic_sparse_decode_split_gb300/csrc/santa_tma.cuh",
                   "stochastic_sparse_decode_split_gb300/csrc/santa_part.cuh",
+                  "stochastic_sparse_decode_split_gb300/csrc/santa_grid.cuh",
+                  "stochastic_sparse_decode_split_gb300/csrc/santa_fused_bf16.cu",
                   "stochastic_sparse_decode_split_gb300/csrc/santa_window.cuh",
                   "stochastic_sparse_decode_split_gb300/csrc/santa_common.cuh",
                   "stochastic_sparse_decode_split_gb300/csrc/santa_seq.cuh"]
@@ -273,6 +275,16 @@ def time_oracle_full_steps(inp, variant, seconds):
     return el / steps * 1e6, steps, n_thr
 
 
+def l2_plan(kv_bytes, mode):
+    """How the timed steps keep L2 from serving the cache: R replicas of the
+    K/V cache used in turn (R = None: a flush between steps), and the note
+    the JSON line carries.  Shared by both arms, so their configs agree."""
+    if mode == "replicas" or (mode == "auto" and kv_bytes * 4 >= FLUSH_BYTES):
+        R = max(2, -(-FLUSH_BYTES // kv_bytes))
+        return R, f"inputs larger than L2: {R} replicas of the K/V cache used in turn ({R * kv_bytes >> 20} MiB)"
+    return None, "L2 flush between steps: write 512 MiB, then read 512 MiB (clean lines)"
+
+
 def run_reference(args):
     ws_, rank, _ = dist_env()
     if rank != 0:
@@ -308,10 +320,11 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wl.name, "variant": wl.variant, "S": inp.S_max, "nk": wl.nk, "batch": B,
                    "n_q_heads": H, "n_kv_heads": wl.n_kv_heads, "head_dim": inp.q.shape[2],
-                   "l2": "host memory (CPU oracle)", "parallelism": "single host thread"},
+                   "l2": l2_plan(inp.K.nbytes * 2, args.l2)[1],
+                   "parallelism": "replicas" if args.gpus > 1 else "single GPU"},
         "cpu_baseline": {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{per_step} of {len(heads)} heads per step (single thread), "
-                                   f"time scaled to all heads"},
+                         "sample": f"{per_step} of {len(heads)} heads per step (single host thread, "
+                                   f"inputs in host memory), time scaled to all heads"},
         "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -351,14 +364,12 @@ def run_ours(args):
     # flush instead: write 512 MiB, then read 512 MiB so that no dirty line of
     # the flush is written back inside the timed step.
     kv_bytes = t["K"].numel() * t["K"].element_size() * 2
-    if args.l2 == "replicas" or (args.l2 == "auto" and kv_bytes * 4 >= FLUSH_BYTES):
-        R = max(2, -(-FLUSH_BYTES // kv_bytes))
+    R, l2_note = l2_plan(kv_bytes, args.l2)
+    if R:
         reps = [(t["K"], t["V"])] + [(t["K"].clone(), t["V"].clone()) for _ in range(R - 1)]
-        l2_note = f"inputs larger than L2: {R} replicas of the K/V cache used in turn ({R * kv_bytes >> 20} MiB)"
         flush = None
     else:
         reps = [(t["K"], t["V"])]
-        l2_note = "L2 flush between steps: write 512 MiB, then read 512 MiB (clean lines)"
         flush = torch.zeros(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     R = len(reps)
     decs = [santa.Decoder(t["q"], Kr, Vr, S=S_max, variant=wl.variant, seed=0, S_per_seq=t["S_per_seq"], **kw)

@@ -255,13 +255,18 @@ santa_status_t santa_get_error(void* workspace, santa_stream_t stream, int32_t* 
  *
  * Arguments, layouts and results are those of santa_decode.  The workspace is
  * a fixed array of SANTA_STATIC_SCRATCH_BYTES bytes in the library's own
- * device memory (every GPU that loads the library holds it until the process
- * exits).  Problems whose santa_workspace_size exceeds it are rejected with
- * SANTA_ERR_SCRATCH_LIMIT before any CUDA call; invalid parameters get the
- * statuses santa_decode gives.  No allocation is made: the first call on a
- * device (the caller's current device) looks up the array's device address
- * once with cudaGetSymbolAddress, so make that first call before any stream
- * capture begins.  Each call clears the array's error word on `stream` first;
+ * device memory, held by each device from the moment the array's module is
+ * loaded there until the process exits.  Under CUDA's default lazy module
+ * loading (CUDA_MODULE_LOADING=LAZY) that happens at the first lookup of the
+ * array's address on the device: the one implicit device allocation (8 MiB)
+ * this entry point makes.  Call santa_static_warmup() once per device at
+ * startup (before the framework's pool takes the device, and before any
+ * stream capture), or run with CUDA_MODULE_LOADING=EAGER; after that no call
+ * allocates.  Problems whose santa_workspace_size exceeds the array are
+ * rejected with SANTA_ERR_SCRATCH_LIMIT, invalid parameters, variants and
+ * buffers with santa_decode's statuses, all before any CUDA call.  Every call
+ * looks up the array's address on the current device again (host-side), so
+ * nothing stale survives a device reset.  Each call clears the array's error word on `stream` first;
  * ragged metadata the device rejects leaves those heads' outputs zero (and
  * their sample_idx entries -1), as in santa_decode, but the flag itself is not
  * reported here (use santa_decode with a workspace and santa_get_error).
@@ -271,6 +276,11 @@ santa_status_t santa_get_error(void* workspace, santa_stream_t stream, int32_t* 
 #define SANTA_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
 santa_status_t santa_decode_static(const santa_params_t* p, int32_t variant, const void* q, const void* K,
                                    const void* V, float* out, santa_stream_t stream, int32_t* sample_idx);
+/* Loads santa_decode_static's array on the current device (the lookup of its
+ * address: under lazy module loading, an 8 MiB device allocation the first
+ * time on each device) and returns SANTA_OK, or SANTA_ERR_CUDA when the
+ * device cannot hold it.  Launches nothing; safe to call again. */
+santa_status_t santa_static_warmup(void);
 
 /* Measurement helper, not part of the method: reads `bytes` bytes at `src`
  * (device, 16-byte aligned, a multiple of 16) once with 16-byte

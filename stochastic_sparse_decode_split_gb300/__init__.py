@@ -29,7 +29,7 @@ __all__ = [
     "SantaError", "Params", "library", "santa_decode", "santa_decode_host_kv", "santa_decode_with_uniforms",
     "santa_dense_decode",
     "workspace_size", "dense_workspace_size", "workspace_layout", "get_error", "Decoder", "exported_symbols",
-    "VARIANTS", "DTYPES", "santa_decode_static", "static_scratch_bytes", "SAMPLERS", "santa_decode_tiled",
+    "VARIANTS", "DTYPES", "santa_decode_static", "static_warmup", "static_scratch_bytes", "SAMPLERS", "santa_decode_tiled",
     "tiled_workspace_size", "tiled_max_draws", "santa_decode_bernoulli", "bernoulli_workspace_size",
 ]
 
@@ -99,6 +99,7 @@ def library():
             lib.santa_decode_with_uniforms.argtypes = [P, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp]
             lib.santa_dense_decode.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
             lib.santa_decode_static.argtypes = [P, i32, vp, vp, vp, vp, vp, vp]
+            lib.santa_static_warmup.argtypes = []
             lib.santa_workspace_layout.argtypes = [P, ctypes.POINTER(WsLayout)]
             lib.santa_tiled_workspace_size.argtypes = [P, i32, i32]
             lib.santa_tiled_workspace_size.restype = sz
@@ -328,6 +329,14 @@ def static_scratch_bytes() -> int:
     santa_decode_static can serve."""
     m = re.search(r"#define SANTA_STATIC_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)", open(HEADER).read())
     return int(m.group(1)) << int(m.group(2))
+
+
+def static_warmup() -> None:
+    """Loads santa_decode_static's fixed array on the current device (under
+    lazy module loading its one allocation); call at startup."""
+    st = library().santa_static_warmup()
+    if st != SANTA_OK:
+        raise SantaError(st, "santa_static_warmup")
 
 
 def santa_decode_static(q, K, V, S: int, variant: str = "systematic", seed: int = 0, step: int = 0, out=None,

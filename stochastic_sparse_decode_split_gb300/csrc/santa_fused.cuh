@@ -71,6 +71,7 @@ constexpr int FW = 16;              // warps per CTA
 constexpr int FT = FW * 32;         // threads per CTA
 constexpr int REG = 64 * 1024;      // phase-B shared-memory region
 constexpr int BAR_G0 = 1, BAR_G1 = 2, BAR_INT = 3;   // named barriers of the phase-B groups
+constexpr int BAR_FIN = 4;                             // the shared pieces' head warps after the grid wait
 constexpr int STATS_CAP = 1024;     // (block, head) statistics a CTA keeps in shared memory
 constexpr int STG_ROW = 20;         // floats per head row of a warp's score staging (16 keys, padded)
 
@@ -1343,8 +1344,22 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
         stage = 2;
         write_tile_stats();
         if (n_shared == 0) break;
-        cp_async_wait_all();   // the shared pieces' staged scores, visible after the wait's barrier
-        arrivals_wait(arrivals, (unsigned)P, a.err);
+        cp_async_wait_all();   // the shared pieces' staged scores and prefixes, visible to all
+        __syncthreads();
+        // only the shared pieces' head warps go on (warps w0 .. w0 + G - 1 of
+        // each group; warp 0 among them, whose thread 0 waits for the grid)
+        const int nhead = n_shared * G;
+        if (warp - sh_w0 >= G) break;
+        if (tid == 0) {
+          const unsigned long long t0 = global_ns();
+          while (ld_acquire(arrivals) < (unsigned)P) {
+            if (global_ns() - t0 > GRID_WAIT_NS) {
+              flag_error(a.err, ERR_TIMEOUT);
+              break;
+            }
+          }
+        }
+        group_sync(BAR_FIN, nhead * 32);
         SANTA_STAMP(8);
         continue;
       }

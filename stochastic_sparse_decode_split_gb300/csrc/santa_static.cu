@@ -10,7 +10,7 @@
 // overlap on the GPU race on it.
 #include <cuda_runtime.h>
 
-#include <mutex>
+#include <cstdint>
 
 #include "../../include/santa.h"
 
@@ -20,26 +20,27 @@ static __device__ __align__(256) unsigned char santa_static_scratch[SANTA_STATIC
 
 namespace {
 
-constexpr int MAX_DEVICES = 64;
-std::mutex setup_mutex;
-void* scratch_on_device[MAX_DEVICES] = {};
-
-// Device address of the scratch on the current device, looked up on the first
-// call for that device (with that device current) and kept.
+// Device address of the scratch on the current device.  Looked up on every
+// call (a host-side table lookup once the array's module is loaded), so that
+// an address never outlives a device reset or a re-created primary context.
 santa_status_t scratch_address(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return SANTA_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(setup_mutex);
-  if (!scratch_on_device[dev]) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, santa_static_scratch) != cudaSuccess || !ptr) return SANTA_ERR_CUDA;
-    scratch_on_device[dev] = ptr;
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, santa_static_scratch) != cudaSuccess || !ptr) {
+    (void)cudaGetLastError();
+    return SANTA_ERR_CUDA;
   }
-  *out = scratch_on_device[dev];
+  *out = ptr;
   return SANTA_OK;
 }
 
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
 }  // namespace
+
+extern "C" santa_status_t santa_static_warmup(void) {
+  void* ws = nullptr;
+  return scratch_address(&ws);
+}
 
 extern "C" santa_status_t santa_decode_static(const santa_params_t* p, int32_t variant, const void* q,
                                               const void* K, const void* V, float* out, santa_stream_t stream,
@@ -48,6 +49,11 @@ extern "C" santa_status_t santa_decode_static(const santa_params_t* p, int32_t v
   if (need == 0)   // invalid or unsupported parameters: santa_decode reports which, before any CUDA call
     return santa_decode(p, variant, q, K, V, out, nullptr, 0, stream, sample_idx);
   if (need > SANTA_STATIC_SCRATCH_BYTES) return SANTA_ERR_SCRATCH_LIMIT;
+  // the rest of santa_decode's argument checks, before any CUDA call
+  if (variant < SANTA_IID || variant > SANTA_SYSTEMATIC) return SANTA_ERR_INVALID_ARG;
+  if (!q || !K || !V || !out) return SANTA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(out, 16)) return SANTA_ERR_INVALID_ARG;
+  if (sample_idx && !aligned(sample_idx, 4)) return SANTA_ERR_INVALID_ARG;
   void* ws = nullptr;
   const santa_status_t st = scratch_address(&ws);
   if (st != SANTA_OK) return st;

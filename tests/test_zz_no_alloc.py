@@ -46,6 +46,12 @@ def test_refuses_problems_beyond_the_array():
     # invalid parameters keep santa_decode's statuses
     assert lib.santa_decode_static(ctypes.byref(_params(n_kv_heads=3)), 2, vp(256), vp(256), vp(256), vp(256),
                                    None, None) == 1
+    # so do a bad variant, null or misaligned buffers: refused before any CUDA
+    # call (no GPU in this test)
+    assert lib.santa_decode_static(ctypes.byref(fits), 7, vp(256), vp(256), vp(256), vp(256), None, None) == 1
+    assert lib.santa_decode_static(ctypes.byref(fits), 2, None, vp(256), vp(256), vp(256), None, None) == 1
+    assert lib.santa_decode_static(ctypes.byref(fits), 2, vp(256), vp(264), vp(256), vp(256), None, None) == 1
+    assert lib.santa_decode_static(ctypes.byref(fits), 2, vp(256), vp(256), vp(256), vp(256), None, vp(258)) == 1
 
 
 def _case(name, B, H, Hkv, d, nk, dtype, S, variant, data_seed):
@@ -57,9 +63,12 @@ def _case(name, B, H, Hkv, d, nk, dtype, S, variant, data_seed):
 def test_two_calls_match_santa_decode():
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
+    santa.static_warmup()
     cases = [  # a second call with another shape, dtype and variant: the array keeps the first call's contents
         (_case("static_a", 2, 8, 2, 128, 3000, "bf16", 64, "systematic", 11), "systematic", 5),
         (_case("static_b", 1, 16, 4, 64, 1500, "fp16", 128, "stratified", 12), "stratified", 6),
+        # the motivating size: one Llama-3.1-8B layer at 32K keys, 256 systematic draws
+        (_case("static_llama32k", 1, 32, 8, 128, 32768, "bf16", 256, "systematic", 13), "systematic", 7),
     ]
     for (inp, t), variant, seed in cases:
         B, H, d = inp.q.shape
@@ -73,3 +82,25 @@ def test_two_calls_match_santa_decode():
         torch.cuda.synchronize()
         assert np.array_equal(idx_s.cpu().numpy(), idx_r.cpu().numpy())
         np.testing.assert_allclose(out_s.cpu().numpy(), out_r.cpu().numpy(), rtol=1e-5, atol=1e-6)
+
+
+@pytest.mark.gpu
+def test_calls_after_warmup_allocate_nothing():
+    """After santa_static_warmup, a call changes neither the device's free
+    memory (cudaMemGetInfo) nor the torch pool."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    santa.static_warmup()
+    inp, t = _case("static_alloc", 1, 32, 8, 128, 32768, "bf16", 256, "systematic", 14)
+    B, H, d = inp.q.shape
+    out = torch.empty((B, H, d), dtype=torch.float32, device="cuda")
+    santa.santa_decode_static(t["q"], t["K"], t["V"], S=256, out=out)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    pool0 = torch.cuda.memory_reserved()
+    for seed in range(3):
+        santa.santa_decode_static(t["q"], t["K"], t["V"], S=256, seed=seed, out=out)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert torch.cuda.memory_reserved() == pool0
+    assert abs(free1 - free0) < (1 << 20), (free0, free1)
