@@ -324,7 +324,18 @@ santa_status_t santa_decode_tiled(const santa_params_t* p, int32_t sampler, int3
   a.tl_pre = reinterpret_cast<int32_t*>(w + L.tl_pre);
   a.tl_w = reinterpret_cast<double*>(w + L.tl_w);
   a.tl_o = reinterpret_cast<float*>(w + L.tl_o);
-  if (santa::launch_score(a) != cudaSuccess) return SANTA_ERR_CUDA;   // out is not touched here
+  // the score pass (out is not touched here): for 16-bit caches the single
+  // launch's stream alone, else the staged score kernel
+  if (p->dtype != SANTA_FP32) {
+    a.score_only = 1;
+    a.variant = SANTA_SYSTEMATIC;
+    if (santa::launch_fused(a, reinterpret_cast<unsigned*>(w + BAR_COUNT), reinterpret_cast<unsigned*>(w + BAR_GEN)) !=
+        cudaSuccess)
+      return SANTA_ERR_CUDA;
+    a.score_only = 0;
+  } else if (santa::launch_score(a) != cudaSuccess) {
+    return SANTA_ERR_CUDA;
+  }
   a.out = out;
   return santa::launch_tiled(a) == cudaSuccess ? SANTA_OK : SANTA_ERR_CUDA;
 }

@@ -587,9 +587,11 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
     const int e = seq_error(a, b, S_b);
     if (e) {
       if (tid == 0) flag_error(a.err, e);
-      float4* o = reinterpret_cast<float4*>(a.out + (int64_t)b * a.H * D);
-      for (int i = tid; i < a.H * D / 4; i += FT) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (a.sample_idx)
+      if (a.out) {
+        float4* o = reinterpret_cast<float4*>(a.out + (int64_t)b * a.H * D);
+        for (int i = tid; i < a.H * D / 4; i += FT) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      if (a.sample_idx && !a.score_only)
         for (int i = tid; i < a.H * a.S_max; i += FT) a.sample_idx[(int64_t)b * a.H * a.S_max + i] = -1;
     }
   }
@@ -604,7 +606,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
       if (needed) {
         const Piece p = piece_at(pc);
         const int64_t bh0 = (int64_t)p.b * a.H + (int64_t)p.kvh * G;
-        if (p.pb_lo >= lo) {
+        if (p.pb_lo >= lo && !a.score_only) {
           if (p.i_first != p.i_last) {
             float4* o = reinterpret_cast<float4*>(a.out + bh0 * D);
             for (int i = tid; i < G * D / 4; i += FT) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -614,7 +616,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
               a.sample_idx[(bh0 + i / (a.S_max - S_b)) * a.S_max + S_b + i % (a.S_max - S_b)] = -1;
         }
         if constexpr (V == VAR_IID)
-          for (int g = 0; g < G; ++g) {
+          for (int g = 0; g < G && !a.score_only; ++g) {
             int sorter = p.i_first + g;
             if (sorter > p.i_last || !pt.nonempty(sorter)) sorter = p.i_first;
             if (sorter == cta)
@@ -745,6 +747,31 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
   __syncthreads();   // statistics of the range written; the ring is free
   SANTA_STAMP(3);
 
+  // The range's 16-key statistics, kept in shared memory during the stream,
+  // out to the workspace (all threads; while the grid barrier is pending).
+  auto write_tile_stats = [&]() {
+    if (!use_ss || !has_range) return;
+    Cur pc = cA;
+    while (pc.b < a.B && pc.pb_lo < hi) {
+      const long long x0 = max(lo, pc.pb_lo), x1 = min(hi, pc.pb_lo + pc.nblk);
+      const int n = (int)(x1 - x0) * G, kb0 = (int)(x0 - pc.pb_lo), j0 = (int)(x0 - lo);
+      const int64_t bh0 = (int64_t)pc.b * a.H + (int64_t)pc.kvh * G;
+      for (int i = tid; i < n; i += FT) {
+        const int jb = i / G, hd = i - jb * G;
+        const float2 st = s_stats[(j0 + jb) * G + hd];
+        const int64_t o = (bh0 + hd) * a.chunks_max + kb0 + jb;
+        a.tile_max[o] = st.x;
+        a.tile_sum[o] = st.y;
+      }
+      pc.kblk = pc.nblk;
+      cur_norm(pc, a);
+    }
+  };
+  if (a.score_only) {   // the score pass alone: the statistics out, no draws
+    write_tile_stats();
+    return;
+  }
+
   // phase-B regions of the ring: 0 and 1 for the shared pieces (one piece
   // alone takes both), 2 for the pieces inside the range
   const int n_shared = (first_shared ? 1 : 0) + (last_shared ? 1 : 0);
@@ -818,26 +845,6 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
   // unless two shared pieces of 8 heads use every warp)
   if (tid == FT - 32) red_release_add(arrivals, 1u);
   SANTA_STAMP(5);
-  // The range's 16-key statistics, kept in shared memory during the stream,
-  // out to the workspace (all threads; while the grid barrier is pending).
-  auto write_tile_stats = [&]() {
-    if (!use_ss || !has_range) return;
-    Cur pc = cA;
-    while (pc.b < a.B && pc.pb_lo < hi) {
-      const long long x0 = max(lo, pc.pb_lo), x1 = min(hi, pc.pb_lo + pc.nblk);
-      const int n = (int)(x1 - x0) * G, kb0 = (int)(x0 - pc.pb_lo), j0 = (int)(x0 - lo);
-      const int64_t bh0 = (int64_t)pc.b * a.H + (int64_t)pc.kvh * G;
-      for (int i = tid; i < n; i += FT) {
-        const int jb = i / G, hd = i - jb * G;
-        const float2 st = s_stats[(j0 + jb) * G + hd];
-        const int64_t o = (bh0 + hd) * a.chunks_max + kb0 + jb;
-        a.tile_max[o] = st.x;
-        a.tile_sum[o] = st.y;
-      }
-      pc.kblk = pc.nblk;
-      cur_norm(pc, a);
-    }
-  };
 
   // =====================================================================
   // phase B

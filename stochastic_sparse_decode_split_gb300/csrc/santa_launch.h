@@ -23,6 +23,7 @@ struct LaunchArgs {
   int tiles_max;   // ceil(nk_max / TILE) score-pass tiles per (b, kv head)
   int num_sms;     // streaming multiprocessors of the device (persistent grid size)
   int k_host;      // K is page-locked host memory read in place (no TMA on it)
+  int score_only;  // single launch: the score pass alone (stash and 16-key statistics), then exit
   // single-launch partition of uniform batches, computed by the launcher
   // (blk_total = 0: ragged, the kernel computes it): total 16-key blocks and
   // blk_total = blk_q * grid + blk_r

@@ -32,6 +32,7 @@ namespace santa {
 
 constexpr int TB_THREADS = 256;   // budget and merge kernels
 constexpr int TB_SMEM_T = 4096;   // tiles whose fractional parts the budget kernel keeps in shared memory
+constexpr int TB_RANK_T = 256;    // up to this many tiles the leftover samples are placed by ranking
 constexpr int TS_THREADS = 256;   // sampler kernel
 constexpr int TS_WARPS = TS_THREADS / 32;
 
@@ -151,8 +152,39 @@ __global__ void __launch_bounds__(TB_THREADS) tiled_budget_kernel(LaunchArgs a) 
       if (above < R) pre[t] += 1;
     }
   };
-  if (T <= TB_SMEM_T) rank_pass(fr_s);
-  else rank_pass(frg);
+  if (T <= TB_RANK_T) {
+    rank_pass(fr_s);
+  } else if (T <= TB_SMEM_T) {
+    // more tiles: sort instead of ranking.  Each key keeps the fractional
+    // part's bits above the lowest 12 of its mantissa and takes 4095 - t in
+    // those 12 (a fraction equal to another's to 2^-40 goes to the lower
+    // tile, as exact equality does); a bitonic network sorts the keys in
+    // decreasing order (zeros pad to a power of two) and the first R tiles
+    // get one more sample
+    int T2 = 1;
+    while (T2 < T) T2 <<= 1;
+    for (int t = tid; t < T2; t += TB_THREADS)
+      fr_s[t] = t < T ? ((fr_s[t] & ~0xFFFull) | (unsigned long long)(4095 - t)) : 0ull;
+    __syncthreads();
+    for (int k = 2; k <= T2; k <<= 1)
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int i = tid; i < T2; i += TB_THREADS) {
+          const int l = i ^ j;
+          if (l > i) {
+            const unsigned long long x = fr_s[i], y = fr_s[l];
+            const bool desc = (i & k) == 0;   // this run sorts in decreasing order
+            if (desc ? x < y : x > y) {
+              fr_s[i] = y;
+              fr_s[l] = x;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    for (int r = tid; r < R; r += TB_THREADS) pre[4095 - (int)(fr_s[r] & 0xFFFull)] += 1;
+  } else {
+    rank_pass(frg);
+  }
   __syncthreads();
   // exclusive prefix in place, TB_THREADS tiles at a time
   int run = 0;

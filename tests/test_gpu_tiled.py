@@ -145,6 +145,7 @@ def test_tiny(sampler, tile_len):
     ("fp32_g8", 1, 16, 2, 128, 777, "fp32", 40, 128),
     ("bf16_tile1024", 1, 8, 8, 128, 5000, "bf16", 300, 1024),
     ("few_samples", 1, 4, 1, 64, 4000, "bf16", 8, 32),   # prop: most tiles get no sample
+    ("many_tiles", 1, 4, 1, 64, 8192, "bf16", 300, 16),  # 512 tiles: prop sorts the fractional parts
 ])
 def test_parity(sampler, case):
     name, B, H, Hkv, d, nk, dtype, S, L = case
