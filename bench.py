@@ -35,6 +35,7 @@ METRIC = "S²ANTA decode-attn µs/step and achieved HBM GB/s vs peak, 32K ctx bf
 UNIT = "us/step"
 FALLBACK_HBM_GBS = 6800.0
 FLUSH_BYTES = 512 * 1024 * 1024
+MAX_REPLICAS = 64   # more copies than this: an L2 flush between steps instead
 KERNEL_SOURCES = ["stochastic_sparse_decode_split_gb300/csrc/santa_fused.cuh",
                   "stochastic_sparse_decode_split_gb300/csrc/santa_fused.cu",
                   "stochastic_sparse_decode_split_gb300/csrc/santa_tma.cuh",
@@ -279,10 +280,10 @@ def l2_plan(kv_bytes, mode):
     """How the timed steps keep L2 from serving the cache: R replicas of the
     K/V cache used in turn (R = None: a flush between steps), and the note
     the JSON line carries.  Shared by both arms, so their configs agree."""
-    if mode == "replicas" or (mode == "auto" and kv_bytes * 4 >= FLUSH_BYTES):
-        R = max(2, -(-FLUSH_BYTES // kv_bytes))
+    R = max(2, -(-FLUSH_BYTES // kv_bytes))
+    if mode == "replicas" or (mode == "auto" and R <= MAX_REPLICAS):
         return R, f"inputs larger than L2: {R} replicas of the K/V cache used in turn ({R * kv_bytes >> 20} MiB)"
-    return None, "L2 flush between steps: write 512 MiB, then read 512 MiB (clean lines)"
+    return None, "L2 flush between steps: write 512 MiB, then read 512 MiB (clean lines), outside each step's events"
 
 
 def graph_replay_ms(fn, n, warm, world):
@@ -440,11 +441,11 @@ def run_ours(args):
             torch.distributed.barrier()
         return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
-    # The timed region: W plain warm-up steps, then the K steps captured once
-    # as a CUDA graph (one kernel node per step over the rotating replicas,
-    # plus the flush where one is used) and replayed between two events on
-    # the launching stream.  The replay removes the host's launch overhead,
-    # not any device work.
+    # The timed region with replicas: W plain warm-up steps, then the K steps
+    # captured once as a CUDA graph (one kernel node per step over the
+    # rotating replicas) and replayed between two events on the launching
+    # stream.  The replay removes the host's launch overhead, not any device
+    # work.
     def graph_timed(fn, n, warm):
         for i in range(warm):
             between_steps()
@@ -471,9 +472,16 @@ def run_ours(args):
         del g
         return e0.elapsed_time(e1)
 
+    def timed_region(fn, n, warm):
+        """Replicas: graph replay of the n steps.  Flush: the flush stays
+        outside the timing, so each step is timed by its own events."""
+        if flush is None:
+            return graph_timed(fn, n, warm)
+        return sum(timed_loop(fn, n, warm))
+
     sampler = ClockSampler(local_rank).start()
     time.sleep(0.3)
-    region_ms = graph_timed(lambda i: decs[i % R](step=0), args.steps, args.warmup)
+    region_ms = timed_region(lambda i: decs[i % R](step=0), args.steps, args.warmup)
     clocks = sampler.stop()
 
     total_ms = max_over_ranks(region_ms, dev)
@@ -543,7 +551,7 @@ def run_ours(args):
     # dense comparator, same protocol
     denses = [santa.Decoder(t["q"], Kr, Vr, S=1, variant=wl.variant, dense=True, **kw) for (Kr, Vr) in reps]
     n_dense = min(args.steps, 1000)
-    dense_ms = graph_timed(lambda i: denses[i % R](), n_dense, args.warmup) / n_dense
+    dense_ms = timed_region(lambda i: denses[i % R](), n_dense, args.warmup) / n_dense
 
     # end to end through the public API with host buffers, the D2H of the
     # output inside the timed region, the cache's host copy in pinned memory
@@ -645,8 +653,9 @@ def run_ours(args):
                      "traffic": recorded_traffic(wl.name) if single else None,
                      "peak_kind": f"of {peak_kind}", "alg_bytes_per_launch": stb,
                      "us_per_launch": kernel_ms * 1e3,
-                     "timing": "graph replay of the K timed steps over rotating replicas, events on the "
-                               "launching stream"},
+                     "timing": ("graph replay of the K timed steps over rotating replicas, events on the "
+                                "launching stream" if flush is None else
+                                "events around each step on the launching stream (L2 flush between steps)")},
         "step": {"alg_bytes": stb, "unique_v_rows": unique_rows, "achieved_GBps": step_achieved,
                  "frac": step_achieved / peak},
         "read_probe": (dict(read_probe, frac_of_peak=read_probe["GBps"] / peak) if read_probe else None),
