@@ -260,26 +260,20 @@ struct Piece {
 // E* - e_own, exactly.
 struct HeadState {
   long long Z, pown, town;  // head units: total mass, prefix and mass of this range
-  long long carry, seg_end; // own units: prefix at the start / end of the current segment
   unsigned long long rcp;   // ceil(2^64 / S_b) (S_b > 1), for the thresholds
   uint32_t ksys;            // systematic: the head's uniform key
   float ref;                // e_own: masses are 2^(s log2(e) - e_own)
   float mstar;              // max score (the piece, when it is this CTA's alone)
   int d;                    // E* - e_own
-  int jcur, jend;           // next threshold of the range; end of the range's thresholds
-  int jseg_lo, jseg_hi;     // thresholds of the current segment
-  int lastnz;               // last chunk of the segment with nonzero mass (-1: none)
 };
 
-// Shared-memory layout of a piece inside a phase-B region: one segment's
-// exact own-unit chunk masses and prefixes per head (a segment: as many
-// chunks as fit; one segment holds the CTA's whole range at a 32K context)
-// and, when they fit too, the range's scores.
+// Shared-memory layout of a piece inside a phase-B region: per head, the
+// own-unit masses of the range's chunks when they fit, then the range's
+// scores when they fit too.
 struct SegLayout {
-  long long* w;             // [G][segc] own-unit chunk masses
-  long long* pref;          // [G][segc + 1] exclusive own-unit chunk prefixes from the segment's carry
+  long long* w;             // [G][segc] own-unit chunk masses, or NULL (computed when needed)
   float* st;                // [G][capk] the range's scores (staged from the 16-byte boundary below), or NULL
-  int segc, nseg, capk;
+  int segc, capk;
 };
 
 // ---------------------------------------------------------------------------
@@ -355,8 +349,6 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
   __shared__ Cur s_cur[2];                            // blocks lo and hi - 1 (ragged batches)
   __shared__ long long s_part[2];                     // T, q (ragged batches)
   __shared__ HeadState s_hs[3][8];                    // per phase-B group and head
-  __shared__ long long s_wtot[2][8][FW];              // shared pieces: chunk-mass totals of each head's warps
-  __shared__ int s_wnz[2][8][FW];                     // and their last chunks with nonzero mass
   __shared__ float2 s_stats[STATS_CAP];               // the range's 16-key (max, exp-sum), when they fit
   __shared__ unsigned s_gen;
   __shared__ CtaRange s_rg;
@@ -778,17 +770,16 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
   unsigned char* const regions = ring;
   auto seg_layout = [&](unsigned char* reg, int reg_bytes, int nch_part) {
     SegLayout L;
-    // per head and chunk: the chunk mass and the exclusive prefix, 16 bytes
-    const int cap = ((int)((float)(reg_bytes - 64) / (float)(16 * G)) - 1) & ~3;
-    L.segc = min(cap, (nch_part + 3) & ~3);
-    L.nseg = (int)(((float)nch_part + (float)(L.segc - 1)) / (float)L.segc);
+    // per head: the range's chunk masses in own units (8 bytes each) when
+    // they fit, then its scores when they fit too
+    L.segc = (nch_part + 3) & ~3;
     L.w = reinterpret_cast<long long*>(reg);
-    L.pref = L.w + (size_t)G * L.segc;
-    const int used = G * L.segc * 8 + G * (L.segc + 1) * 8;
-    L.capk = BK * L.segc + 8;
-    L.st = L.nseg == 1 && used + 16 + G * L.capk * 4 <= reg_bytes
-               ? reinterpret_cast<float*>(reg + ((used + 15) & ~15))
-               : nullptr;
+    const int used = G * L.segc * 8;
+    const bool w_fit = used + 64 <= reg_bytes;
+    if (!w_fit) L.w = nullptr;
+    L.capk = BK * nch_part + 8;
+    const int off = w_fit ? ((used + 15) & ~15) : 0;
+    L.st = off + 16 + G * L.capk * 4 <= reg_bytes ? reinterpret_cast<float*>(reg + off) : nullptr;
     return L;
   };
   // Copies the range's scores of piece p (rows from the 16-byte boundary at
@@ -849,29 +840,6 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
   // =====================================================================
   // phase B
   // =====================================================================
-  // One warp (head wl): exact exclusive prefixes of the own-unit chunk masses
-  // w[0, nch) of its head from `carry` (each lane a run of consecutive chunks,
-  // one 64-bit warp scan); returns the segment's end and its last chunk with
-  // nonzero mass.
-  auto scan_head = [&](const SegLayout& L, int wl, int nch, long long carry, int& lastnz) {
-    const long long* w = L.w + wl * L.segc;
-    long long* pr = L.pref + wl * (L.segc + 1);
-    const int run = (nch + 31) >> 5;   // chunks per lane
-    const int ca = min(nch, lane * run), cb = min(nch, ca + run);
-    long long s = 0;
-    int nz = -1;
-    for (int c = ca; c < cb; ++c) {
-      s += w[c];
-      if (w[c] > 0) nz = c;
-    }
-    long long x = carry + warp_inclusive_scan(s, lane) - s;
-    for (int c = ca; c < cb; ++c) {
-      pr[c] = x;
-      x += w[c];
-    }
-    lastnz = __reduce_max_sync(FULL, nz);
-    return __shfl_sync(FULL, x, 31);
-  };
   // Chunk c of head g of piece p (a chunk of this range) as an aggregate:
   // exponent e_c and mass relative to 2^e_c, from its 16-key statistics
   // (kept in shared memory during the stream when the range's chunks fit)
@@ -891,37 +859,6 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
     return dd < 63 ? (x.F >> dd) : 0ll;
   };
 
-  // As scan_head, with the masses computed on the way (chunk c0 + c of head
-  // wl of piece p at the power 2^e_own) and left in w.
-  auto scan_masses = [&](const Piece& p, const SegLayout& L, int wl, int nch, int c0, int e_own, long long carry,
-                         int& lastnz) {
-    long long* w = L.w + wl * L.segc;
-    long long* pr = L.pref + wl * (L.segc + 1);
-    const int run = (nch + 31) >> 5;   // chunks per lane
-    const int ca = min(nch, lane * run), cb = min(nch, ca + run);
-    long long s = 0;
-    int nz = -1;
-    for (int c = ca; c < cb; c += 4) {   // four independent chunks at a time
-      long long m4[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) m4[u] = c + u < cb ? chunk_mass(p, wl, c0 + c + u, e_own) : 0ll;
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (c + u < cb) {
-          w[c + u] = m4[u];
-          s += m4[u];
-          if (m4[u] > 0) nz = c + u;
-        }
-    }
-    long long x = carry + warp_inclusive_scan(s, lane) - s;
-    for (int c = ca; c < cb; ++c) {
-      pr[c] = x;
-      x += w[c];
-    }
-    lastnz = __reduce_max_sync(FULL, nz);
-    return __shfl_sync(FULL, x, 31);
-  };
-
   // Preparation of one piece by one group of nw warps (warps w0 .. w0 + nw -
   // 1; named barrier bar_id) in region reg, needing nothing from other CTAs:
   // per head (warp w0 + g) the own power e_own, the threshold constants
@@ -936,26 +873,40 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
     if (seq_error(a, p.b, S_b)) return;
     SANTA_STAMP(16);
     const int64_t bh0 = (int64_t)p.b * a.H + (int64_t)p.kvh * G;
-    const int nch_part = p.c_hi - p.c_lo;
-    const int nch0 = min(L.segc, nch_part);
-    // the range's scores, copied while the rest is prepared (a shared
-    // piece's were copied after the stream)
-    if (L.st && !shared) stage_scores(p, L, tg, nthr);
+    const int nch = p.c_hi - p.c_lo;
+    if (shared) {
+      // the range's part of a shared piece: its heads' constants, and its
+      // chunk masses at the published powers by the whole group (their
+      // prefixes are formed while the draws are resolved)
+      if (tg < G) {
+        HeadState& H = s_hs[gid][tg];
+        H.ref = (float)s_eown[slot][tg];
+        H.rcp = s_rcp[slot];
+        if constexpr (V == VAR_SYS) H.ksys = s_ksys[slot][tg];
+      }
+      if (L.w) {
+        const int cpw = (nch + 31) & ~31;   // chunks per head, rounded to whole warps
+        for (int it = tg; it < G * cpw; it += nthr) {
+          const int h = it / cpw, c = it - h * cpw;
+          if (c < nch) L.w[h * L.segc + c] = chunk_mass(p, h, p.c_lo + c, s_eown[slot][h]);
+        }
+      }
+      SANTA_STAMP(22);
+      return;
+    }
+    // a piece wholly inside the range: its scores, copied while the rest is
+    // prepared; per head (warp w0 + g): the threshold constants, e_own from the
+    // chunk maxima, Z the exact sum of the chunk masses, the masses themselves
+    if (L.st) stage_scores(p, L, tg, nthr);
     SANTA_STAMP(17);
-    // threshold constants of head g by warp w0 + (G + g) % nw (lane 0); a
-    // shared piece's were computed at the start
-    for (int g = 0; g < G; ++g)
-      if (!shared && wl == (G + g) % nw && lane == 0) {
-        HeadState& H = s_hs[gid][g];
+    if (wl < G) {
+      HeadState& H = s_hs[gid][wl];
+      if (lane == 0) {
         H.rcp = (V != VAR_IID && S_b > 1) ? ~0ull / (unsigned)S_b + 1ull : 0ull;
-        H.ksys = V == VAR_SYS ? philox4x32_10(make_uint4(0u, (uint32_t)(p.kvh * G + g), (uint32_t)p.b, a.step), k0,
+        H.ksys = V == VAR_SYS ? philox4x32_10(make_uint4(0u, (uint32_t)(p.kvh * G + wl), (uint32_t)p.b, a.step), k0,
                                               k1).x >> 8
                               : 0u;
       }
-    if (!shared && wl < G) {
-      // the whole piece is this CTA's: e_own from the chunk maxima (and Z,
-      // when the chunks do not fit one segment, their exact sum)
-      HeadState& H = s_hs[gid][wl];
       float mstar = -INFINITY;
       int e_own = AGG_EMPTY;
       const int64_t bh = bh0 + wl;
@@ -966,102 +917,20 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
       mstar = warp_max(mstar);
       e_own = __reduce_max_sync(FULL, e_own);
       long long Z = 0;
-      if (nch0 < nch_part) {
-        for (int c = lane; c < p.nblk; c += 32) Z += chunk_mass(p, wl, c, e_own);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(FULL, Z, o);
+      for (int c = lane; c < p.nblk; c += 32) {
+        const long long m = chunk_mass(p, wl, c, e_own);
+        if (L.w) L.w[wl * L.segc + c] = m;
+        Z += m;
       }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(FULL, Z, o);
       if (lane == 0) {
         H.ref = (float)e_own;
         H.mstar = mstar;
         H.Z = Z;
-      }
-    }
-    SANTA_STAMP(18);
-    if (shared) {
-      // the range's part of a shared piece: each head's warp alone, its chunk
-      // masses at the published power and their prefixes (no group barrier)
-      if (tg < G) {
-        HeadState& H = s_hs[gid][tg];
-        H.ref = (float)s_eown[slot][tg];
-        H.rcp = s_rcp[slot];
-        if constexpr (V == VAR_SYS) H.ksys = s_ksys[slot][tg];
-      }
-      // wph warps per head, each a contiguous share of the chunks (one
-      // 64-bit warp scan each), their totals combined through shared memory
-      const int wph = max(1, nw / G);
-      const int hw = wl / wph, kw = wl - hw * wph;
-      long long* const w = L.w + hw * L.segc;
-      long long* const pr = L.pref + hw * (L.segc + 1);
-      int la = 0, lb = 0;
-      long long excl = 0, tot = 0;
-      if (hw < G) {
-        const int cpw = (nch0 + wph - 1) / wph;
-        const int c_a = min(nch0, kw * cpw), n = min(nch0, c_a + cpw) - c_a, run = (n + 31) >> 5;
-        la = c_a + min(n, lane * run);
-        lb = c_a + min(n, lane * run + run);
-        const int e_own = s_eown[slot][hw];
-        long long sm = 0;
-        int nz = -1;
-        for (int c = la; c < lb; ++c) {
-          const long long m = chunk_mass(p, hw, p.c_lo + c, e_own);
-          w[c] = m;
-          sm += m;
-          if (m > 0) nz = c;
-        }
-        const long long incl = warp_inclusive_scan(sm, lane);
-        excl = incl - sm;
-        tot = __shfl_sync(FULL, incl, 31);
-        nz = __reduce_max_sync(FULL, nz);
-        if (lane == 0) {
-          s_wtot[gid][hw][kw] = tot;
-          s_wnz[gid][hw][kw] = nz;
-        }
-      }
-      if (wph > 1) group_sync(bar_id, nthr);
-      if (hw < G) {
-        long long base = 0;
-        int lastnz = -1;
-        for (int k = 0; k < wph; ++k) {
-          if (k < kw) base += s_wtot[gid][hw][k];
-          lastnz = max(lastnz, s_wnz[gid][hw][k]);
-        }
-        long long x = base + excl;
-        for (int c = la; c < lb; ++c) {
-          pr[c] = x;
-          x += w[c];
-        }
-        if (kw == wph - 1 && lane == 0) {
-          s_hs[gid][hw].seg_end = base + tot;
-          s_hs[gid][hw].lastnz = lastnz;
-        }
-      }
-      SANTA_STAMP(22);
-      return;
-    }
-    if (!shared) group_sync(bar_id, nthr);   // own powers visible (a shared piece's are in s_eown)
-    // the first segment's chunk masses by the whole group, then one warp per head scans them
-    const float inv_nch0 = 1.0f / (float)nch0;
-    for (int it = tg; it < G * nch0; it += nthr) {
-      const int h = (int)(((float)it + 0.5f) * inv_nch0), c = it - h * nch0;   // it / nch0 (exact: it < 2^13)
-      L.w[h * L.segc + c] = chunk_mass(p, h, p.c_lo + c, shared ? s_eown[slot][h] : (int)s_hs[gid][h].ref);
-    }
-    group_sync(bar_id, nthr);
-    SANTA_STAMP(19);
-    if (wl < G) {
-      HeadState& H = s_hs[gid][wl];
-      int lastnz;
-      const long long end = scan_head(L, wl, nch0, 0, lastnz);
-      __syncwarp();
-      if (lane == 0) {
-        H.seg_end = end;
-        H.lastnz = lastnz;
-        if (!shared) {
-          if (nch0 == nch_part) H.Z = end;
-          H.pown = 0;
-          H.town = H.Z;
-          H.d = 0;
-        }
+        H.pown = 0;
+        H.town = Z;
+        H.d = 0;
       }
     }
     SANTA_STAMP(22);
@@ -1160,129 +1029,152 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
       const int2 jr = dr.count2(pown, none ? pown : pown + town, lane);
       SANTA_STAMP(9);
       const T* Vb = static_cast<const T*>(a.V) + (p.row0 * a.Hkv + p.kvh) * (int64_t)D + lane * CPL;
-      const long long* pr = L.pref + wl * (L.segc + 1);
       float acc[CPL];
 #pragma unroll
       for (int k = 0; k < CPL; ++k) acc[k] = 0.f;
-      long long seg_end = H.seg_end;
-      int lastnz = H.lastnz;
-      int j = jr.x;
-      for (int sg = 0; sg < L.nseg && j < jr.y; ++sg) {
-        const int c0 = p.c_lo + sg * L.segc, nch = min(L.segc, p.c_hi - c0);
-        if (sg > 0) {   // this segment's chunk prefixes, by this warp alone
-          for (int c = lane; c < nch; c += 32) L.w[wl * L.segc + c] = chunk_mass(p, wl, c0 + c, (int)ref);
-          __syncwarp();
-          seg_end = scan_head(L, wl, nch, seg_end, lastnz);
-          __syncwarp();
-        }
-        // own-unit offset x >= seg_end  <=>  theta >= pown + ceil(seg_end / 2^d)
-        int jhi = jr.y;
-        if (sg + 1 < L.nseg) {
-          const long long X = pown + (long long)(((unsigned long long)seg_end + (1ull << d) - 1ull) >> d);
-          jhi = max(j, min(jr.y, dr.count2(min(X, pown + town), 0, lane).x));
-        }
-        SANTA_STAMP(10);
-        for (int jb = j; jb < jhi; jb += 32) {
-          // ---- thresholds jb .. jb + 31, one per lane
-          const int jj = jb + lane;
-          const bool valid = jj < jhi;
-          int key = -1;
-          if (valid) {
-            const long long x = (dr.theta(jj) - pown) << d;   // own-unit offset in this range
-            int c;
-            const bool gap = x >= seg_end;   // rounding gap at the range's end: the last nonzero chunk
-            if (gap) {
-              c = lastnz;
-            } else {   // the last chunk with pref <= x (pref[0] <= x), by halving steps
-              c = 0;
+      // The range's chunks 32 at a time (lane = chunk): their own-unit masses
+      // (from the preparation when they fit in shared memory) and, by one
+      // 64-bit warp scan carried from window to window, their exact prefixes.
+      // Thresholds are non-decreasing, so a window once passed is never needed
+      // again; the last window's end is the range's total, past which a
+      // threshold (the rounding gap) takes the last chunk with nonzero mass.
+      const int nch = p.c_hi - p.c_lo, e_own = (int)ref;
+      int wc0 = 0, lastnz = -1;
+      long long wcarry = 0, m_l = 0, incl_l = 0;
+      bool win = false;
+      auto load_window = [&]() {
+        const int c = wc0 + lane;
+        m_l = c < nch ? (L.w ? L.w[wl * L.segc + c] : chunk_mass(p, wl, p.c_lo + c, e_own)) : 0ll;
+        incl_l = warp_inclusive_scan(m_l, lane) + wcarry;
+        const unsigned nzb = __ballot_sync(FULL, m_l > 0);
+        if (nzb) lastnz = wc0 + 31 - __clz((int)nzb);
+        win = true;
+      };
+      SANTA_STAMP(10);
+      for (int jb = jr.x; jb < jr.y; jb += 32) {
+        // ---- thresholds jb .. jb + 31, one per lane
+        const int jj = jb + lane;
+        const bool valid = jj < jr.y;
+        const long long x = valid ? (dr.theta(jj) - pown) << d : 0ll;   // own-unit offset in this range
+        int c = -1;
+        long long xc = 0;
+        bool pending = valid;
+        while (__any_sync(FULL, pending)) {
+          if (!win) load_window();
+          const long long wend = __shfl_sync(FULL, incl_l, 31);
+          const bool here = pending && x < wend;
+          if (__any_sync(FULL, here)) {
+            // the last lane (chunk) whose exclusive prefix is <= x, by halving
+            const long long ex_l = incl_l - m_l;
+            int Lc = 0;
 #pragma unroll
-              for (int sh = 12; sh >= 0; --sh) {
-                const int t = c + (1 << sh);
-                if (t < nch && pr[t] <= x) c = t;
-              }
+            for (int sh = 4; sh >= 0; --sh) {
+              const int t = Lc + (1 << sh);
+              const long long ex_t = __shfl_sync(FULL, ex_l, t & 31);
+              if (t < 32 && ex_t <= x) Lc = t;
             }
-            if (c < 0) {
-              key = c0 * BK;   // no mass in the range at all (never expected)
+            const long long ex_c = __shfl_sync(FULL, ex_l, Lc);
+            if (here) {
+              c = wc0 + Lc;
+              xc = x - ex_c;
+              pending = false;
+            }
+          }
+          if (__any_sync(FULL, pending)) {
+            if (wc0 + 32 >= nch) {   // past the range's total: the rounding gap
+              if (pending) {
+                c = lastnz;
+                xc = LLONG_MAX;
+                pending = false;
+              }
             } else {
-              // the first key of the chunk whose inclusive key-mass prefix
-              // exceeds x - pref[c]; past the chunk's key total, its last
-              // nonzero key
-              const long long xc = gap ? LLONG_MAX : x - pr[c];
-              const int64_t kc = (int64_t)(c0 + c) * BK;
-              const int64_t kr0 = (int64_t)p.c_lo * BK;   // the range's first key
-              const float* sc = L.st ? L.st + wl * L.capk + (int)((bh * a.nk_max + kr0) & 3) + (int)(kc - kr0)
-                                     : a.stash + bh * a.nk_max + kc;
-              float s[BK];
-              if (((reinterpret_cast<uintptr_t>(sc) & 15) == 0) && kc + BK <= p.nk) {   // four 16-byte loads
-#pragma unroll
-                for (int q4 = 0; q4 < BK / 4; ++q4) {
-                  const float4 v = reinterpret_cast<const float4*>(sc)[q4];
-                  s[4 * q4] = v.x;
-                  s[4 * q4 + 1] = v.y;
-                  s[4 * q4 + 2] = v.z;
-                  s[4 * q4 + 3] = v.w;
-                }
-              } else {
-#pragma unroll
-                for (int kk = 0; kk < BK; ++kk) s[kk] = kc + kk < p.nk ? sc[kk] : -INFINITY;
-              }
-              long long F = 0;
-              int found = -1, lastk = 0;
-#pragma unroll
-              for (int kk = 0; kk < BK; ++kk) {
-                const long long w = mass_fixed(fast_exp2(fmaf(s[kk], LOG2E, -ref)));
-                F += w;
-                lastk = w > 0 ? kk : lastk;
-                found = (found < 0 && F > xc) ? kk : found;
-              }
-              key = (int)(kc + (found >= 0 ? found : lastk));
-            }
-            if (a.sample_idx) a.sample_idx[bh * a.S_max + jj] = key;
-          }
-          SANTA_STAMP(12);
-          // ---- the distinct keys (keys are non-decreasing along the lanes)
-          //      with their counts, gathered four at a time
-          const int kprev = __shfl_up_sync(FULL, key, 1);
-          const bool start = valid && (lane == 0 || kprev != key);
-          if (start) {   // every distinct row of this pass requested at once, into L2
-            const char* row = reinterpret_cast<const char*>(Vb - lane * CPL + (int64_t)key * a.Hkv * D);
-#pragma unroll
-            for (int o = 0; o < D * 2; o += 128) prefetch_l2(row + o);
-          }
-          unsigned starts = __ballot_sync(FULL, start);
-          const int nval = __popc(__ballot_sync(FULL, valid));
-          const unsigned later = starts & ~((2u << lane) - 1u);
-          const float cnt = (float)((later ? __ffs(later) - 1 : nval) - lane);   // meaningful at run starts
-          while (starts) {   // warp-uniform
-            int src[4];
-            uint2 raw[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              src[u] = starts ? __ffs(starts) - 1 : -1;
-              starts &= starts ? starts - 1 : 0u;
-              const int kk = __shfl_sync(FULL, key, src[u] < 0 ? 0 : src[u]);
-              raw[u] = make_uint2(0u, 0u);
-              if (src[u] >= 0) {
-                const T* row = Vb + (int64_t)kk * a.Hkv * D;
-                if constexpr (CPL == 4) raw[u] = *reinterpret_cast<const uint2*>(row);
-                else raw[u].x = *reinterpret_cast<const uint32_t*>(row);
-              }
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const float c = __shfl_sync(FULL, cnt, src[u] < 0 ? 0 : src[u]);
-              f2x pr2[4];
-              Pairs<T>::get(make_uint4(raw[u].x, raw[u].y, 0u, 0u), pr2);
-              const float2 p0 = unpack2(pr2[0]), p1 = unpack2(pr2[1]);
-              const float vf[4] = {p0.x, p0.y, p1.x, p1.y};
-#pragma unroll
-              for (int k = 0; k < CPL; ++k) acc[k] = src[u] >= 0 ? fmaf(c, vf[k], acc[k]) : acc[k];
+              wcarry = wend;
+              wc0 += 32;
+              win = false;
             }
           }
-          SANTA_STAMP(13);
         }
-        j = jhi;   // the next segment's first threshold
-      }
+        int key = -1;
+        if (valid) {
+          if (c < 0) {
+            key = p.c_lo * BK;   // no mass in the range at all (never expected)
+          } else {
+            // the first key of the chunk whose inclusive key-mass prefix
+            // exceeds x - pref[c]; past the chunk's key total, its last
+            // nonzero key
+            const int64_t kc = (int64_t)(p.c_lo + c) * BK;
+            const int64_t kr0 = (int64_t)p.c_lo * BK;   // the range's first key
+            const float* sc = L.st ? L.st + wl * L.capk + (int)((bh * a.nk_max + kr0) & 3) + (int)(kc - kr0)
+                                   : a.stash + bh * a.nk_max + kc;
+            float s[BK];
+            if (((reinterpret_cast<uintptr_t>(sc) & 15) == 0) && kc + BK <= p.nk) {   // four 16-byte loads
+#pragma unroll
+              for (int q4 = 0; q4 < BK / 4; ++q4) {
+                const float4 v = reinterpret_cast<const float4*>(sc)[q4];
+                s[4 * q4] = v.x;
+                s[4 * q4 + 1] = v.y;
+                s[4 * q4 + 2] = v.z;
+                s[4 * q4 + 3] = v.w;
+              }
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < BK; ++kk) s[kk] = kc + kk < p.nk ? sc[kk] : -INFINITY;
+            }
+            long long F = 0;
+            int found = -1, lastk = 0;
+#pragma unroll
+            for (int kk = 0; kk < BK; ++kk) {
+              const long long w = mass_fixed(fast_exp2(fmaf(s[kk], LOG2E, -ref)));
+              F += w;
+              lastk = w > 0 ? kk : lastk;
+              found = (found < 0 && F > xc) ? kk : found;
+            }
+            key = (int)(kc + (found >= 0 ? found : lastk));
+          }
+          if (a.sample_idx) a.sample_idx[bh * a.S_max + jj] = key;
+        }
+        SANTA_STAMP(12);
+        // ---- the distinct keys (keys are non-decreasing along the lanes)
+        //      with their counts, gathered four at a time
+        const int kprev = __shfl_up_sync(FULL, key, 1);
+        const bool start = valid && (lane == 0 || kprev != key);
+        if (start) {   // every distinct row of this pass requested at once, into L2
+          const char* row = reinterpret_cast<const char*>(Vb - lane * CPL + (int64_t)key * a.Hkv * D);
+#pragma unroll
+          for (int o = 0; o < D * 2; o += 128) prefetch_l2(row + o);
+        }
+        unsigned starts = __ballot_sync(FULL, start);
+        const int nval = __popc(__ballot_sync(FULL, valid));
+        const unsigned later = starts & ~((2u << lane) - 1u);
+        const float cnt = (float)((later ? __ffs(later) - 1 : nval) - lane);   // meaningful at run starts
+        while (starts) {   // warp-uniform
+          int src[4];
+          uint2 raw[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            src[u] = starts ? __ffs(starts) - 1 : -1;
+            starts &= starts ? starts - 1 : 0u;
+            const int kk = __shfl_sync(FULL, key, src[u] < 0 ? 0 : src[u]);
+            raw[u] = make_uint2(0u, 0u);
+            if (src[u] >= 0) {
+              const T* row = Vb + (int64_t)kk * a.Hkv * D;
+              if constexpr (CPL == 4) raw[u] = *reinterpret_cast<const uint2*>(row);
+              else raw[u].x = *reinterpret_cast<const uint32_t*>(row);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float c = __shfl_sync(FULL, cnt, src[u] < 0 ? 0 : src[u]);
+            f2x pr2[4];
+            Pairs<T>::get(make_uint4(raw[u].x, raw[u].y, 0u, 0u), pr2);
+            const float2 p0 = unpack2(pr2[0]), p1 = unpack2(pr2[1]);
+            const float vf[4] = {p0.x, p0.y, p1.x, p1.y};
+#pragma unroll
+            for (int k = 0; k < CPL; ++k) acc[k] = src[u] >= 0 ? fmaf(c, vf[k], acc[k]) : acc[k];
+          }
+        }
+        SANTA_STAMP(13);
+        }
       // ---- the head's sums, times 1/S_b, into out
       const float inv_S = 1.0f / (float)S_b;
       float* o = a.out + bh * D + lane * CPL;
