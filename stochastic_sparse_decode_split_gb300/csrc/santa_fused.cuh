@@ -1024,6 +1024,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
         town = H.town;
         if (lane == 0) a.head_max[bh] = H.mstar;
       }
+      SANTA_STAMP(19);
       dr.tc = theta_ctx_rcp(Z, V == VAR_IID ? 1u : (unsigned)S_b, H.rcp);
       const bool none = town == 0 || d > 61;   // no threshold falls in this range
       const int2 jr = dr.count2(pown, none ? pown : pown + town, lane);
@@ -1056,6 +1057,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
         const int jj = jb + lane;
         const bool valid = jj < jr.y;
         const long long x = valid ? (dr.theta(jj) - pown) << d : 0ll;   // own-unit offset in this range
+        SANTA_STAMP(18);
         int c = -1;
         long long xc = 0;
         bool pending = valid;
@@ -1094,6 +1096,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
             }
           }
         }
+        SANTA_STAMP(11);
         int key = -1;
         if (valid) {
           if (c < 0) {

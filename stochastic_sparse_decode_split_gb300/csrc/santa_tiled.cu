@@ -33,8 +33,9 @@ namespace santa {
 constexpr int TB_THREADS = 256;   // budget and merge kernels
 constexpr int TB_SMEM_T = 4096;   // tiles whose fractional parts the budget kernel keeps in shared memory
 constexpr int TB_RANK_T = 256;    // up to this many tiles the leftover samples are placed by ranking
-constexpr int TS_THREADS = 256;   // sampler kernel
-constexpr int TS_WARPS = TS_THREADS / 32;
+constexpr int TF_THREADS = 1024;  // budget and merge kernels, fast path
+constexpr int TF_KC = 8;          // statistics chunks per thread on the fast path
+constexpr int TF_T = TF_THREADS;  // tiles per head on the fast path
 
 __device__ __forceinline__ int64_t seq_rows(const LaunchArgs& a, int b, int64_t& row0) {
   if (a.kv_offsets) {
@@ -102,6 +103,67 @@ __device__ double tile_masses(const LaunchArgs& a, int64_t bh, int64_t nk, int T
     zloc += w[t];
   }
   return block_reduce<TB_THREADS>(zloc, OpAdd(), red);
+}
+
+// Reduction over a CTA of TF_THREADS threads (every thread gets the result,
+// the same in each: a fixed butterfly order); red holds 32 values.
+template <typename V_, typename Op>
+__device__ __forceinline__ V_ block_reduce_1k(V_ v, Op op, V_* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(FULL, v, o));
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  v = red[lane];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(FULL, v, o));
+  return v;
+}
+
+// The fast path's tile statistics (TF_THREADS threads, every load in flight
+// at once): tiles of C chunks, C a power of two <= 32, at most TF_KC *
+// TF_THREADS chunks and TF_T tiles.  Thread i takes chunks i + TF_THREADS k,
+// so a tile's C chunks sit on C neighbouring lanes and combine by shuffles:
+// m_t the max of the chunk maxima, l_t = sum_c sum_c-chunk * exp(max_c - m_t),
+// into sm_m[t], sm_l[t].
+__device__ __forceinline__ void tile_stats_fast(const LaunchArgs& a, int64_t bh, int nch, int C, int T, float* sm_m,
+                                                float* sm_l) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const float* mx = a.tile_max + bh * a.chunks_max;
+  const float* sm = a.tile_sum + bh * a.chunks_max;
+  float vm[TF_KC], vs[TF_KC];
+#pragma unroll
+  for (int k = 0; k < TF_KC; ++k) {
+    const int c = k * TF_THREADS + tid;
+    vm[k] = c < nch ? mx[c] : -INFINITY;
+    vs[k] = c < nch ? sm[c] : 0.f;
+  }
+#pragma unroll
+  for (int k = 0; k < TF_KC; ++k) {
+    if (k * TF_THREADS >= nch) break;   // uniform over the CTA
+    float m = vm[k];
+    for (int o = 1; o < C; o <<= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
+    float l = vm[k] > -INFINITY ? vs[k] * expf(vm[k] - m) : 0.f;
+    for (int o = 1; o < C; o <<= 1) l += __shfl_xor_sync(FULL, l, o);
+    const int c = k * TF_THREADS + tid;
+    if ((lane & (C - 1)) == 0 && c / C < T) {
+      sm_m[c / C] = m;
+      sm_l[c / C] = l;
+    }
+  }
+}
+
+// W = e * l (e in [0, 1], l in [1, 2^10]: an exp factor and a tile's sum) as
+// an integer in units of 2^-40, exactly (the 48-bit product of the two
+// mantissas, shifted; truncated below 2^-40).
+__device__ __forceinline__ unsigned long long weight_fixed(float e, float l) {
+  const uint32_t be = __float_as_uint(e), bl = __float_as_uint(l);
+  const int xe = (int)((be >> 23) & 0xffu), xl = (int)((bl >> 23) & 0xffu);
+  if (xe == 0 || xl == 0 || xe == 0xff || xl == 0xff || ((be | bl) >> 31)) return 0ull;
+  const unsigned long long prod =
+      (unsigned long long)((be & 0x7fffffu) | 0x800000u) * (unsigned long long)((bl & 0x7fffffu) | 0x800000u);
+  const int sh = (xe - 150) + (xl - 150) + 40;   // e l 2^40 = prod 2^sh
+  return sh >= 0 ? prod << min(sh, 15) : (sh > -64 ? prod >> -sh : 0ull);
 }
 
 // ---------------------------------------------------------------------------
@@ -213,6 +275,111 @@ __global__ void __launch_bounds__(TB_THREADS) tiled_budget_kernel(LaunchArgs a) 
   if (tid == 0) pre[T] = run;
 }
 
+// The same budgets on the fast path (one CTA of TF_THREADS threads per head,
+// thread t = tile t), with no float64 (its pipe is narrow on this part): the
+// statistics with every load in flight; W_t = exp(m_t - m*) l_t as an exact
+// 2^-40 integer and Z their integer sum, so that S W_t = S_t Z + r_t by one
+// integer division gives the floor S_t and the fractional part r_t / Z, and
+// the fractional parts rank as the remainders r_t (one denominator); the
+// leftover samples by a parallel ranking (several threads per tile, up to
+// TB_RANK_T tiles) or a bitonic sort of the remainders.
+__global__ void __launch_bounds__(TF_THREADS) tiled_budget_fast_kernel(LaunchArgs a) {
+  const int64_t bh = blockIdx.x;
+  const int b = (int)(bh / a.H);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ float s_m[TF_T], s_l[TF_T];
+  __shared__ unsigned long long s_key[TF_T];
+  __shared__ int s_bud[TF_T];
+  __shared__ unsigned long long s_redz[32];
+  __shared__ float s_redf[32];
+  __shared__ int s_redi[32], s_wsum[32];
+  int S_b;
+  if (seq_error(a, b, S_b)) return;   // flagged by the merge kernel
+  int64_t row0;
+  const int64_t nk = seq_rows(a, b, row0);
+  const int T = (int)((nk + a.tl_len - 1) / a.tl_len);
+  const int nch = (int)((nk + SUB - 1) / SUB);
+  int32_t* pre = a.tl_pre + bh * (a.tl_T + 1);
+  tile_stats_fast(a, bh, nch, a.tl_len / SUB, T, s_m, s_l);
+  __syncthreads();
+  const float mt = tid < T ? s_m[tid] : -INFINITY;
+  const float mstar = block_reduce_1k(mt, OpMax(), s_redf);
+  const unsigned long long W = (tid < T && mt > -INFINITY) ? weight_fixed(expf(mt - mstar), s_l[tid]) : 0ull;
+  const unsigned long long Z = block_reduce_1k(W, OpAdd(), s_redz);
+  int fl = 0;
+  if (tid < T) {
+    const unsigned long long SW = (unsigned long long)S_b * W;   // < 2^62: W < 2^50, S_b < 2^12
+    const unsigned long long f = Z ? SW / Z : 0ull;
+    fl = (int)f;
+    s_bud[tid] = fl;
+    s_key[tid] = SW - f * Z;   // the fractional part's numerator over Z
+  }
+  const int R = S_b - block_reduce_1k(fl, OpAdd(), s_redi);
+  __syncthreads();   // every key and floor written
+  if (T <= TB_RANK_T) {
+    // tile tt gets one more sample when fewer than R tiles rank above it;
+    // tpt threads per tile each compare every tpt-th key
+    int T2 = 1;
+    while (T2 < T) T2 <<= 1;
+    const int tpt = min(32, TF_THREADS / T2);
+    const int tt = tid / tpt, j = tid & (tpt - 1);
+    int above = 0;
+    if (tt < T) {
+      const unsigned long long kt = s_key[tt];
+      for (int u = j; u < T; u += tpt) {
+        const unsigned long long ku = s_key[u];
+        above += (ku > kt || (ku == kt && u < tt)) ? 1 : 0;
+      }
+    }
+    for (int o = 1; o < tpt; o <<= 1) above += __shfl_xor_sync(FULL, above, o);
+    if (j == 0 && tt < T && above < R) s_bud[tt] += 1;
+  } else {
+    // as the general kernel: keys keep the remainder's bits above the lowest
+    // 12 and take 4095 - t in those 12 (remainders equal to 2^-48 of Z go to
+    // the lower tile); a bitonic network sorts them in decreasing order and
+    // the first R tiles get one more sample
+    int T2 = 1;
+    while (T2 < T) T2 <<= 1;
+    if (tid < T2) s_key[tid] = tid < T ? ((s_key[tid] & ~0xFFFull) | (unsigned long long)(4095 - tid)) : 0ull;
+    __syncthreads();
+    for (int k = 2; k <= T2; k <<= 1)
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        const int l = tid ^ j;
+        if (tid < T2 && l > tid) {
+          const unsigned long long x = s_key[tid], y = s_key[l];
+          const bool desc = (tid & k) == 0;
+          if (desc ? x < y : x > y) {
+            s_key[tid] = y;
+            s_key[l] = x;
+          }
+        }
+        __syncthreads();
+      }
+    if (tid < R) s_bud[4095 - (int)(s_key[tid] & 0xFFFull)] += 1;
+  }
+  __syncthreads();
+  // exclusive prefix of the budgets (one per thread), then the total
+  const int v = tid < T ? s_bud[tid] : 0;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(FULL, x, o);
+    if (lane >= o) x += n;
+  }
+  if (lane == 31) s_wsum[warp] = x;
+  __syncthreads();
+  const int y = s_wsum[lane];
+  int yi = y;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(FULL, yi, o);
+    if (lane >= o) yi += n;
+  }
+  const int before = __shfl_sync(FULL, yi - y, warp), total = __shfl_sync(FULL, yi, 31);
+  if (tid < T) pre[tid] = before + x - v;
+  if (tid == 0) pre[T] = total;
+}
+
 // ---------------------------------------------------------------------------
 // Per-tile systematic counts and the count-weighted gather (App. O, Alg. 5;
 // App. P, Alg. 7).  One CTA per (tile, sequence, KV head): each head
@@ -244,20 +411,21 @@ __device__ __forceinline__ void load_cols(const T* src, float (&v)[CPL]) {
   }
 }
 
-// Dynamic shared memory of tiled_sample_kernel for tiles of `len` keys.
+// Dynamic shared memory of tiled_sample_kernel for tiles of `len` keys (GM
+// warps: one per head of the group).
 template <int D, int GM>
 __host__ __device__ constexpr size_t tiled_sample_smem(int len) {
-  return (size_t)GM * len * 8 + (size_t)GM * len * 4 + (size_t)GM * len * 4 + (size_t)TS_WARPS * GM * D * 4;
+  return (size_t)GM * len * 8 + (size_t)GM * len * 4 + (size_t)GM * GM * D * 4;
 }
 
 template <typename T, int D, int GM>
-__global__ void __launch_bounds__(TS_THREADS) tiled_sample_kernel(LaunchArgs a) {
+__global__ void __launch_bounds__(32 * GM, 32 / GM) tiled_sample_kernel(LaunchArgs a) {
+  constexpr int TS_WARPS = GM, TS_THREADS = 32 * GM;
   extern __shared__ __align__(16) unsigned char smem[];
   const int Lt = a.tl_len;
   long long* Fall = reinterpret_cast<long long*>(smem);             // [GM][Lt] inclusive mass prefix per head
   int* cnt = reinterpret_cast<int*>(Fall + (size_t)GM * Lt);          // [GM][Lt] counts
-  float* sco = reinterpret_cast<float*>(cnt + (size_t)GM * Lt);       // [GM][Lt] the tile's scores per head
-  float* part = sco + (size_t)GM * Lt;                                // [TS_WARPS][GM][D] per-warp sums
+  float* part = reinterpret_cast<float*>(cnt + (size_t)GM * Lt);     // [TS_WARPS][GM][D] per-warp sums
   __shared__ int rows[TL_MAX_LEN];
   __shared__ int red_i[TS_WARPS];
   constexpr int CPL = D / 32;   // output columns per lane
@@ -283,36 +451,50 @@ __global__ void __launch_bounds__(TS_THREADS) tiled_sample_kernel(LaunchArgs a) 
   __syncthreads();
 
   // one warp per head of the group: tile max, fixed-point masses
-  // 2^((s_n - m_t) log2 e) with their inclusive prefix (32 keys a round),
-  // then the head's S_t thresholds
+  // 2^((s_n - m_t) log2 e) with their inclusive prefix, then the head's S_t
+  // thresholds.  Keys n = lane + 32 i, eight rounds i at a time in
+  // registers: their loads at once (with the budget's), eight interleaved
+  // warp scans, the rounds' sums carried in order
+  constexpr int RG = 8;
   for (int g = warp; g < G; g += TS_WARPS) {
     const int h = kvh * G + g;
     const int64_t bh = (int64_t)b * a.H + h;
     const int32_t* pre = a.tl_pre + bh * (a.tl_T + 1);
-    const int St = a.tl_sampler == 0 ? pre[t + 1] - pre[t] : S_tile;
-    if (St <= 0) continue;   // uniform over the warp
     const float* st = a.stash + bh * a.nk_max + k0;
+    const int St = a.tl_sampler == 0 ? pre[t + 1] - pre[t] : S_tile;
+    float v[RG];
+#pragma unroll
+    for (int i = 0; i < RG; ++i) v[i] = lane + 32 * i < len ? st[lane + 32 * i] : -INFINITY;
+    if (St <= 0) continue;   // uniform over the warp
     long long* F = Fall + (size_t)g * Lt;
-    float* sc = sco + (size_t)g * Lt;
     float m = -INFINITY;
-#pragma unroll 8
-    for (int n = lane; n < len; n += 32) {   // one round of loads, kept in shared memory
-      const float v = st[n];
-      sc[n] = v;
-      m = fmaxf(m, v);
-    }
+    for (int n = lane + 32 * RG; n < len; n += 32) m = fmaxf(m, st[n]);   // tiles past 32 RG keys
+#pragma unroll
+    for (int i = 0; i < RG; ++i) m = fmaxf(m, v[i]);
     m = warp_max(m);
     long long carry = 0;
-    for (int n0 = 0; n0 < len; n0 += 32) {
-      const int n = n0 + lane;
-      long long x = n < len ? mass_fixed(fast_exp2((sc[n] - m) * LOG2E)) : 0;
+    for (int r0 = 0; r0 < len; r0 += 32 * RG) {
+      long long x[RG];
+#pragma unroll
+      for (int i = 0; i < RG; ++i) {
+        const int n = r0 + lane + 32 * i;
+        if (r0 > 0) v[i] = n < len ? st[n] : -INFINITY;
+        x[i] = n < len ? mass_fixed(fast_exp2((v[i] - m) * LOG2E)) : 0ll;
+      }
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const long long y = __shfl_up_sync(FULL, x, o);
-        if (lane >= o) x += y;
+#pragma unroll
+        for (int i = 0; i < RG; ++i) {
+          const long long y = __shfl_up_sync(FULL, x[i], o);
+          if (lane >= o) x[i] += y;
+        }
       }
-      if (n < len) F[n] = carry + x;
-      carry += __shfl_sync(FULL, x, 31);
+#pragma unroll
+      for (int i = 0; i < RG; ++i) {
+        const int n = r0 + lane + 32 * i;
+        if (n < len) F[n] = carry + x[i];
+        carry += __shfl_sync(FULL, x[i], 31);
+      }
     }
     __syncwarp();   // F visible to the warp
     const long long L = carry;
@@ -469,6 +651,79 @@ __global__ void __launch_bounds__(TB_THREADS) tiled_merge_kernel(LaunchArgs a) {
   }
 }
 
+// The merge on the fast path (one CTA of TF_THREADS threads per head): the
+// tiles' weights as above (flash: from the fast tile statistics), then thread
+// (c, j) sums column c over tiles j, j + NJ, ... with all its loads in flight
+// (NJ = TF_THREADS / D), and the NJ partial sums are added in a fixed order.
+template <int D>
+__global__ void __launch_bounds__(TF_THREADS) tiled_merge_fast_kernel(LaunchArgs a) {
+  const int64_t bh = blockIdx.x;
+  const int b = (int)(bh / a.H), h = (int)(bh % a.H);
+  const int tid = threadIdx.x;
+  __shared__ float s_m[TF_T], s_w[TF_T];
+  __shared__ float s_part[TF_THREADS];
+  __shared__ unsigned long long s_redz[32];
+  __shared__ float s_redf[32];
+  int S_b;
+  const int e = seq_error(a, b, S_b);
+  if (e) {
+    if (tid == 0 && h == 0) flag_error(a.err, e);
+    for (int c = tid; c < D; c += TF_THREADS) a.out[bh * D + c] = 0.f;
+    if (a.sample_idx)
+      for (int j = tid; j < a.tl_draws; j += TF_THREADS) a.sample_idx[bh * a.tl_draws + j] = -1;
+    return;
+  }
+  int64_t row0;
+  const int64_t nk = seq_rows(a, b, row0);
+  const int T = (int)((nk + a.tl_len - 1) / a.tl_len);
+  const int S_tile = flash_tile_budget(S_b, T);
+  if (a.tl_sampler == 1) {
+    tile_stats_fast(a, bh, (int)((nk + SUB - 1) / SUB), a.tl_len / SUB, T, s_m, s_w);
+    __syncthreads();
+    const float mt = tid < T ? s_m[tid] : -INFINITY;
+    const float mstar = block_reduce_1k(mt, OpMax(), s_redf);
+    const unsigned long long W = (tid < T && mt > -INFINITY) ? weight_fixed(expf(mt - mstar), s_w[tid]) : 0ull;
+    const unsigned long long Z = block_reduce_1k(W, OpAdd(), s_redz);
+    // W_t / (Z S_tile) in fp32 (both in units of 2^-40)
+    const float inv = 1.f / ((float)Z * (float)S_tile);
+    __syncthreads();   // every s_w read
+    if (tid < T) s_w[tid] = (float)W * inv;
+  } else if (tid < T) {
+    const int32_t* pre = a.tl_pre + bh * (a.tl_T + 1);
+    s_w[tid] = pre[tid + 1] > pre[tid] ? 1.f / (float)S_b : 0.f;
+  }
+  __syncthreads();
+  constexpr int NJ = TF_THREADS / D, U = 16;
+  const float* o = a.tl_o + bh * a.tl_T * D;
+  {
+    const int c = tid % D, j = tid / D;
+    float sum = 0.f;
+    for (int t0 = j; t0 < T; t0 += U * NJ) {
+      float v[U], wt[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int t = t0 + u * NJ;
+        wt[u] = t < T ? s_w[t] : 0.f;
+        v[u] = (t < T && wt[u] != 0.f) ? o[(int64_t)t * D + c] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) sum = fmaf(wt[u], v[u], sum);
+    }
+    s_part[tid] = sum;
+  }
+  __syncthreads();
+  if (tid < D) {
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) sum += s_part[j * D + tid];
+    a.out[bh * D + tid] = sum;
+  }
+  if (a.sample_idx) {
+    const int used = a.tl_sampler == 0 ? S_b : T * S_tile;
+    for (int j = used + tid; j < a.tl_draws; j += TF_THREADS) a.sample_idx[bh * a.tl_draws + j] = -1;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // launcher
 // ---------------------------------------------------------------------------
@@ -478,25 +733,36 @@ static cudaError_t launch_tiled_g(const LaunchArgs& a) {
   cudaError_t e = cudaFuncSetAttribute(tiled_sample_kernel<T, D, GM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)tiled_sample_smem<D, GM>(TL_MAX_LEN));
   if (e != cudaSuccess) return e;
+  // one wave of samplers needs about seven CTAs per SM: all of its shared memory
+  e = cudaFuncSetAttribute(tiled_sample_kernel<T, D, GM>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
   const unsigned heads = (unsigned)((int64_t)a.B * a.H);
+  // the fast budget and merge kernels: tiles of a power-of-two number of
+  // chunks (at most 32), at most TF_T tiles and TF_KC * TF_THREADS chunks
+  const int C = a.tl_len / SUB;
+  const bool fast = (C & (C - 1)) == 0 && C <= 32 && a.tl_T <= TF_T && a.chunks_max <= TF_KC * TF_THREADS;
   // plain stream order (launching the next kernel early with programmatic
   // dependent launch was measured slower: its waiting CTAs hold SM slots)
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(TB_THREADS);
+  cfg.blockDim = dim3(fast ? TF_THREADS : TB_THREADS);
   cfg.stream = a.stream;
   if (a.tl_sampler == 0) {
     cfg.gridDim = dim3(heads);
     cfg.dynamicSmemBytes = 0;
-    if ((e = cudaLaunchKernelEx(&cfg, tiled_budget_kernel, a)) != cudaSuccess) return e;
+    if ((e = fast ? cudaLaunchKernelEx(&cfg, tiled_budget_fast_kernel, a)
+                  : cudaLaunchKernelEx(&cfg, tiled_budget_kernel, a)) != cudaSuccess)
+      return e;
   }
   cfg.gridDim = dim3((unsigned)((unsigned long long)a.tl_T * a.B * a.Hkv));
-  cfg.blockDim = dim3(TS_THREADS);
+  cfg.blockDim = dim3(32 * GM);
   cfg.dynamicSmemBytes = smem;
   if ((e = cudaLaunchKernelEx(&cfg, tiled_sample_kernel<T, D, GM>, a)) != cudaSuccess) return e;
   cfg.gridDim = dim3(heads);
-  cfg.blockDim = dim3(TB_THREADS);
+  cfg.blockDim = dim3(fast ? TF_THREADS : TB_THREADS);
   cfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&cfg, tiled_merge_kernel<D>, a);
+  return fast ? cudaLaunchKernelEx(&cfg, tiled_merge_fast_kernel<D>, a)
+              : cudaLaunchKernelEx(&cfg, tiled_merge_kernel<D>, a);
 }
 
 template <typename T, int D>

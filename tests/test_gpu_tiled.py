@@ -146,6 +146,8 @@ def test_tiny(sampler, tile_len):
     ("bf16_tile1024", 1, 8, 8, 128, 5000, "bf16", 300, 1024),
     ("few_samples", 1, 4, 1, 64, 4000, "bf16", 8, 32),   # prop: most tiles get no sample
     ("many_tiles", 1, 4, 1, 64, 8192, "bf16", 300, 16),  # 512 tiles: prop sorts the fractional parts
+    ("tile48", 1, 4, 1, 64, 3000, "bf16", 100, 48),      # 3 chunks per tile: the general budget and merge
+    ("tiles_2048", 1, 4, 1, 64, 32768, "bf16", 600, 16),  # 2048 tiles: past the fast path's 1024
 ])
 def test_parity(sampler, case):
     name, B, H, Hkv, d, nk, dtype, S, L = case
