@@ -1039,10 +1039,43 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
       // Thresholds are non-decreasing, so a window once passed is never needed
       // again; the last window's end is the range's total, past which a
       // threshold (the rounding gap) takes the last chunk with nonzero mass.
+      // A range of more than one window whose masses are in shared memory
+      // instead turns them into inclusive prefixes in place (four windows at
+      // a time, interleaved scans) and each lane bisects them.
       const int nch = p.c_hi - p.c_lo, e_own = (int)ref;
       int wc0 = 0, lastnz = -1;
       long long wcarry = 0, m_l = 0, incl_l = 0;
       bool win = false;
+      const bool bis = L.w != nullptr && nch > 32;
+      long long* const wrow = L.w ? L.w + wl * L.segc : nullptr;
+      if (bis) {
+        long long carry = 0;
+        for (int c0 = 0; c0 < nch; c0 += 128) {
+          long long v4[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int c = c0 + 32 * u + lane;
+            v4[u] = c < nch ? wrow[c] : 0ll;
+            const unsigned nzb = __ballot_sync(FULL, v4[u] > 0);
+            if (nzb) lastnz = c0 + 32 * u + 31 - __clz((int)nzb);
+          }
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const long long y = __shfl_up_sync(FULL, v4[u], o);
+              if (lane >= o) v4[u] += y;
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int c = c0 + 32 * u + lane;
+            if (c < nch) wrow[c] = v4[u] + carry;
+            carry += __shfl_sync(FULL, v4[u], 31);
+          }
+        }
+        __syncwarp();   // the prefixes visible to the warp
+      }
       auto load_window = [&]() {
         const int c = wc0 + lane;
         m_l = c < nch ? (L.w ? L.w[wl * L.segc + c] : chunk_mass(p, wl, p.c_lo + c, e_own)) : 0ll;
@@ -1061,7 +1094,23 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
         int c = -1;
         long long xc = 0;
         bool pending = valid;
-        while (__any_sync(FULL, pending)) {
+        if (bis && valid) {   // the first chunk whose inclusive prefix exceeds x
+          int lo2 = 0, hi2 = nch;
+          while (lo2 < hi2) {
+            const int mid = (lo2 + hi2) >> 1;
+            if (wrow[mid] > x) hi2 = mid;
+            else lo2 = mid + 1;
+          }
+          if (lo2 < nch) {
+            c = lo2;
+            xc = x - (lo2 ? wrow[lo2 - 1] : 0ll);
+          } else {   // past the range's total: the rounding gap
+            c = lastnz;
+            xc = LLONG_MAX;
+          }
+          pending = false;
+        }
+        while (!bis && __any_sync(FULL, pending)) {
           if (!win) load_window();
           const long long wend = __shfl_sync(FULL, incl_l, 31);
           const bool here = pending && x < wend;
