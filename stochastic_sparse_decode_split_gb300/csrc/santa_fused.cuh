@@ -349,6 +349,9 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
   __shared__ Cur s_cur[2];                            // blocks lo and hi - 1 (ragged batches)
   __shared__ long long s_part[2];                     // T, q (ragged batches)
   __shared__ HeadState s_hs[3][8];                    // per phase-B group and head
+  __shared__ float s_pm[FW];                          // pieces inside the range: per-warp partial max,
+  __shared__ int s_pe[FW];                            // exponent
+  __shared__ long long s_pz[FW];                      // and mass sum
   __shared__ float2 s_stats[STATS_CAP];               // the range's 16-key (max, exp-sum), when they fit
   __shared__ unsigned s_gen;
   __shared__ CtaRange s_rg;
@@ -843,27 +846,30 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
   // Chunk c of head g of piece p (a chunk of this range) as an aggregate:
   // exponent e_c and mass relative to 2^e_c, from its 16-key statistics
   // (kept in shared memory during the stream when the range's chunks fit)
-  auto chunk_agg = [&](const Piece& p, int g, int c) {
-    if (use_ss) {
-      const float2 st = s_stats[(int)(p.pb_lo + c - lo) * G + g];
-      return make_agg(st.x, st.y);
-    }
+  auto chunk_stats = [&](const Piece& p, int g, int c) {
+    if (use_ss) return s_stats[(int)(p.pb_lo + c - lo) * G + g];
     const int64_t gi2 = ((int64_t)p.b * a.H + (int64_t)p.kvh * G + g) * a.chunks_max + c;
-    return make_agg(a.tile_max[gi2], a.tile_sum[gi2]);
+    return make_float2(a.tile_max[gi2], a.tile_sum[gi2]);
   };
-  // Own-unit mass of chunk c of head g of piece p: its mass relative to
-  // 2^e_c shifted to the CTA's power 2^e_own (e_own >= e_c), as T_k of an aggregate.
-  auto chunk_mass = [&](const Piece& p, int g, int c, int e_own) {
-    const Agg x = chunk_agg(p, g, c);
+  auto chunk_agg = [&](const Piece& p, int g, int c) {
+    const float2 st = chunk_stats(p, g, c);
+    return make_agg(st.x, st.y);
+  };
+  // Own-unit mass of a chunk with statistics st: its mass relative to 2^e_c
+  // shifted to the CTA's power 2^e_own (e_own >= e_c), as T_k of an aggregate.
+  auto stats_mass = [&](float2 st, int e_own) {
+    const Agg x = make_agg(st.x, st.y);
     const int dd = e_own - x.e;
     return dd < 63 ? (x.F >> dd) : 0ll;
   };
+  // the same for chunk c of head g of piece p
+  auto chunk_mass = [&](const Piece& p, int g, int c, int e_own) { return stats_mass(chunk_stats(p, g, c), e_own); };
 
   // Preparation of one piece by one group of nw warps (warps w0 .. w0 + nw -
   // 1; named barrier bar_id) in region reg, needing nothing from other CTAs:
   // per head (warp w0 + g) the own power e_own, the threshold constants
-  // (budget reciprocal, systematic key), the own-unit chunk prefixes of the
-  // first segment (masses by the whole group) and, for a piece wholly inside
+  // (budget reciprocal, systematic key), the own-unit chunk masses when they
+  // fit in the region (by the whole group) and, for a piece wholly inside
   // this range, Z; and the range's scores staged when they fit.  Not
   // synchronised at the end.
   auto prep_piece = [&](const Piece& p, const SegLayout& L, bool shared, int slot, int gid, int bar_id, int w0,
@@ -872,7 +878,6 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
     int S_b;
     if (seq_error(a, p.b, S_b)) return;
     SANTA_STAMP(16);
-    const int64_t bh0 = (int64_t)p.b * a.H + (int64_t)p.kvh * G;
     const int nch = p.c_hi - p.c_lo;
     if (shared) {
       // the range's part of a shared piece: its heads' constants, and its
@@ -895,43 +900,71 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tmap, LaunchArgs a, unsi
       return;
     }
     // a piece wholly inside the range: its scores, copied while the rest is
-    // prepared; per head (warp w0 + g): the threshold constants, e_own from the
-    // chunk maxima, Z the exact sum of the chunk masses, the masses themselves
+    // prepared; per head: the threshold constants (lane 0 of warp w0 + g);
+    // by wph = nw / G warps per head, each a stride of the chunks with its
+    // loads in flight, combined through shared memory: the max score, e_own
+    // the max of the chunks' exponents, then the chunk masses at 2^e_own and
+    // Z their exact sum
     if (L.st) stage_scores(p, L, tg, nthr);
     SANTA_STAMP(17);
-    if (wl < G) {
+    if (wl < G && lane == 0) {
       HeadState& H = s_hs[gid][wl];
-      if (lane == 0) {
-        H.rcp = (V != VAR_IID && S_b > 1) ? ~0ull / (unsigned)S_b + 1ull : 0ull;
-        H.ksys = V == VAR_SYS ? philox4x32_10(make_uint4(0u, (uint32_t)(p.kvh * G + wl), (uint32_t)p.b, a.step), k0,
-                                              k1).x >> 8
-                              : 0u;
+      H.rcp = (V != VAR_IID && S_b > 1) ? ~0ull / (unsigned)S_b + 1ull : 0ull;
+      H.ksys = V == VAR_SYS ? philox4x32_10(make_uint4(0u, (uint32_t)(p.kvh * G + wl), (uint32_t)p.b, a.step), k0,
+                                            k1).x >> 8
+                            : 0u;
+    }
+    const int wph = nw / G, hh = wl / wph, sub = wl - hh * wph;
+    const bool mine = hh < G;   // warps past G * wph sit the passes out
+    float mloc = -INFINITY;
+    int eloc = AGG_EMPTY;
+    if (mine) {
+#pragma unroll 8
+      for (int c = sub * 32 + lane; c < nch; c += wph * 32) {
+        const float m = chunk_stats(p, hh, c).x;
+        mloc = fmaxf(mloc, m);
+        eloc = max(eloc, m > -INFINITY ? (int)ceilf(m * LOG2E) : AGG_EMPTY);
       }
-      float mstar = -INFINITY;
-      int e_own = AGG_EMPTY;
-      const int64_t bh = bh0 + wl;
-      for (int c = lane; c < p.nblk; c += 32) {
-        mstar = fmaxf(mstar, use_ss ? s_stats[(int)(p.pb_lo + c - lo) * G + wl].x : a.tile_max[bh * a.chunks_max + c]);
-        e_own = max(e_own, chunk_agg(p, wl, c).e);
-      }
-      mstar = warp_max(mstar);
-      e_own = __reduce_max_sync(FULL, e_own);
-      long long Z = 0;
-      for (int c = lane; c < p.nblk; c += 32) {
-        const long long m = chunk_mass(p, wl, c, e_own);
-        if (L.w) L.w[wl * L.segc + c] = m;
+    }
+    mloc = warp_max(mloc);
+    eloc = __reduce_max_sync(FULL, eloc);
+    if (lane == 0) {
+      s_pm[wl] = mloc;
+      s_pe[wl] = eloc;
+    }
+    group_sync(bar_id, nthr);
+    int e_own = AGG_EMPTY;
+    if (mine)
+      for (int k = 0; k < wph; ++k) e_own = max(e_own, s_pe[hh * wph + k]);
+    long long Z = 0;
+    if (mine) {
+#pragma unroll 8
+      for (int c = sub * 32 + lane; c < nch; c += wph * 32) {
+        const long long m = stats_mass(chunk_stats(p, hh, c), e_own);
+        if (L.w) L.w[hh * L.segc + c] = m;
         Z += m;
       }
+    }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(FULL, Z, o);
-      if (lane == 0) {
-        H.ref = (float)e_own;
-        H.mstar = mstar;
-        H.Z = Z;
-        H.pown = 0;
-        H.town = Z;
-        H.d = 0;
+    for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(FULL, Z, o);
+    if (lane == 0) s_pz[wl] = Z;
+    group_sync(bar_id, nthr);
+    if (tg < G) {
+      HeadState& H = s_hs[gid][tg];
+      float mstar = -INFINITY;
+      long long Zh = 0;
+      int eh = AGG_EMPTY;
+      for (int k = 0; k < wph; ++k) {
+        mstar = fmaxf(mstar, s_pm[tg * wph + k]);
+        Zh += s_pz[tg * wph + k];
+        eh = max(eh, s_pe[tg * wph + k]);
       }
+      H.ref = (float)eh;
+      H.mstar = mstar;
+      H.Z = Zh;
+      H.pown = 0;
+      H.town = Zh;
+      H.d = 0;
     }
     SANTA_STAMP(22);
   };
