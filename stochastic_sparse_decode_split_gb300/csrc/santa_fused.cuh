@@ -278,35 +278,63 @@ struct SegLayout {
 
 // ---------------------------------------------------------------------------
 // i.i.d.: sorted 24-bit uniform keys of one head into ukeys (all threads of
-// the CTA).  Up to 1024 keys are placed by rank (each thread counts the keys
-// below its own: one barrier), more by a bitonic network in `keys`.
+// the CTA).  Up to 2048 keys: each key becomes the unique composite
+// (key << 12) | index, each warp sorts a run of 32 composites by a bitonic
+// network over its lanes, and a composite's rank is its place in its own run
+// plus, for every other run, the number of that run's composites below it (a
+// bisection of 32 sorted values): the order of the keys with equal keys by
+// index, as a stable sort gives.  More keys: a bitonic network over the keys
+// in shared memory.  `keys` holds at least 2048 composites.
 // ---------------------------------------------------------------------------
 static __device__ __noinline__ void sort_head_keys(int b, int h, int S_b, uint32_t step, uint32_t k0, uint32_t k1,
                                                   uint32_t* dst, uint32_t* keys) {
-  const int tid = threadIdx.x;
-  int S2 = 1;
-  while (S2 < S_b) S2 <<= 1;
-  for (int i = tid; i < S2; i += FT) {
-    uint32_t k = 0xffffffffu;
-    if (i < S_b) {
-      const uint4 w = philox4x32_10(make_uint4((uint32_t)(i >> 2), (uint32_t)h, (uint32_t)b, step), k0, k1);
-      const uint32_t x = (i & 3) == 0 ? w.x : (i & 3) == 1 ? w.y : (i & 3) == 2 ? w.z : w.w;
-      k = x >> 8;
+  const int tid = threadIdx.x, lane = tid & 31;
+  auto key_of = [&](int i) {
+    const uint4 w = philox4x32_10(make_uint4((uint32_t)(i >> 2), (uint32_t)h, (uint32_t)b, step), k0, k1);
+    const uint32_t x = (i & 3) == 0 ? w.x : (i & 3) == 1 ? w.y : (i & 3) == 2 ? w.z : w.w;
+    return x >> 8;
+  };
+  if (S_b <= 2048) {
+    unsigned long long* ck = reinterpret_cast<unsigned long long*>(keys);
+    const int nrun = (S_b + 31) >> 5;
+    for (int i = tid; i < nrun * 32; i += FT) {   // whole warps: lane = place in the run
+      unsigned long long c = i < S_b ? ((unsigned long long)key_of(i) << 12) | (unsigned)i : ~0ull;
+#pragma unroll
+      for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+          const unsigned long long o = __shfl_xor_sync(FULL, c, j);
+          const bool up = (lane & k) == 0, low = (lane & j) == 0;
+          c = (up == low) ? (c < o ? c : o) : (c < o ? o : c);
+        }
+      ck[i] = c;
     }
-    keys[i] = k;
-  }
-  __syncthreads();
-  if (S_b <= 1024) {
+    __syncthreads();
     for (int i = tid; i < S_b; i += FT) {
-      const uint32_t ki = keys[i];
-      int rank = 0;
-      for (int u = 0; u < S_b; ++u) {
-        const uint32_t ku = keys[u];
-        rank += (ku < ki || (ku == ki && u < i)) ? 1 : 0;
+      const unsigned long long c = ck[i];
+      if (c == ~0ull) continue;
+      const int r = i >> 5;
+      int rank = i & 31;
+      for (int q = 0; q < nrun; ++q) {
+        if (q == r) continue;
+        const unsigned long long* run = ck + 32 * q;
+        int n = 0;   // composites of run q below c
+        if (run[31] < c) {
+          n = 32;
+        } else {
+#pragma unroll
+          for (int half = 16; half > 0; half >>= 1)
+            if (run[n + half - 1] < c) n += half;
+        }
+        rank += n;
       }
-      dst[rank] = ki;
+      dst[rank] = (uint32_t)(c >> 12);
     }
   } else {
+    int S2 = 1;
+    while (S2 < S_b) S2 <<= 1;
+    for (int i = tid; i < S2; i += FT) keys[i] = i < S_b ? key_of(i) : 0xffffffffu;
+    __syncthreads();
     for (int kk = 2; kk <= S2; kk <<= 1) {
       for (int jj = kk >> 1; jj > 0; jj >>= 1) {
         for (int i = tid; i < S2; i += FT) {
