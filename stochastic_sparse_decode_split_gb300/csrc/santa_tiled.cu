@@ -502,12 +502,20 @@ __global__ void __launch_bounds__(32 * GM, 32 / GM) tiled_sample_kernel(LaunchAr
     const uint4 r4 = philox4x32_10(make_uint4((uint32_t)(t >> 2), (uint32_t)h, (uint32_t)b, a.step), s0, s1);
     const uint32_t a24 = ((t & 3) == 0 ? r4.x : (t & 3) == 1 ? r4.y : (t & 3) == 2 ? r4.z : r4.w) >> 8;
     const int pos0 = a.tl_sampler == 0 ? pre[t] : t * S_tile;
+    // ceil(2^64 / St), once per head: top < 2^62 (N <= 2^36, L <= 2^50), so
+    // the multiply-high below is floor(top / St) or one more
+    const unsigned long long rcpSt = St > 1 ? ~0ull / (unsigned)St + 1ull : 0ull;
     for (int k = 1 + lane; k <= St; k += 32) {
       // theta = ceil(N L / (St 2^24)), N = k 2^24 - a24 <= St 2^24, in 128 bits
       const unsigned long long N = ((unsigned long long)k << 24) - a24;
       const unsigned long long lo = N * (unsigned long long)L, hi = __umul64hi(N, (unsigned long long)L);
       const unsigned long long top = (hi << 40) | (lo >> 24);   // floor(N L / 2^24) < 2^64
-      const unsigned long long Q = top / (unsigned)St, Rm = top - Q * (unsigned)St;
+      unsigned long long Q = top;
+      if (St > 1) {
+        Q = __umul64hi(top, rcpSt);
+        if (Q * (unsigned)St > top) --Q;
+      }
+      const unsigned long long Rm = top - Q * (unsigned)St;
       const long long theta = (long long)(Q + ((Rm | (lo & 0xffffffull)) ? 1ull : 0ull));
       int l0 = 0, l1 = len - 1;   // the first key with F >= theta (F[len - 1] = L >= theta)
       while (l0 < l1) {
