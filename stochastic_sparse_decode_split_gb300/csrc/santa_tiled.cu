@@ -695,6 +695,18 @@ __global__ void __launch_bounds__(TF_THREADS) tiled_merge_fast_kernel(LaunchArgs
   const int64_t nk = seq_rows(a, b, row0);
   const int T = (int)((nk + a.tl_len - 1) / a.tl_len);
   const int S_tile = flash_tile_budget(S_b, T);
+  // thread (c, j): column c, tiles j, j + NJ, ...; its first U partials are
+  // requested now, in flight while the weights are formed (a tile without a
+  // budget holds zeros)
+  constexpr int NJ = TF_THREADS / D, U = 16;
+  const float* o = a.tl_o + bh * a.tl_T * D;
+  const int c = tid % D, j = tid / D;
+  float v0[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int t = j + u * NJ;
+    v0[u] = t < T ? o[(int64_t)t * D + c] : 0.f;
+  }
   if (a.tl_sampler == 1) {
     tile_stats_fast(a, bh, (int)((nk + SUB - 1) / SUB), a.tl_len / SUB, T, s_m, s_w);
     __syncthreads();
@@ -711,12 +723,14 @@ __global__ void __launch_bounds__(TF_THREADS) tiled_merge_fast_kernel(LaunchArgs
     s_w[tid] = pre[tid + 1] > pre[tid] ? 1.f / (float)S_b : 0.f;
   }
   __syncthreads();
-  constexpr int NJ = TF_THREADS / D, U = 16;
-  const float* o = a.tl_o + bh * a.tl_T * D;
   {
-    const int c = tid % D, j = tid / D;
     float sum = 0.f;
-    for (int t0 = j; t0 < T; t0 += U * NJ) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int t = j + u * NJ;
+      sum = fmaf(t < T ? s_w[t] : 0.f, v0[u], sum);
+    }
+    for (int t0 = j + U * NJ; t0 < T; t0 += U * NJ) {   // more than U NJ tiles
       float v[U], wt[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
