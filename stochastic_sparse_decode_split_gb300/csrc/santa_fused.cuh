@@ -29,17 +29,20 @@
 // and a threshold maps into the CTA's units exactly by a shift.  So all that
 // needs the other CTAs comes last: a CTA publishes one aggregate per head of
 // the (at most two) pieces it shares (max, and the mass in its own units),
-// arrives at the one grid barrier, and while it waits stages its chunk
-// statistics and scores in shared memory and forms the exact chunk prefixes
-// in its own units.  After the barrier one warp per head reads the covering
-// CTAs' aggregates (about 20 at a 32K context), which give E*, the head's
-// total mass Z and the prefix and mass of this CTA's range; places the
-// thresholds that fall in the range; and resolves them one per lane (chunk by
-// binary search over the prefixes, key by the chunk's 16 key masses).  The
-// group's warps then gather the drawn V rows, each distinct row once for every
-// head of the KV group, into shared-memory sums that go to out.  A piece
-// wholly inside one range needs no other CTA and is done before the wait; the
-// two shared pieces of a CTA run on two halves of the CTA at once.
+// arrives at the one grid barrier, and while it waits stages its scores in
+// shared memory and computes its chunk masses in its own units.  After the
+// barrier one warp per head reads the covering CTAs' aggregates (about 20 at
+// a 32K context), which give E*, the head's total mass Z and the prefix and
+// mass of this CTA's range; places the thresholds that fall in the range; and
+// resolves them one per lane: the chunk by a halving search over one 32-chunk
+// window's prefixes (a warp scan), window after window, or, in a longer range,
+// by bisection over prefixes formed in place first; the key by the chunk's 16
+// key masses.  The head warps then gather their drawn V rows, each distinct
+// row of a head once with its count, at the same time, so a row drawn by
+// several heads of the KV group is read from memory once and served to the
+// others from L2.  A piece wholly inside one range needs no other CTA and is
+// done before the wait by all warps; the two shared pieces of a CTA run on two
+// halves of the CTA at once.
 //
 // Difference from the pages' kernels: Alg. 4 rounds per-tile budgets by
 // largest remainder and samples each tile on its own; here the S thresholds of
