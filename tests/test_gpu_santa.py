@@ -172,6 +172,9 @@ GRID = [
     (3, 10, 2, 64, 777, "fp32", 33, "stratified"),      # group 5
     (2, 15, 3, 128, 1800, "bf16", 128, "systematic"),   # 3 KV heads: units of one head, group 5
     (1, 12, 6, 64, 2500, "fp16", 64, "iid"),            # 6 KV heads: units of two heads, group 2
+    (1, 2, 1, 64, 90000, "bf16", 256, "systematic"),    # ~37 blocks per CTA: prefixes in place, bisection
+    (1, 2, 1, 64, 90000, "fp16", 128, "iid"),
+    (256, 4, 1, 64, 256, "bf16", 32, "stratified"),     # pieces of 16 blocks wholly inside ranges of ~27
 ]
 
 
